@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP32 GEMM C = A x B on GB300, one JSON line on rank 0.
+
+Workload: M = N = K = 4096, row-major FP32, A and B uniform on [-1, 1) from the
+seeds 1004 / 2004 (the compute-bound headline shape). One step = one call of
+the product kernel over the whole product. Inputs are resident in HBM when the
+timed region starts; the L2 cache (129 MB) is flushed by writing a 256 MB buffer
+before every timed step, outside the timed interval; each step is timed with CUDA
+events on the stream the kernel is launched on.
+
+`--impl reference` times the CPU oracle (the deliberately plain C triple loop) on
+a bounded row sample of the same workload on the host cores instead.
+
+Under torchrun (WORLD_SIZE > 1) every rank runs an independent replica of the
+workload on its own GPU (no collective on the data path); the time is the max
+over ranks and the value counts the work of all ranks ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "FP32 GEMM TFLOP/s at 1024³/4096³ and % of GB300 FP32 roofline (1 GPU)"
+UNIT = "TFLOP/s"
+WORKLOAD = dict(M=4096, N=4096, K=4096, config_no=4)
+L2_FLUSH_BYTES = 256 << 20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FFMA_PROFILE = os.path.join(ROOT, "profiles", "sgemm_ffma_4096.md")
+TF32X3_PROFILE = os.path.join(ROOT, "profiles", "gemm_tf32x3_4096.md")
+KERNEL_SOURCES = {
+    "ffma": ["sgemm_ffma.cu", "t2s_device.cuh"],
+    "tf32x3": ["gemm_tf32x3.cu", "t2s_device.cuh"],
+}
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return ws, rank, local
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def kernel_hash(kind: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "roofline_driven_tiling_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(path: str, kind: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (the summary records the source hash); else None."""
+    if not os.path.exists(path):
+        return None
+    text = open(path, encoding="utf-8").read()
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_hash(kind):
+        return None
+    return float(m_bytes.group(1))
+
+
+def measured_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms (background)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        if shutil.which("nvidia-smi"):
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, flag in zip(names, parts[5:9]):
+                    if flag.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- CPU leg
+def cpu_oracle_rate(A, B, target_s: float):
+    """Times the oracle on a bounded row sample of C = A x B; returns (TFLOP/s, info)."""
+    import oracle  # test infrastructure, used here only as the CPU baseline
+    M, K = A.shape
+    N = B.shape[1]
+    t0 = time.perf_counter()
+    oracle.sgemm_rows(A, B, 0, 1, oracle.MUL_ADD)  # one row to calibrate
+    per_row = max(time.perf_counter() - t0, 1e-4)
+    rows = int(min(M, max(2, target_s / per_row)))
+    t0 = time.perf_counter()
+    oracle.sgemm_rows(A, B, 0, rows, oracle.MUL_ADD)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * N * K
+    info = {"cores": oracle.num_threads(), "rows": rows, "seconds": dt,
+            "sample": "rows 0..%d of the %dx%dx%d product (%d outputs, each a %d-term FP32 "
+                      "dot product, two roundings per term)" % (rows - 1, M, N, K, rows * N, K)}
+    return flops / dt / 1e12, info
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from roofline_driven_tiling_gb300 import inputs
+    import oracle
+    oracle.build()
+    w = WORKLOAD
+    A, B = inputs.uniform_pair(w["M"], w["N"], w["K"], w["config_no"])
+    per_step = float(os.environ.get("T2S_REF_STEP_SECONDS", "4"))
+    for _ in range(args.warmup):
+        cpu_oracle_rate(A, B, min(per_step, 1.0))
+    rates, infos = [], []
+    for _ in range(args.steps):
+        r, info = cpu_oracle_rate(A, B, per_step)
+        rates.append(r)
+        infos.append(info)
+    value = statistics.mean(rates)
+    ms = statistics.mean(i["seconds"] for i in infos) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": infos[0]["cores"],
+                         "kind": "oracle", "sample": infos[0]["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block():
+    w = WORKLOAD
+    return {"workload": "sgemm %dx%dx%d fp32 row-major, A,B uniform[-1,1) seeds %d/%d"
+                        % (w["M"], w["N"], w["K"], 1000 + w["config_no"], 2000 + w["config_no"]),
+            "M": w["M"], "N": w["N"], "K": w["K"], "layout": "row-major dense",
+            "kernel": "t2s_gemm_f32 (FFMA2, TMA + mbarrier pipeline)",
+            "l2": "flushed (256 MB write) before every timed step"}
+
+
+# --------------------------------------------------------------------------- GPU leg
+def time_steps(fn, steps, warmup, stream, flush_buf):
+    """Runs fn() warmup times, then `steps` timed times with an L2 flush before each;
+    returns per-step milliseconds measured by CUDA events on `stream`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for s, e in ev:
+            flush_buf.add_(1)  # 256 MB read + write: evicts A, B and C from L2
+            s.record(stream)
+            fn()
+            e.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return [s.elapsed_time(e) for s, e in ev]
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from roofline_driven_tiling_gb300 import binding, inputs
+    from roofline_driven_tiling_gb300 import roofline as rl
+
+    w = WORKLOAD
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B = inputs.uniform_pair(M, N, K, w["config_no"])
+    dA = torch.from_numpy(A).to(dev)
+    dB = torch.from_numpy(B).to(dev)
+    dC = torch.empty((M, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev).zero_()
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+    lib = binding.lib()
+
+    def step():
+        rc = lib.t2s_gemm_f32(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sp)
+        if rc != 0:
+            raise binding.T2SError(rc, "t2s_gemm_f32")
+
+    flops = rl.gemm_flops(M, N, K)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        times = time_steps(step, args.steps, max(args.warmup, 3), stream, flush)
+    clocks = clk.summary()
+    if binding.t2s_device_status(sp) != binding.T2S_OK:
+        raise RuntimeError("device status reports a timed-out wait")
+    t_total = reduce_max(sum(times) / 1e3, device=dev if ws > 1 else None)
+    ms_per_step = t_total / args.steps * 1e3
+    value = flops * args.steps * ws / t_total / 1e12
+    avg_launch_s = sum(times) / len(times) / 1e3
+
+    peaks = measured_peaks()
+    bw = float(peaks.get("hbm_gbs", 6800.0))
+    fp32_peak = rl.fp32_peak_tflops()
+    achieved = flops / avg_launch_s / 1e12
+    roof = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": UNIT,
+            "frac": achieved / fp32_peak,
+            "traffic": profile_traffic(FFMA_PROFILE, "ffma"),
+            "peak_basis": "152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz (unit counts and max clock)",
+            "algorithmic_flops_per_launch": flops,
+            "algorithmic_bytes_per_launch": rl.gemm_bytes(M, N, K),
+            "ai_algorithmic": rl.gemm_ai(M, N, K),
+            "ridge_ai": rl.ridge_ai(fp32_peak, bw / 1e3),
+            "hbm_gbs_measured": bw}
+    if clocks and clocks.get("sm_mhz"):
+        at_clock = rl.fp32_peak_tflops(mhz=clocks["sm_mhz"])
+        roof["peak_at_observed_clock"] = at_clock
+        roof["frac_at_observed_clock"] = achieved / at_clock
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        step()
+        hC.copy_(dC, non_blocking=True)
+
+    e2e_times = time_steps(e2e_step, max(1, min(args.steps, 10)), 2, stream, flush)
+    e2e_t = reduce_max(sum(e2e_times) / 1e3, device=dev if ws > 1 else None)
+    e2e_value = flops * len(e2e_times) * ws / e2e_t / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(),
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * 4 * M * K,
+                "d2h_bytes_per_step": 4 * M * N},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+
+    # ---- reported separately: 3xTF32 tensor-core kernel and the 1024^3 shape
+    if not args.skip_extras:
+        line["tf32x3"] = extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws)
+        line["also_1024"] = extra_1024(lib, dev, stream, flush, args, ws)
+
+    if rank == 0 and ws == 1 and not args.skip_cpu:
+        rate, info = cpu_oracle_rate(A, B, float(os.environ.get("T2S_CPU_SECONDS", "12")))
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": info["cores"],
+                                "kind": "oracle", "sample": info["sample"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws):
+    import torch
+    from roofline_driven_tiling_gb300 import binding
+    from roofline_driven_tiling_gb300 import roofline as rl
+    need = lib.t2s_gemm_f32_tf32x3_workspace_size(M, N, K)
+    wsbuf = torch.empty(need, dtype=torch.uint8, device=dev)
+    dC = torch.empty((M, N), dtype=torch.float32, device=dev)
+    sp = stream.cuda_stream
+
+    def step():
+        rc = lib.t2s_gemm_f32_tf32x3(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
+                                     wsbuf.data_ptr(), need, sp)
+        if rc != 0:
+            raise binding.T2SError(rc, "t2s_gemm_f32_tf32x3")
+
+    try:
+        times = time_steps(step, args.steps, max(args.warmup, 3), stream, flush)
+    except binding.T2SError as e:
+        return {"unavailable": str(e)}
+    flops = rl.gemm_flops(M, N, K)
+    t = sum(times) / len(times) / 1e3
+    peaks = measured_peaks()
+    # TF32 dense peak: the measured bf16 burst figure x the nominal tf32 : bf16 ratio (1.1 : 2.25).
+    tf32_peak = float(peaks.get("bf16_tflops", 1898.5)) * 1.1 / 2.25
+    return {"value": flops / t / 1e12, "unit": UNIT, "ms_per_step": t * 1e3,
+            "kernel": "t2s_gemm_f32_tf32x3 (split pre-pass + tcgen05 kind::tf32, 3 MMAs)",
+            "roofline": {"bound": "tensor", "achieved_effective": flops / t / 1e12,
+                         "tensor_flops_per_launch": 3 * flops,
+                         "achieved_tensor": 3 * flops / t / 1e12, "peak": tf32_peak,
+                         "frac": 3 * flops / t / 1e12 / tf32_peak, "unit": UNIT,
+                         "peak_basis": "measured bf16 burst x 1.1/2.25 (nominal tf32:bf16)",
+                         "traffic": profile_traffic(TF32X3_PROFILE, "tf32x3")}}
+
+
+def extra_1024(lib, dev, stream, flush, args, ws):
+    import torch
+    from roofline_driven_tiling_gb300 import inputs
+    from roofline_driven_tiling_gb300 import roofline as rl
+    n = 1024
+    A, B = inputs.integer_pattern(n, n, n)
+    dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+    dC = torch.empty((n, n), dtype=torch.float32, device=dev)
+    sp = stream.cuda_stream
+    out = {"workload": "sgemm 1024^3 fp32, integer pattern (L2 flushed per step)"}
+    for name, fn in (("ffma", lib.t2s_gemm_f32), ("naive", lib.t2s_gemm_f32_naive),
+                     ("smem32", lib.t2s_gemm_f32_smem32)):
+        times = time_steps(lambda: fn(n, n, n, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sp),
+                           max(args.steps, 10), 3, stream, flush)
+        t = sum(times) / len(times) / 1e3
+        out[name] = {"ms": t * 1e3, "tflops": rl.gemm_flops(n, n, n) / t / 1e12,
+                     "frac_fp32_peak": rl.gemm_flops(n, n, n) / t / 1e12 / rl.fp32_peak_tflops()}
+    return out
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--skip-cpu", action="store_true", help="omit the CPU oracle baseline")
+    p.add_argument("--skip-extras", action="store_true", help="omit tf32x3 and 1024^3 lines")
+    args = p.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

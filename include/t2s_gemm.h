@@ -1,0 +1,159 @@
+/*
+ * t2s_gemm.h -- C ABI of the GB300 (sm_103a) FP32 matrix-multiply library.
+ *
+ * Operation (all entry points): C = A x B in IEEE binary32, row-major, dense.
+ *
+ *   A is M x K, element (row, k)   at A[row * K + k]
+ *   B is K x N, element (k, col)   at B[k * N + col]
+ *   C is M x N, element (row, col) at C[row * N + col]
+ *   2 * M * N * K floating-point operations.
+ *
+ * The layout and index formulas are those of page "GEMM 커널 테스트 코드 작성 및
+ * 최적화 (1024^3 크기 실험)", section "메모리 레이아웃"; the per-element operation
+ * (one FP32 accumulator per C element, k ascending) is that of its section
+ * "Naive GEMM 커널 동작 방식". As on that page, there are no leading dimensions,
+ * no alpha/beta scaling and no transposes: the three matrices are dense.
+ *
+ * Common contract of the GEMM entry points
+ * ----------------------------------------
+ *  - A, B, C are DEVICE pointers to memory the caller owns (for example from
+ *    torch or cudaMalloc) on the current CUDA device. The library keeps no
+ *    reference to them after the call returns.
+ *  - The call is asynchronous: it validates the arguments on the host,
+ *    enqueues kernels on `stream` and returns. `stream` is a cudaStream_t
+ *    (NULL = the legacy default stream). Results are visible after the
+ *    stream is synchronised.
+ *  - A and B must not overlap C (the pages' kernels declare all three
+ *    __restrict__). Pointer equality of C with A or B is rejected; partial
+ *    overlap is undefined behaviour and not detected.
+ *  - Pointers must be 4-byte aligned. No other alignment is required; when
+ *    K % 4 == 0, N % 4 == 0 and all three pointers are 16-byte aligned the
+ *    product kernel loads tiles with the Tensor Memory Accelerator, otherwise
+ *    with 4-byte asynchronous copies. Both give identical results.
+ *  - M == 0 or N == 0: nothing to do, returns T2S_OK without touching memory.
+ *    K == 0: C is set to +0.0f (the empty sum).
+ *  - Each dimension must be <= T2S_MAX_DIM. A pointer may be NULL only if the
+ *    matrix it points to has no elements.
+ *  - No entry point allocates device or host memory, except that the first
+ *    call on a device looks up the address of the library's device status
+ *    word (a static device variable; no allocation).
+ *
+ * Return codes
+ *  - T2S_OK:            the kernels were enqueued.
+ *  - T2S_ERR_INVALID:   an argument broke the contract; nothing was enqueued.
+ *  - T2S_ERR_CUDA:      a CUDA runtime or driver call failed (for example no
+ *                       sm_103a device, or a launch error); the CUDA error code
+ *                       is available from t2s_last_cuda_error().
+ *  - T2S_ERR_WORKSPACE: the workspace passed to t2s_gemm_f32_tf32x3 is NULL
+ *                       or smaller than t2s_gemm_f32_tf32x3_workspace_size().
+ *  - T2S_ERR_TIMEOUT:   only from t2s_device_status(): a kernel gave up a
+ *                       bounded wait on a pipeline barrier (it records this
+ *                       in the device status word and returns instead of
+ *                       hanging).
+ */
+#ifndef T2S_GEMM_H
+#define T2S_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header needs no CUDA header. */
+typedef struct CUstream_st *t2s_stream_t;
+
+#define T2S_OK 0
+#define T2S_ERR_INVALID 1
+#define T2S_ERR_CUDA 2
+#define T2S_ERR_TIMEOUT 3
+#define T2S_ERR_WORKSPACE 4
+
+#define T2S_MAX_DIM ((int64_t)1 << 30) /* per dimension */
+
+/*
+ * The product kernel. FP32 fused multiply-adds on the CUDA cores (packed
+ * two-wide, one rounding each), one accumulator per C element summed in
+ * ascending k, CTA tiles staged through shared memory by a multi-stage
+ * barrier pipeline. Because every step is an IEEE fused multiply-add taken in
+ * the page's order, the result is bit-identical to the definition evaluated
+ * with fmaf() (page "GEMM 커널 테스트 코드 작성 및 최적화 (1024^3 크기 실험)",
+ * section "Naive GEMM 커널 동작 방식" read with nvcc's default contraction), for
+ * every input. The tiling follows page "4주차: Roofline과 Tiling", section
+ * "3. Tiling": each tile of A and B is read from HBM once per CTA tile and
+ * reused from shared memory and registers.
+ */
+int t2s_gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
+                 float *C, t2s_stream_t stream);
+
+/*
+ * Comparison point: one thread per C element, k loop over global memory,
+ * 16 x 16 thread blocks (page "GEMM 커널 테스트 코드 작성 및 최적화 (1024^3 크기
+ * 실험)", sections "Naive GEMM 커널 동작 방식" and "쓰레드 매핑"). Uses fmaf, so
+ * its result is bit-identical to t2s_gemm_f32.
+ */
+int t2s_gemm_f32_naive(int64_t M, int64_t N, int64_t K, const float *A,
+                       const float *B, float *C, t2s_stream_t stream);
+
+/*
+ * Comparison point: 32 x 32 shared-memory tiles, one C element per thread,
+ * zero-filled ragged edges, two block barriers per K tile (same page, sections
+ * "Shared Memory Tiled GEMM 연산 방식", "타일 개념", "타일 로딩 단계"). Uses
+ * fmaf, so its result is bit-identical to t2s_gemm_f32.
+ */
+int t2s_gemm_f32_smem32(int64_t M, int64_t N, int64_t K, const float *A,
+                        const float *B, float *C, t2s_stream_t stream);
+
+/*
+ * Tensor-core variant: error-compensated 3xTF32 on tcgen05 tensor cores with
+ * TMEM accumulators. Each operand x is split into big = tf32(x) and
+ * small = tf32(x - big); C accumulates small*big + big*small + big*big in FP32.
+ * This is not on the pages (the split is from Ootomo and Yokota, "Recovering
+ * single precision accuracy from Tensor Cores while surpassing the FP32
+ * theoretical peak performance", 2022). The result is not bit-identical to the
+ * FP32 definition (the tensor core fixes its own summation order); it meets
+ * max |C - C_fp32| <= 1e-6 * K * max|a| * max|b|, and it is exact wherever
+ * every FP32 product and partial sum is exact (for example small integers).
+ *
+ * `workspace` is a DEVICE buffer of at least
+ * t2s_gemm_f32_tf32x3_workspace_size(M, N, K) bytes, owned by the caller,
+ * that holds the split operands; it must not overlap A, B or C and must stay
+ * untouched until the stream has run the call. Returns T2S_ERR_WORKSPACE if it
+ * is NULL or too small.
+ */
+size_t t2s_gemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K);
+int t2s_gemm_f32_tf32x3(int64_t M, int64_t N, int64_t K, const float *A,
+                        const float *B, float *C, void *workspace,
+                        size_t workspace_bytes, t2s_stream_t stream);
+
+/* Static description of a return code. Never NULL. */
+const char *t2s_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the status word of the current
+ * device. Returns T2S_OK, T2S_ERR_TIMEOUT if a kernel since the last read gave
+ * up a bounded barrier wait, or T2S_ERR_CUDA if synchronising or reading failed.
+ */
+int t2s_device_status(t2s_stream_t stream);
+
+/* The last CUDA error code seen by a failing call on this host thread (0 if none). */
+int t2s_last_cuda_error(void);
+
+/*
+ * Self-test of the bounded-wait mechanism: launches one block that waits on a
+ * barrier nothing will ever complete, with a limit of `limit_ns` nanoseconds
+ * (clamped to [1e3, 1e9]). The kernel records T2S_ERR_TIMEOUT in the status
+ * word and returns; t2s_device_status() then reports it. Returns T2S_OK if
+ * the kernel was enqueued.
+ */
+int t2s_selftest_wait_timeout(int64_t limit_ns, t2s_stream_t stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int t2s_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* T2S_GEMM_H */

@@ -1,0 +1,169 @@
+"""ctypes binding of libt2s_gemm.so: the C ABI of include/t2s_gemm.h under the same names.
+
+Argument marshalling only. Every step of the multiply runs in the CUDA library;
+there is no fallback of any kind. If the library is missing the import of a
+function raises, naming the build step.
+
+The ``gemm`` helper takes torch CUDA tensors (row-major, contiguous, float32),
+passes their device pointers and the current torch stream, and raises on any
+non-zero status. ``t2s_*`` functions take raw integers (pointers as ints, the
+stream as the integer value of a cudaStream_t).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libt2s_gemm.so")
+
+T2S_OK = 0
+T2S_ERR_INVALID = 1
+T2S_ERR_CUDA = 2
+T2S_ERR_TIMEOUT = 3
+T2S_ERR_WORKSPACE = 4
+T2S_MAX_DIM = 1 << 30
+
+#: Every function the header declares, with (argtypes, restype).
+_i64, _p, _i, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "t2s_gemm_f32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
+    "t2s_gemm_f32_naive": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
+    "t2s_gemm_f32_smem32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
+    "t2s_gemm_f32_tf32x3_workspace_size": ([_i64, _i64, _i64], _sz),
+    "t2s_gemm_f32_tf32x3": ([_i64, _i64, _i64, _p, _p, _p, _p, _sz, _p], _i),
+    "t2s_status_string": ([_i], ctypes.c_char_p),
+    "t2s_device_status": ([_p], _i),
+    "t2s_last_cuda_error": ([], _i),
+    "t2s_selftest_wait_timeout": ([_i64, _p], _i),
+    "t2s_version": ([], _i),
+}
+
+_lib = None
+
+
+class T2SError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = "%s failed: %s" % (what, status_string(status))
+        if status == T2S_ERR_CUDA:
+            msg += " (cudaError %d)" % lib().t2s_last_cuda_error()
+        super().__init__(msg)
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libt2s_gemm.so is not built: run "
+                              "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            f = getattr(l, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = l
+    return _lib
+
+
+# ---- the C ABI, same names ------------------------------------------------------------
+def t2s_gemm_f32(M, N, K, A, B, C, stream=0) -> int:
+    return lib().t2s_gemm_f32(M, N, K, A, B, C, stream)
+
+
+def t2s_gemm_f32_naive(M, N, K, A, B, C, stream=0) -> int:
+    return lib().t2s_gemm_f32_naive(M, N, K, A, B, C, stream)
+
+
+def t2s_gemm_f32_smem32(M, N, K, A, B, C, stream=0) -> int:
+    return lib().t2s_gemm_f32_smem32(M, N, K, A, B, C, stream)
+
+
+def t2s_gemm_f32_tf32x3_workspace_size(M, N, K) -> int:
+    return lib().t2s_gemm_f32_tf32x3_workspace_size(M, N, K)
+
+
+def t2s_gemm_f32_tf32x3(M, N, K, A, B, C, workspace, workspace_bytes, stream=0) -> int:
+    return lib().t2s_gemm_f32_tf32x3(M, N, K, A, B, C, workspace, workspace_bytes, stream)
+
+
+def t2s_status_string(status: int) -> str:
+    return lib().t2s_status_string(status).decode()
+
+
+def t2s_device_status(stream=0) -> int:
+    return lib().t2s_device_status(stream)
+
+
+def t2s_last_cuda_error() -> int:
+    return lib().t2s_last_cuda_error()
+
+
+def t2s_selftest_wait_timeout(limit_ns: int, stream=0) -> int:
+    return lib().t2s_selftest_wait_timeout(limit_ns, stream)
+
+
+def t2s_version() -> int:
+    return lib().t2s_version()
+
+
+status_string = t2s_status_string
+
+# ---- torch convenience ----------------------------------------------------------------
+KERNELS = {
+    "ffma": "t2s_gemm_f32",
+    "naive": "t2s_gemm_f32_naive",
+    "smem32": "t2s_gemm_f32_smem32",
+    "tf32x3": "t2s_gemm_f32_tf32x3",
+}
+
+
+def _check(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+        raise TypeError("%s must be a float32 CUDA tensor" % name)
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous 2-D (row-major) tensor" % name)
+
+
+def gemm(A, B, out=None, kernel: str = "ffma", workspace=None, stream=None):
+    """C = A @ B through the library (torch tensors in, torch tensor out).
+
+    `kernel` is one of "ffma" (the product), "naive", "smem32", "tf32x3". For
+    "tf32x3" a workspace tensor is allocated here (by torch) unless one is passed.
+    """
+    import torch
+    _check(A, "A")
+    _check(B, "B")
+    if A.shape[1] != B.shape[0]:
+        raise ValueError("shape mismatch: A %s, B %s" % (tuple(A.shape), tuple(B.shape)))
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _check(out, "out")
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be %d x %d" % (M, N))
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device).cuda_stream
+    fn = getattr(lib(), KERNELS[kernel])
+    if kernel == "tf32x3":
+        need = t2s_gemm_f32_tf32x3_workspace_size(M, N, K)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
+        rc = fn(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(), workspace.data_ptr(),
+                workspace.numel() * workspace.element_size(), stream)
+    else:
+        rc = fn(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(), stream)
+    if rc != T2S_OK:
+        raise T2SError(rc, KERNELS[kernel])
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    return t2s_device_status(stream)

@@ -1,0 +1,196 @@
+// api.cu -- the C ABI of include/t2s_gemm.h: argument checks, dispatch to the
+// kernels, the device status word, and the bounded-wait self-test.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "t2s_device.cuh"
+#include "t2s_internal.h"
+
+namespace t2s {
+namespace {
+
+// Bounded waits that give up record T2S_ERR_TIMEOUT here (one word per device;
+// a static device variable, so nothing is allocated). Host code must not pass
+// the symbol itself to a kernel: its device address is looked up per device.
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_status_ptr[kMaxDevices] = {};
+thread_local int g_last_cuda_error = 0;
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return T2S_ERR_CUDA;
+}
+
+// Device address of the status word on the current device, looked up once per device.
+cudaError_t status_word(unsigned** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+bool misaligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; }
+
+// Checks the common contract; on success fills `p` and returns T2S_OK. `*noop` is set
+// when there is nothing to compute (M == 0 or N == 0).
+int prepare(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+            t2s_stream_t stream, Problem* p, bool* noop) {
+  if (M < 0 || N < 0 || K < 0) return T2S_ERR_INVALID;
+  if (M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return T2S_ERR_INVALID;
+  const bool has_a = M > 0 && K > 0, has_b = K > 0 && N > 0, has_c = M > 0 && N > 0;
+  if ((has_a && A == nullptr) || (has_b && B == nullptr) || (has_c && C == nullptr))
+    return T2S_ERR_INVALID;
+  if ((has_a && misaligned4(A)) || (has_b && misaligned4(B)) || (has_c && misaligned4(C)))
+    return T2S_ERR_INVALID;
+  if (has_c && ((has_a && static_cast<const void*>(C) == A) ||
+                (has_b && static_cast<const void*>(C) == B)))
+    return T2S_ERR_INVALID;
+  *noop = !has_c;
+  if (*noop) return T2S_OK;
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->A = A;
+  p->B = B;
+  p->C = C;
+  p->stream = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = status_word(&p->status);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return T2S_OK;
+}
+
+// K == 0: the empty sum, +0.0f everywhere.
+int zero_fill(const Problem& p) {
+  const cudaError_t e = cudaMemsetAsync(p.C, 0, static_cast<size_t>(p.M) * p.N * sizeof(float),
+                                        p.stream);
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
+using Launcher = cudaError_t (*)(const Problem&);
+
+int gemm_common(Launcher launch, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                float* C, t2s_stream_t stream) {
+  Problem p{};
+  bool noop = false;
+  const int rc = prepare(M, N, K, A, B, C, stream, &p, &noop);
+  if (rc != T2S_OK || noop) return rc;
+  if (K == 0) return zero_fill(p);
+  const cudaError_t e = launch(p);
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
+__global__ void wait_selftest_kernel(unsigned* status, uint64_t limit_ns) {
+  __shared__ alignas(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on this barrier: the wait must give up and record it.
+  if (threadIdx.x == 0) mbar_wait_bounded(b, 0, status, limit_ns);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace t2s
+
+using namespace t2s;
+
+extern "C" {
+
+int t2s_gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+                 t2s_stream_t stream) {
+  return gemm_common(launch_ffma, M, N, K, A, B, C, stream);
+}
+
+int t2s_gemm_f32_naive(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                       float* C, t2s_stream_t stream) {
+  return gemm_common(launch_naive, M, N, K, A, B, C, stream);
+}
+
+int t2s_gemm_f32_smem32(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                        float* C, t2s_stream_t stream) {
+  return gemm_common(launch_smem32, M, N, K, A, B, C, stream);
+}
+
+size_t t2s_gemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return 0;
+  return tf32x3_workspace_bytes(M, N, K);
+}
+
+int t2s_gemm_f32_tf32x3(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+                        void* workspace, size_t workspace_bytes, t2s_stream_t stream) {
+  Problem p{};
+  bool noop = false;
+  const int rc = prepare(M, N, K, A, B, C, stream, &p, &noop);
+  if (rc != T2S_OK || noop) return rc;
+  if (K == 0) return zero_fill(p);
+  const size_t need = tf32x3_workspace_bytes(M, N, K);
+  if (workspace == nullptr || workspace_bytes < need) return T2S_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return T2S_ERR_WORKSPACE;
+  const cudaError_t e = launch_tf32x3(p, workspace);
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
+const char* t2s_status_string(int status) {
+  switch (status) {
+    case T2S_OK: return "ok";
+    case T2S_ERR_INVALID: return "invalid argument";
+    case T2S_ERR_CUDA: return "CUDA error (see t2s_last_cuda_error)";
+    case T2S_ERR_TIMEOUT: return "a kernel gave up a bounded barrier wait";
+    case T2S_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+int t2s_device_status(t2s_stream_t stream) {
+  unsigned* word = nullptr;
+  cudaError_t e = status_word(&word);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  unsigned value = 0;
+  e = cudaMemcpyAsync(&value, word, sizeof(value), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(word, 0, sizeof(unsigned), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return value == 0 ? T2S_OK : static_cast<int>(value);
+}
+
+int t2s_last_cuda_error(void) { return g_last_cuda_error; }
+
+int t2s_selftest_wait_timeout(int64_t limit_ns, t2s_stream_t stream) {
+  unsigned* word = nullptr;
+  cudaError_t e = status_word(&word);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (limit_ns < 1000) limit_ns = 1000;
+  if (limit_ns > 1000000000) limit_ns = 1000000000;
+  e = launch_wait_selftest(word, static_cast<uint64_t>(limit_ns),
+                           reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
+int t2s_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,39 @@
+// t2s_internal.h -- declarations shared by the library's translation units.
+// Not part of the public C ABI (that is include/t2s_gemm.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/t2s_gemm.h"
+
+namespace t2s {
+
+// Bounded barrier waits give up after this long (2 s); a correct kernel never
+// waits more than microseconds on one barrier.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// One validated product: sizes, device pointers, stream, and the device status
+// word the kernels record bounded-wait failures in.
+struct Problem {
+  int64_t M, N, K;
+  const float* A;
+  const float* B;
+  float* C;
+  cudaStream_t stream;
+  unsigned* status;
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_naive(const Problem& p);
+cudaError_t launch_smem32(const Problem& p);
+cudaError_t launch_ffma(const Problem& p);
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_tf32x3(const Problem& p, void* workspace);
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
+
+// Tensor-map encoding through the driver entry point (no link-time libcuda).
+// Returns cudaSuccess or the error from looking up the driver function; the
+// CUresult of the encode itself is returned through `cu_result`.
+struct CUtensorMap_st;
+}  // namespace t2s

@@ -1,0 +1,95 @@
+"""The C ABI without a GPU: the library loads, exports what the header declares,
+and rejects bad arguments before touching CUDA."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from roofline_driven_tiling_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "t2s_gemm.h")
+
+
+def header_functions():
+    with open(HEADER, encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(t2s_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return binding.lib()
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for required in ("t2s_gemm_f32", "t2s_gemm_f32_naive", "t2s_gemm_f32_smem32",
+                     "t2s_gemm_f32_tf32x3", "t2s_gemm_f32_tf32x3_workspace_size",
+                     "t2s_status_string", "t2s_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), "libt2s_gemm.so does not export %s" % name
+        assert name in binding.SIGNATURES, "binding lacks %s" % name
+
+
+def test_binding_declares_nothing_the_header_lacks():
+    assert set(binding.SIGNATURES) == set(header_functions())
+
+
+def test_status_strings(lib):
+    for code in range(0, 6):
+        s = binding.t2s_status_string(code)
+        assert isinstance(s, str) and s
+    assert binding.t2s_status_string(binding.T2S_OK) == "ok"
+
+
+@pytest.mark.parametrize("fn", ["t2s_gemm_f32", "t2s_gemm_f32_naive", "t2s_gemm_f32_smem32"])
+def test_invalid_arguments_rejected_on_host(lib, fn):
+    f = getattr(binding, fn)
+    fake = 1 << 20  # never dereferenced: every case below fails validation first
+    assert f(-1, 4, 4, fake, fake, fake + 4096) == binding.T2S_ERR_INVALID
+    assert f(4, -1, 4, fake, fake, fake + 4096) == binding.T2S_ERR_INVALID
+    assert f(4, 4, -1, fake, fake, fake + 4096) == binding.T2S_ERR_INVALID
+    big = binding.T2S_MAX_DIM + 1
+    assert f(big, 4, 4, fake, fake, fake + 4096) == binding.T2S_ERR_INVALID
+    assert f(4, 4, 4, 0, fake, fake + 4096) == binding.T2S_ERR_INVALID  # NULL A
+    assert f(4, 4, 4, fake, 0, fake + 4096) == binding.T2S_ERR_INVALID  # NULL B
+    assert f(4, 4, 4, fake, fake, 0) == binding.T2S_ERR_INVALID  # NULL C
+    assert f(4, 4, 4, fake + 2, fake, fake + 4096) == binding.T2S_ERR_INVALID  # misaligned
+    assert f(4, 4, 4, fake, fake, fake) == binding.T2S_ERR_INVALID  # C aliases A
+    assert f(4, 4, 4, fake + 4096, fake, fake) == binding.T2S_ERR_INVALID  # C aliases B
+
+
+@pytest.mark.parametrize("fn", ["t2s_gemm_f32", "t2s_gemm_f32_naive", "t2s_gemm_f32_smem32"])
+def test_empty_output_is_a_noop(lib, fn):
+    f = getattr(binding, fn)
+    # M == 0 or N == 0: nothing to compute; NULL is fine for empty matrices.
+    assert f(0, 0, 0, 0, 0, 0) == binding.T2S_OK
+    assert f(0, 7, 0, 0, 0, 0) == binding.T2S_OK
+    assert f(5, 0, 0, 0, 0, 0) == binding.T2S_OK
+
+
+def test_tf32x3_workspace_size(lib):
+    ws = binding.t2s_gemm_f32_tf32x3_workspace_size
+    # Two planes (big, small) of A (M x K) and of B (N x K), 4 bytes each, 256-byte padded.
+    assert ws(4096, 4096, 4096) == 4 * 4 * 4096 * 4096
+    assert ws(0, 0, 0) == 0
+    assert ws(-1, 2, 3) == 0
+    assert ws(3, 5, 7) % 256 == 0 and ws(3, 5, 7) >= 2 * 4 * (3 * 7 + 5 * 7)
+    fake = 1 << 20
+    assert binding.t2s_gemm_f32_tf32x3(-1, 4, 4, fake, fake, fake + 4096, fake, 1 << 20) == \
+        binding.T2S_ERR_INVALID
+
+
+def test_version(lib):
+    assert binding.t2s_version() >= 100

@@ -1,0 +1,233 @@
+"""Parity of the CUDA kernels with the CPU oracle (GPU tests, through the C ABI).
+
+Bars:
+* the FFMA kernels (product, naive, smem32) use one IEEE fused multiply-add per k in
+  ascending k, so they must equal the oracle's fused reading bit for bit on every
+  input; on the integer-pattern inputs, where every operation is exact, they must
+  also equal the two-rounding reading bit for bit;
+* against the two-rounding reading (the literal C statement), the bound is
+  max |C_gpu - C_oracle| <= 1e-6 * K * max|a| * max|b|;
+* the 3xTF32 tensor-core kernel must meet that same bound against both readings,
+  and be exact on the integer pattern.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from roofline_driven_tiling_gb300 import binding, inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+FFMA_KERNELS = ("ffma", "naive", "smem32")
+GUARD = 64  # canary floats on each side of every buffer
+C_SENTINEL = np.float32(-12345.678)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    assert binding.device_status() == binding.T2S_OK
+
+
+class Guarded:
+    """A device copy of a matrix with NaN canaries (inputs) or sentinels (output)
+    on both sides; `shift` floats of extra offset make the data 4-byte aligned only."""
+
+    def __init__(self, x: np.ndarray, fill: float, shift: int = 0):
+        n = x.size
+        self.shape = x.shape
+        self.n = n
+        self.start = GUARD + shift
+        self.buf = torch.full((n + 2 * GUARD + shift,), float(fill), dtype=torch.float32,
+                              device="cuda")
+        if n:
+            self.buf[self.start:self.start + n] = torch.from_numpy(np.ascontiguousarray(x).ravel()).cuda()
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr() + 4 * self.start
+
+    def data(self) -> np.ndarray:
+        return self.buf[self.start:self.start + self.n].cpu().numpy().reshape(self.shape)
+
+    def guards_intact(self, fill: float) -> bool:
+        host = self.buf.cpu().numpy()
+        lo, hi = host[:self.start], host[self.start + self.n:]
+        if np.isnan(fill):
+            return bool(np.all(np.isnan(lo)) and np.all(np.isnan(hi)))
+        return bool(np.all(lo == fill) and np.all(hi == fill))
+
+
+def run(kernel: str, A: np.ndarray, B: np.ndarray, shift: int = 0, stream=None):
+    """Runs one kernel through the C ABI on guarded device buffers; returns C (host)."""
+    M, K = A.shape
+    N = B.shape[1]
+    dA = Guarded(A, np.nan, shift)
+    dB = Guarded(B, np.nan, shift)
+    dC = Guarded(np.full((M, N), C_SENTINEL, np.float32), C_SENTINEL, shift)
+    s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    if kernel == "tf32x3":
+        need = binding.t2s_gemm_f32_tf32x3_workspace_size(M, N, K)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+        rc = binding.t2s_gemm_f32_tf32x3(M, N, K, dA.ptr, dB.ptr, dC.ptr, ws.data_ptr(),
+                                         ws.numel(), s)
+    else:
+        rc = getattr(binding, binding.KERNELS[kernel])(M, N, K, dA.ptr, dB.ptr, dC.ptr, s)
+    assert rc == binding.T2S_OK, binding.status_string(rc)
+    assert binding.t2s_device_status(s) == binding.T2S_OK
+    assert dA.guards_intact(np.nan) and dB.guards_intact(np.nan)
+    assert dC.guards_intact(C_SENTINEL), "write outside C"
+    return dC.data()
+
+
+def bits_equal(x: np.ndarray, y: np.ndarray) -> bool:
+    return np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
+def mismatch(x: np.ndarray, y: np.ndarray) -> str:
+    bad = np.argwhere(x.view(np.uint32) != y.view(np.uint32))
+    if bad.size == 0:
+        return "equal"
+    i = tuple(bad[0])
+    return "%d elements differ; first at %s: %r vs %r" % (len(bad), i, x[i], y[i])
+
+
+def tolerance(A: np.ndarray, B: np.ndarray) -> float:
+    K = A.shape[1]
+    return 1e-6 * K * float(np.max(np.abs(A))) * float(np.max(np.abs(B)))
+
+
+# ------------------------------------------------------------------ the workloads
+@pytest.mark.parametrize("kernel", FFMA_KERNELS)
+@pytest.mark.parametrize("n", [256, 1024])
+def test_integer_pattern_bit_exact(kernel, n):
+    A, B = inputs.integer_pattern(n, n, n)
+    C = run(kernel, A, B)
+    for mode in (oracle.FMA, oracle.MUL_ADD):
+        want = oracle.sgemm(A, B, mode)
+        assert bits_equal(C, want), mismatch(C, want)
+
+
+@pytest.mark.parametrize("kernel", FFMA_KERNELS)
+def test_constant_inputs_1024(kernel):
+    n = 1024
+    A, B = inputs.constant(n, n, n)
+    C = run(kernel, A, B)
+    want = oracle.sgemm_rows(A, B, 0, 8, oracle.FMA)[0, 0]
+    assert np.all(C == want)  # every entry is the same sum
+    exact = n * 0.5 * float(np.float32(0.4))
+    gamma = n * 2.0 ** -24 / (1 - n * 2.0 ** -24)
+    assert abs(float(C[0, 0]) - exact) <= gamma * exact  # closed form 0.2 K within gamma_K
+
+
+@pytest.mark.parametrize("kernel", FFMA_KERNELS)
+def test_ragged_1000x1003x997(kernel):
+    M, N, K = 1000, 1003, 997
+    A, B = inputs.uniform_pair(M, N, K, 3)
+    C = run(kernel, A, B)
+    want = oracle.sgemm(A, B, oracle.FMA)
+    assert bits_equal(C, want), mismatch(C, want)
+    lit = oracle.sgemm(A, B, oracle.MUL_ADD)
+    assert float(np.max(np.abs(C - lit))) <= tolerance(A, B)
+
+
+def sample_positions(M, N, rng, n_random=4096):
+    rows = [0, M - 1, M // 2]
+    cols = [0, N - 1, N // 2]
+    r = [np.full(N, i) for i in rows] + [np.arange(M) for _ in cols]
+    c = [np.arange(N) for _ in rows] + [np.full(M, j) for j in cols]
+    r.append(rng.integers(0, M, n_random))
+    c.append(rng.integers(0, N, n_random))
+    return np.concatenate(r), np.concatenate(c)
+
+
+def check_sampled(C, A, B, seed=0):
+    M, N = C.shape
+    rows, cols = sample_positions(M, N, np.random.default_rng(seed))
+    want = oracle.sgemm_at(A, B, rows, cols, oracle.FMA)
+    got = C[rows, cols]
+    assert bits_equal(got, want), mismatch(got, want)
+    lit = oracle.sgemm_at(A, B, rows, cols, oracle.MUL_ADD)
+    assert float(np.max(np.abs(got - lit))) <= tolerance(A, B)
+
+
+def test_headline_4096_sampled():
+    """The benchmarked workload (4096^3, uniform, config 4) in the benchmarked launch."""
+    A, B = inputs.uniform_pair(4096, 4096, 4096, 4)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    C = binding.gemm(dA, dB).cpu().numpy()
+    assert binding.device_status() == binding.T2S_OK
+    assert np.all(np.isfinite(C))
+    check_sampled(C, A, B)
+
+
+@pytest.mark.parametrize("shape", inputs.SWEEP, ids=lambda s: "x".join(map(str, s)))
+def test_sweep_sampled(shape):
+    M, N, K = shape
+    A, B = inputs.uniform_pair(M, N, K, 5)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    C = binding.gemm(dA, dB).cpu().numpy()
+    assert binding.device_status() == binding.T2S_OK
+    check_sampled(C, A, B, seed=M + N + K)
+
+
+# ------------------------------------------------------------------ edges
+def small_shapes():
+    edge = [1, 2, 3, 4, 5, 7, 8, 31, 32, 33, 63, 64, 65, 127, 128, 129, 191, 257]
+    rng = np.random.default_rng(1234)
+    shapes = {(1, 1, 1), (1, 1, 257), (257, 1, 1), (1, 257, 1), (129, 129, 129), (64, 64, 64),
+              (128, 128, 32), (128, 128, 33), (65, 300, 31)}
+    while len(shapes) < 90:
+        shapes.add(tuple(int(x) for x in rng.choice(edge, 3)))
+    return sorted(shapes)
+
+
+@pytest.mark.parametrize("shift", [0, 1], ids=["aligned", "misaligned"])
+@pytest.mark.parametrize("shape", small_shapes(), ids=lambda s: "x".join(map(str, s)))
+def test_small_ragged_shapes(shape, shift):
+    M, N, K = shape
+    A = inputs.uniform(M, K, 7 + M)
+    B = inputs.uniform(K, N, 9 + N)
+    want = oracle.sgemm(A, B, oracle.FMA)
+    for kernel in FFMA_KERNELS if shift == 0 else ("ffma",):
+        C = run(kernel, A, B, shift=shift)
+        assert bits_equal(C, want), "%s: %s" % (kernel, mismatch(C, want))
+
+
+def test_misaligned_equals_aligned():
+    """The cp.async load path (4-byte aligned pointers) gives the TMA path's bits."""
+    A, B = inputs.uniform_pair(384, 256, 512, 11)
+    assert bits_equal(run("ffma", A, B, shift=0), run("ffma", A, B, shift=1))
+
+
+@pytest.mark.parametrize("kernel", FFMA_KERNELS)
+def test_k_zero_writes_positive_zero(kernel):
+    A = np.zeros((33, 0), np.float32)
+    B = np.zeros((0, 17), np.float32)
+    C = run(kernel, A, B)
+    assert np.all(C.view(np.uint32) == 0)
+
+
+def test_non_default_stream():
+    A, B = inputs.uniform_pair(520, 260, 132, 12)
+    s = torch.cuda.Stream()
+    C = run("ffma", A, B, stream=s)
+    assert bits_equal(C, oracle.sgemm(A, B, oracle.FMA))
+
+
+def test_bounded_wait_reports_timeout():
+    """A barrier nothing arrives on: the kernel gives up, records the timeout and the
+    context stays usable."""
+    s = torch.cuda.current_stream().cuda_stream
+    assert binding.t2s_selftest_wait_timeout(2_000_000, s) == binding.T2S_OK
+    assert binding.t2s_device_status(s) == binding.T2S_ERR_TIMEOUT
+    assert binding.t2s_device_status(s) == binding.T2S_OK  # read clears it
+    A, B = inputs.uniform_pair(64, 64, 64, 13)
+    assert bits_equal(run("ffma", A, B), oracle.sgemm(A, B, oracle.FMA))
