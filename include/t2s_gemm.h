@@ -116,11 +116,11 @@ int t2s_gemm_f32_smem32(int64_t M, int64_t N, int64_t K, const float *A,
  * max |C - C_fp32| <= 1e-6 * K * max|a| * max|b|, and it is exact wherever
  * every FP32 product and partial sum is exact (for example small integers).
  *
- * `workspace` is a DEVICE buffer of at least
+ * `workspace` is a DEVICE buffer, 256-byte aligned, of at least
  * t2s_gemm_f32_tf32x3_workspace_size(M, N, K) bytes, owned by the caller,
  * that holds the split operands; it must not overlap A, B or C and must stay
  * untouched until the stream has run the call. Returns T2S_ERR_WORKSPACE if it
- * is NULL or too small.
+ * is NULL, too small or not 256-byte aligned.
  */
 size_t t2s_gemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K);
 int t2s_gemm_f32_tf32x3(int64_t M, int64_t N, int64_t K, const float *A,

@@ -12,30 +12,35 @@
 // what moves the kernel from the bandwidth slope to the FP32 compute roof.
 //
 // GB300 design:
-//  * Warp specialisation. One producer warp fills a STAGES-deep ring of shared-memory
-//    buffers; consumer warps compute. Each ring slot has a "full" mbarrier (data
-//    landed) and an "empty" mbarrier (all consumer warps done reading it).
-//  * Producer, aligned case (K % 4 == 0, N % 4 == 0, 16-byte aligned pointers): the
-//    Tensor Memory Accelerator loads a BM x BK box of A and a BK x BN box of B per
-//    stage; out-of-range elements of edge boxes are filled with zeros by the TMA
-//    unit, and completion is counted in transaction bytes on the full barrier.
-//  * Producer, general case: 4-byte cp.async copies with zero fill write the same
-//    shared-memory image; each producer lane arrives on the full barrier when its
-//    copies land (cp.async.mbarrier.arrive.noinc).
+//  * A STAGES-deep ring of shared-memory buffers per CTA, one "full" mbarrier per slot.
+//    There is no producer warp: a CTA is 4 compute warps, so two CTAs (8 warps, two per
+//    SM sub-partition) fit one SM with up to 255 registers per thread.
+//  * Aligned case (K % 4 == 0, N % 4 == 0, 16-byte aligned pointers): the Tensor Memory
+//    Accelerator loads a BM x BK box of A and a BK x BN box of B per stage; elements
+//    outside the matrices are filled with zeros by the TMA unit, and completion is
+//    counted in transaction bytes on the full barrier. The last warp to finish reading a
+//    slot (a shared-memory counter per slot) issues the refill, so no warp ever blocks
+//    waiting for another to free a slot.
+//  * General case: every thread copies its share of a stage with 4-byte cp.async and zero
+//    fill, writing the same shared-memory image, and arrives on the full barrier when its
+//    copies land (cp.async.mbarrier.arrive.noinc); an "empty" barrier per slot tells the
+//    threads when all warps are done with a slot so it can be refilled.
 //  * A is stored K-major as it is in global memory (TMA cannot transpose 4-byte
 //    elements). Rows of BK floats are XOR-swizzled in 16-byte chunks (the TMA
 //    128/64/32-byte swizzle), so that the 8 rows a warp reads at one k chunk fall in
-//    8 distinct bank groups. Each thread reads its A values as float4 along k.
+//    8 distinct bank groups.
 //  * B is stored as it is (rows of BN floats); a warp reads 4 consecutive 16-byte
 //    chunks of one row per load, which is conflict-free without a swizzle.
-//  * Each consumer thread owns an 8 x 16 register tile of C: rows g + 8i of its
-//    warp's 64 rows (g = lane / 4) and columns 4h + 16j + {0..3} of its warp's 64
-//    columns (h = lane % 4). Accumulators are packed in pairs along n and updated
-//    with fma.rn.f32x2: one instruction does two IEEE fused multiply-adds, which
-//    halves the issue slots the FMAs need and leaves the rest for shared loads.
-//  * Every barrier wait is bounded; on expiry the kernel records T2S_ERR_TIMEOUT in
-//    the device status word and returns instead of hanging. The producer always
-//    waits for its own in-flight copies before it exits.
+//  * Each thread owns an 8 x 16 register tile of C: rows g + 8i of its warp's 64 rows
+//    (g = lane / 4) and columns 4h + 16j + {0..3} of its warp's 64 columns (h = lane % 4).
+//    Accumulators are packed in pairs along n and updated with fma.rn.f32x2: one
+//    instruction does two IEEE fused multiply-adds, which halves the issue slots the
+//    FMAs need and leaves the rest for shared loads.
+//  * The k loop runs in groups of 8 k values (fully unrolled inside a group) so that the
+//    loop body stays small enough for the instruction cache.
+//  * Every barrier wait is bounded; on expiry the kernel records T2S_ERR_TIMEOUT in the
+//    device status word and returns instead of hanging, after letting its own in-flight
+//    copies land.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -53,102 +58,78 @@
 namespace t2s {
 namespace {
 
-template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_, int MAX_REGS_,
-          int AV_>
+template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_, int AV_>
 struct FfmaConfig {
   static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
-  static constexpr int AV = AV_;  // k values per shared load of A (1, 2 or 4)
   static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
-  static constexpr int MAX_REGS = MAX_REGS_;  // per thread; sets how many CTAs fit an SM
+  static constexpr int AV = AV_;         // k values per shared load of A (1, 2 or 4)
   static constexpr int TM = 8, TN = 16;  // per-thread C tile
   static constexpr int LM = 8, LN = 4;   // lanes along m and n (LM x LN = 32)
   static constexpr int WM = LM * TM, WN = LN * TN;
   static_assert(BM == WARPS_M * WM && BN == WARPS_N * WN, "tile / warp mismatch");
   static_assert(BK == 8 || BK == 16 || BK == 32, "A rows must be 32, 64 or 128 bytes");
-  static_assert((AV == 1 || AV == 2 || AV == 4) && BK % AV == 0, "A load width");
-  static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
-  static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
+  static_assert((AV == 1 || AV == 2 || AV == 4) && 8 % AV == 0, "A load width");
+  static constexpr int WARPS = WARPS_M * WARPS_N;
+  static constexpr int THREADS = WARPS * 32;
+  // Two warps per SM sub-partition at most: every thread may use up to 255 registers.
+  static constexpr int MIN_BLOCKS = 8 / WARPS > 0 ? 8 / WARPS : 1;
   static constexpr int A_ROW_BYTES = BK * 4;
   static constexpr int SWZ_MASK = A_ROW_BYTES / 16 - 1;  // 7 (128 B), 3 (64 B), 1 (32 B)
   static constexpr int A_STAGE_BYTES = BM * BK * 4;
   static constexpr int B_STAGE_BYTES = BK * BN * 4;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   static_assert(A_STAGE_BYTES % 1024 == 0 && B_STAGE_BYTES % 1024 == 0, "stage alignment");
-  // Ring buffers, 2 * STAGES barriers, and up to 1 KB to align the base to 1024 B
-  // (the repeat of the 128-byte swizzle pattern).
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGES * 8 + 1024;
+  // Ring, full[S] and empty[S] barriers, refill counters, and up to 1 KB to align the
+  // base to 1024 B (the repeat of the 128-byte swizzle pattern).
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGES * 8 + STAGES * 4 + 1024;
 };
 
-// Byte offset inside an A stage of 16-byte chunk `chunk` of row `row`, after the
-// TMA swizzle: the chunk index is XORed with bits 7.. of the unswizzled offset.
+// Byte offset inside an A stage after the TMA swizzle: the 16-byte chunk index is XORed
+// with bits 7.. of the unswizzled offset.
 template <class Cfg>
 __device__ __forceinline__ uint32_t a_swizzled(uint32_t off) {
   return off ^ (((off >> 7) & Cfg::SWZ_MASK) << 4);
 }
 
-template <class Cfg, bool kTma>
-__device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                         const float* __restrict__ A, const float* __restrict__ B,
-                                         int M, int N, int K, int m0, int n0, int nkb,
-                                         uint32_t sA, uint32_t sB, uint32_t sBar, int lane,
-                                         unsigned* status) {
-  constexpr int S = Cfg::STAGES;
-  auto full = [&](int s) { return sBar + 8u * s; };
-  auto empty = [&](int s) { return sBar + 8u * (S + s); };
-  int issued = 0;
-  if (kTma) {
-    if (lane == 0) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % S;
-        const uint32_t round = static_cast<uint32_t>(kb / S);
-        if (kb >= S && !mbar_wait_bounded(empty(s), (round - 1u) & 1u, status)) break;
-        mbar_arrive_expect_tx(full(s), Cfg::STAGE_BYTES);
-        tma_load_2d(sA + s * Cfg::A_STAGE_BYTES, tmA, kb * Cfg::BK, m0, full(s));
-        tma_load_2d(sB + s * Cfg::B_STAGE_BYTES, tmB, n0, kb * Cfg::BK, full(s));
-        issued = kb + 1;
-      }
-    }
-  } else {
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % S;
-      const uint32_t round = static_cast<uint32_t>(kb / S);
-      if (kb >= S) {
-        const bool freed = mbar_wait_bounded(empty(s), (round - 1u) & 1u, status);
-        if (!__all_sync(0xffffffffu, freed)) break;
-      }
-      const int k0 = kb * Cfg::BK;
-      const uint32_t a_dst = sA + s * Cfg::A_STAGE_BYTES;
+// All threads of the CTA copy one stage (A box and B box) with 4-byte cp.async and zero
+// fill, then arrive on the stage's full barrier when their copies have landed.
+template <class Cfg>
+__device__ __forceinline__ void cp_async_stage(const float* __restrict__ A,
+                                               const float* __restrict__ B, int M, int N, int K,
+                                               int m0, int n0, int kb, uint32_t a_dst,
+                                               uint32_t b_dst, uint32_t full_bar) {
+  const int k0 = kb * Cfg::BK;
 #pragma unroll 4
-      for (int e = lane; e < Cfg::BM * Cfg::BK; e += 32) {
-        const int r = e / Cfg::BK, c = e % Cfg::BK;
-        const int gm = m0 + r, gk = k0 + c;
-        const bool v = gm < M && gk < K;
-        const float* src = v ? A + (static_cast<int64_t>(gm) * K + gk) : A;
-        cp_async_4(a_dst + a_swizzled<Cfg>(r * Cfg::A_ROW_BYTES + c * 4), src, v ? 4u : 0u);
-      }
-      const uint32_t b_dst = sB + s * Cfg::B_STAGE_BYTES;
+  for (int e = threadIdx.x; e < Cfg::BM * Cfg::BK; e += Cfg::THREADS) {
+    const int r = e / Cfg::BK, c = e % Cfg::BK;
+    const int gm = m0 + r, gk = k0 + c;
+    const bool v = gm < M && gk < K;
+    const float* src = v ? A + (static_cast<int64_t>(gm) * K + gk) : A;
+    cp_async_4(a_dst + a_swizzled<Cfg>(r * Cfg::A_ROW_BYTES + c * 4), src, v ? 4u : 0u);
+  }
 #pragma unroll 4
-      for (int e = lane; e < Cfg::BK * Cfg::BN; e += 32) {
-        const int r = e / Cfg::BN, c = e % Cfg::BN;
-        const int gk = k0 + r, gn = n0 + c;
-        const bool v = gk < K && gn < N;
-        const float* src = v ? B + (static_cast<int64_t>(gk) * N + gn) : B;
-        cp_async_4(b_dst + (r * Cfg::BN + c) * 4, src, v ? 4u : 0u);
-      }
-      cp_async_arrive_noinc(full(s));
-      issued = kb + 1;
-    }
+  for (int e = threadIdx.x; e < Cfg::BK * Cfg::BN; e += Cfg::THREADS) {
+    const int r = e / Cfg::BN, c = e % Cfg::BN;
+    const int gk = k0 + r, gn = n0 + c;
+    const bool v = gk < K && gn < N;
+    const float* src = v ? B + (static_cast<int64_t>(gk) * N + gn) : B;
+    cp_async_4(b_dst + (r * Cfg::BN + c) * 4, src, v ? 4u : 0u);
   }
-  // Do not leave while copies into this CTA's shared memory are still in flight.
-  if (kTma && lane != 0) return;
-  const int first = issued > S ? issued - S : 0;
-  for (int kb = first; kb < issued; ++kb) {
-    if (!mbar_wait_bounded(full(kb % S), static_cast<uint32_t>(kb / S) & 1u, status)) break;
-  }
+  cp_async_arrive_noinc(full_bar);
+}
+
+// One TMA stage: a BM x BK box of A and a BK x BN box of B, completion counted in bytes.
+template <class Cfg>
+__device__ __forceinline__ void tma_stage(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                          int m0, int n0, int kb, uint32_t a_dst,
+                                          uint32_t b_dst, uint32_t full_bar) {
+  mbar_arrive_expect_tx(full_bar, Cfg::STAGE_BYTES);
+  tma_load_2d(a_dst, tmA, kb * Cfg::BK, m0, full_bar);
+  tma_load_2d(b_dst, tmB, n0, kb * Cfg::BK, full_bar);
 }
 
 template <class Cfg, bool kTma>
-__global__ void __launch_bounds__(Cfg::THREADS) __maxnreg__(Cfg::MAX_REGS)
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const float* __restrict__ A,
                       const float* __restrict__ B, float* __restrict__ C, int M, int N, int K,
@@ -158,7 +139,12 @@ __global__ void __launch_bounds__(Cfg::THREADS) __maxnreg__(Cfg::MAX_REGS)
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sA = base;
   const uint32_t sB = sA + S * Cfg::A_STAGE_BYTES;
-  const uint32_t sBar = sB + S * Cfg::B_STAGE_BYTES;
+  const uint32_t sBar = sB + S * Cfg::B_STAGE_BYTES;  // full[S], empty[S]
+  const uint32_t sCnt = sBar + 16u * S;                // refill counters (TMA path)
+  auto full = [&](int s) { return sBar + 8u * s; };
+  auto empty = [&](int s) { return sBar + 8u * (S + s); };
+  auto a_stage = [&](int s) { return sA + static_cast<uint32_t>(s) * Cfg::A_STAGE_BYTES; };
+  auto b_stage = [&](int s) { return sB + static_cast<uint32_t>(s) * Cfg::B_STAGE_BYTES; };
 
   // Grouped tile order: 8 tile-rows at a time sweep the columns, so that the A rows
   // and B columns in flight stay resident in L2.
@@ -167,31 +153,32 @@ __global__ void __launch_bounds__(Cfg::THREADS) __maxnreg__(Cfg::MAX_REGS)
   const int per_group = kGroup * tiles_n;
   const int first_m = (tile / per_group) * kGroup;
   const int gsz = min(tiles_m - first_m, kGroup);
-  const int tm = first_m + (tile % per_group) % gsz;
-  const int tn = (tile % per_group) / gsz;
-  const int m0 = tm * Cfg::BM, n0 = tn * Cfg::BN;
+  const int m0 = (first_m + (tile % per_group) % gsz) * Cfg::BM;
+  const int n0 = ((tile % per_group) / gsz) * Cfg::BN;
   const int nkb = (K + Cfg::BK - 1) / Cfg::BK;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(sBar + 8u * s, kTma ? 1u : 32u);
-      mbar_init(sBar + 8u * (S + s), Cfg::CONSUMER_WARPS);
+      mbar_init(full(s), kTma ? 1u : static_cast<uint32_t>(Cfg::THREADS));
+      mbar_init(empty(s), Cfg::WARPS);
+      asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
     }
     mbar_fence_init();
-  }
-  if (kTma && warp == Cfg::CONSUMER_WARPS && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    if (kTma) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      for (int kb = 0; kb < S && kb < nkb; ++kb)
+        tma_stage<Cfg>(&tmA, &tmB, m0, n0, kb, a_stage(kb), b_stage(kb), full(kb));
+    }
   }
   __syncthreads();
-
-  if (warp == Cfg::CONSUMER_WARPS) {
-    producer<Cfg, kTma>(&tmA, &tmB, A, B, M, N, K, m0, n0, nkb, sA, sB, sBar, lane, status);
-    return;
+  if (!kTma) {
+    // Prologue of the cp.async ring: stages 0 .. S-2 (stage kb + S - 1 is issued at kb).
+    for (int kb = 0; kb < S - 1 && kb < nkb; ++kb)
+      cp_async_stage<Cfg>(A, B, M, N, K, m0, n0, kb, a_stage(kb), b_stage(kb), full(kb));
   }
 
-  // ---------------------------------------------------------------- consumers
   const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
   const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
   const int g = lane >> 2, h = lane & 3;
@@ -202,42 +189,83 @@ __global__ void __launch_bounds__(Cfg::THREADS) __maxnreg__(Cfg::MAX_REGS)
 #pragma unroll
     for (int j = 0; j < Cfg::TN / 2; ++j) acc[i][j] = 0ull;  // two +0.0f
 
-  // Row offsets (unswizzled) of this thread's 8 A rows, and the B column offset.
+  // This thread's A rows are wm0 + g + 8i: every one has the same swizzle XOR (the row
+  // index mod 8 is g), so the swizzle reduces to XORing the chunk index with `xr`.
   const uint32_t a_row0 = static_cast<uint32_t>((wm0 + g) * Cfg::A_ROW_BYTES);
+  const uint32_t xr = (a_row0 >> 7) & Cfg::SWZ_MASK;
   const uint32_t b_col0 = static_cast<uint32_t>((wn0 + 4 * h) * 4);
 
   for (int kb = 0; kb < nkb; ++kb) {
     const int s = kb % S;
+    if (!kTma) {
+      // Refill the slot freed at kb - 1 with stage kb + S - 1, once every warp is done with it.
+      const int nk = kb + S - 1;
+      if (nk < nkb) {
+        const int ns = nk % S;
+        bool freed = true;
+        if (kb >= 1) freed = mbar_wait_bounded(empty(ns), static_cast<uint32_t>((kb - 1) / S) & 1u, status);
+        if (!__all_sync(0xffffffffu, freed)) {
+          asm volatile("cp.async.wait_all;" ::: "memory");
+          return;
+        }
+        cp_async_stage<Cfg>(A, B, M, N, K, m0, n0, nk, a_stage(ns), b_stage(ns), full(ns));
+      }
+    }
     // Every lane polls; the decision to give up is taken by the whole warp at once.
-    const bool landed = mbar_wait_bounded(sBar + 8u * s, static_cast<uint32_t>(kb / S) & 1u, status);
-    if (!__all_sync(0xffffffffu, landed)) return;
-    const uint32_t a_base = sA + s * Cfg::A_STAGE_BYTES;
-    const uint32_t b_base = sB + s * Cfg::B_STAGE_BYTES + b_col0;
+    const bool landed = mbar_wait_bounded(full(s), static_cast<uint32_t>(kb / S) & 1u, status);
+    if (!__all_sync(0xffffffffu, landed)) {
+      if (!kTma) asm volatile("cp.async.wait_all;" ::: "memory");
+      if (kTma && lane == 0) {
+        // Let copies already issued into this CTA's ring land before leaving.
+        for (int j = kb; j < kb + S && j < nkb; ++j)
+          mbar_wait_bounded(full(j % S), static_cast<uint32_t>(j / S) & 1u, status, 10000000ull);
+      }
+      return;
+    }
+    const uint32_t a_base = a_stage(s) + a_row0;
+    const uint32_t b_base = b_stage(s) + b_col0;
+#pragma unroll 1
+    for (int kg = 0; kg < Cfg::BK / 8; ++kg) {
+      // 8 k values = two 16-byte chunks of each A row, swizzled.
+      const uint32_t c0 = ((2u * kg) ^ xr) << 4, c1 = ((2u * kg + 1u) ^ xr) << 4;
+      const uint32_t b_kg = b_base + kg * (8 * Cfg::BN * 4);
 #pragma unroll
-    for (int kc = 0; kc < Cfg::BK / Cfg::AV; ++kc) {
-      // AV consecutive k values of each of this thread's TM rows of A.
-      float a[Cfg::TM][Cfg::AV];
+      for (int kv = 0; kv < 8 / Cfg::AV; ++kv) {
+        const uint32_t koff = (kv * Cfg::AV < 4 ? c0 : c1) + (kv * Cfg::AV % 4) * 4;
+        float a[Cfg::TM][Cfg::AV];
 #pragma unroll
-      for (int i = 0; i < Cfg::TM; ++i)
-        lds_vec<Cfg::AV>(a_base + a_swizzled<Cfg>(a_row0 + i * Cfg::LM * Cfg::A_ROW_BYTES +
-                                                   kc * Cfg::AV * 4),
-                         a[i]);
+        for (int i = 0; i < Cfg::TM; ++i)
+          lds_vec<Cfg::AV>(a_base + i * Cfg::LM * Cfg::A_ROW_BYTES + koff, a[i]);
 #pragma unroll
-      for (int kk = 0; kk < Cfg::AV; ++kk) {
-        uint64_t b[Cfg::TN / 2];
-        const uint32_t b_row = b_base + (kc * Cfg::AV + kk) * (Cfg::BN * 4);
+        for (int kk = 0; kk < Cfg::AV; ++kk) {
+          uint64_t b[Cfg::TN / 2];
+          const uint32_t b_row = b_kg + (kv * Cfg::AV + kk) * (Cfg::BN * 4);
 #pragma unroll
-        for (int j = 0; j < Cfg::TN / 4; ++j) lds128_pairs(b_row + j * 64, b[2 * j], b[2 * j + 1]);
+          for (int j = 0; j < Cfg::TN / 4; ++j) lds128_pairs(b_row + j * 64, b[2 * j], b[2 * j + 1]);
 #pragma unroll
-        for (int i = 0; i < Cfg::TM; ++i) {
-          const uint64_t ap = pack_dup(a[i][kk]);
+          for (int i = 0; i < Cfg::TM; ++i) {
+            const uint64_t ap = pack_dup(a[i][kk]);
 #pragma unroll
-          for (int j = 0; j < Cfg::TN / 2; ++j) ffma2(acc[i][j], ap, b[j]);
+            for (int j = 0; j < Cfg::TN / 2; ++j) ffma2(acc[i][j], ap, b[j]);
+          }
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(sBar + 8u * (S + s));
+    if (lane == 0) {
+      if (kTma) {
+        // The last warp to finish with this slot refills it with stage kb + S.
+        uint32_t old;
+        asm volatile("atom.shared.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(sCnt + 4u * s) : "memory");
+        if (old == Cfg::WARPS - 1) {
+          asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
+          if (kb + S < nkb)
+            tma_stage<Cfg>(&tmA, &tmB, m0, n0, kb + S, a_stage(s), b_stage(s), full(s));
+        }
+      } else {
+        mbar_arrive(empty(s));
+      }
+    }
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -294,13 +322,13 @@ cudaError_t run(const Problem& p) {
   return cudaGetLastError();
 }
 
-// 128 x 128 CTA tile, 4 consumer warps (2 x 2 of 64 x 64), BK = 32, 3 stages:
-// 96 KB of ring per CTA, two CTAs per SM.
-using Big = FfmaConfig<128, 128, 32, 3, 2, 2, 200, BIG_AV>;
+// 128 x 128 CTA tile, 4 warps (2 x 2 of 64 x 64), BK = 32, 3 stages: 96 KB of ring per
+// CTA, two CTAs (8 warps) per SM.
+using Big = FfmaConfig<128, 128, 32, 3, 2, 2, BIG_AV>;
 // 64 x 128 tiles for products too small to give every SM two 128 x 128 tiles.
-using Mid = FfmaConfig<64, 128, 32, 4, 1, 2, 200, 2>;
-// 64 x 64 tiles, one consumer warp, for the smallest products.
-using Small = FfmaConfig<64, 64, 32, 4, 1, 1, 200, 2>;
+using Mid = FfmaConfig<64, 128, 32, 3, 1, 2, 2>;
+// 64 x 64 tiles, one warp, for the smallest products.
+using Small = FfmaConfig<64, 64, 32, 3, 1, 1, 2>;
 
 bool tma_ok(const Problem& p) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.A), b = reinterpret_cast<uintptr_t>(p.B);

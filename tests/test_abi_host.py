@@ -83,6 +83,8 @@ def test_tf32x3_workspace_size(lib):
     ws = binding.t2s_gemm_f32_tf32x3_workspace_size
     # Two planes (big, small) of A (M x K) and of B (N x K), 4 bytes each, 256-byte padded.
     assert ws(4096, 4096, 4096) == 4 * 4 * 4096 * 4096
+    # K is padded to a multiple of 32 in the planes.
+    assert ws(128, 128, 997) == 4 * 4 * 128 * 1024
     assert ws(0, 0, 0) == 0
     assert ws(-1, 2, 3) == 0
     assert ws(3, 5, 7) % 256 == 0 and ws(3, 5, 7) >= 2 * 4 * (3 * 7 + 5 * 7)

@@ -231,3 +231,78 @@ def test_bounded_wait_reports_timeout():
     assert binding.t2s_device_status(s) == binding.T2S_OK  # read clears it
     A, B = inputs.uniform_pair(64, 64, 64, 13)
     assert bits_equal(run("ffma", A, B), oracle.sgemm(A, B, oracle.FMA))
+
+
+# ------------------------------------------------------------------ 3xTF32 tensor-core kernel
+@pytest.mark.parametrize("n", [256, 1024])
+def test_tf32x3_integer_pattern_exact(n):
+    """Small integers are exact in TF32 (the small parts are zero) and every sum is exact."""
+    A, B = inputs.integer_pattern(n, n, n)
+    C = run("tf32x3", A, B)
+    want = oracle.sgemm(A, B, oracle.FMA)
+    assert bits_equal(C, want), mismatch(C, want)
+
+
+def test_tf32x3_ragged_tolerance():
+    M, N, K = 1000, 1003, 997
+    A, B = inputs.uniform_pair(M, N, K, 3)
+    C = run("tf32x3", A, B)
+    for mode in (oracle.FMA, oracle.MUL_ADD):
+        ref = oracle.sgemm(A, B, mode)
+        assert float(np.max(np.abs(C - ref))) <= tolerance(A, B)
+
+
+def test_tf32x3_constant_closed_form():
+    n = 1024
+    A, B = inputs.constant(n, n, n)
+    C = run("tf32x3", A, B)
+    exact = n * 0.5 * float(np.float32(0.4))
+    gamma = n * 2.0 ** -24 / (1 - n * 2.0 ** -24)
+    assert float(np.max(np.abs(C.astype(np.float64) - exact))) <= 2 * gamma * exact
+
+
+def test_tf32x3_headline_sampled():
+    A, B = inputs.uniform_pair(4096, 4096, 4096, 4)
+    C = binding.gemm(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), kernel="tf32x3")
+    assert binding.device_status() == binding.T2S_OK
+    C = C.cpu().numpy()
+    rows, cols = sample_positions(4096, 4096, np.random.default_rng(4))
+    got = C[rows, cols]
+    for mode in (oracle.FMA, oracle.MUL_ADD):
+        ref = oracle.sgemm_at(A, B, rows, cols, mode)
+        assert float(np.max(np.abs(got - ref))) <= tolerance(A, B)
+
+
+@pytest.mark.parametrize("shape", small_shapes()[::3], ids=lambda s: "x".join(map(str, s)))
+def test_tf32x3_small_shapes(shape):
+    M, N, K = shape
+    A = inputs.uniform(M, K, 17 + M)
+    B = inputs.uniform(K, N, 19 + N)
+    C = run("tf32x3", A, B)
+    ref = oracle.sgemm(A, B, oracle.MUL_ADD)
+    assert float(np.max(np.abs(C - ref))) <= tolerance(A, B)
+
+
+@pytest.mark.parametrize("shift", [1])
+def test_tf32x3_misaligned_inputs(shift):
+    A, B = inputs.uniform_pair(257, 131, 67, 14)
+    C = run("tf32x3", A, B, shift=shift)
+    assert float(np.max(np.abs(C - oracle.sgemm(A, B, oracle.MUL_ADD)))) <= tolerance(A, B)
+
+
+def test_tf32x3_workspace_checks():
+    M, N, K = 64, 64, 64
+    dA = torch.zeros((M, K), device="cuda")
+    dB = torch.zeros((K, N), device="cuda")
+    dC = torch.zeros((M, N), device="cuda")
+    need = binding.t2s_gemm_f32_tf32x3_workspace_size(M, N, K)
+    ws = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    f = binding.t2s_gemm_f32_tf32x3
+    assert f(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), 0, need, s) == binding.T2S_ERR_WORKSPACE
+    assert f(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), ws.data_ptr(), need - 1, s) == \
+        binding.T2S_ERR_WORKSPACE
+    assert f(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), ws.data_ptr() + 4, need, s) == \
+        binding.T2S_ERR_WORKSPACE
+    assert f(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), ws.data_ptr(), need, s) == binding.T2S_OK
+    assert binding.t2s_device_status(s) == binding.T2S_OK
