@@ -1,0 +1,58 @@
+"""Host logic of bench.py's multi-rank path on CPU: two gloo ranks, max over ranks."""
+from __future__ import annotations
+
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ws, r, local = bench.dist_env()
+    assert (ws, r, local) == (world, rank, rank)
+    # Each rank's own time; the job's time is the slowest rank.
+    got = bench.reduce_max(1.5 + rank)
+    bench.barrier()
+    out[rank] = got
+    dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] == out[1] == 2.5
+
+
+def test_reduce_max_single_process_is_identity():
+    import bench
+    assert bench.reduce_max(3.25) == 3.25
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
+    assert capsys.readouterr().out == ""
