@@ -46,6 +46,8 @@
  *                       is available from t2s_last_cuda_error().
  *  - T2S_ERR_WORKSPACE: the workspace passed to t2s_gemm_f32_tf32x3 is NULL
  *                       or smaller than t2s_gemm_f32_tf32x3_workspace_size().
+ *  - T2S_ERR_TOO_LARGE: only from t2s_gemm_f32_tf32x3_noalloc: the problem needs
+ *                       more scratch than its built-in array holds.
  *  - T2S_ERR_TIMEOUT:   only from t2s_device_status(): a kernel gave up a
  *                       bounded wait on a pipeline barrier (it records this
  *                       in the device status word and returns instead of
@@ -69,6 +71,7 @@ typedef struct CUstream_st *t2s_stream_t;
 #define T2S_ERR_CUDA 2
 #define T2S_ERR_TIMEOUT 3
 #define T2S_ERR_WORKSPACE 4
+#define T2S_ERR_TOO_LARGE 5
 
 #define T2S_MAX_DIM ((int64_t)1 << 30) /* per dimension */
 
@@ -126,6 +129,33 @@ size_t t2s_gemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K);
 int t2s_gemm_f32_tf32x3(int64_t M, int64_t N, int64_t K, const float *A,
                         const float *B, float *C, void *workspace,
                         size_t workspace_bytes, t2s_stream_t stream);
+
+/*
+ * The same 3xTF32 product for callers that cannot allocate device memory (the source
+ * pages have no counterpart of this entry point). Examples: a plugin inside a framework
+ * that owns all device memory through its own pool and budget, a latency-critical loop
+ * that cannot afford the implicit synchronisation and unbounded time of cudaMalloc /
+ * cudaFree, or C code without a device allocator of its own.
+ *
+ * Instead of a caller-owned workspace, the split operands live in a static device array of
+ * T2S_TF32X3_NOALLOC_MAX_SCRATCH bytes (32 MiB) inside this library. Every GPU that loads
+ * the library holds that array until the process exits. The call allocates nothing and
+ * calls no allocating routine.
+ *  - Limit: t2s_gemm_f32_tf32x3_workspace_size(M, N, K) must not exceed
+ *    T2S_TF32X3_NOALLOC_MAX_SCRATCH, i.e. about 16 * (M + N) * ceil(K / 32) * 32 bytes
+ *    (for example M = N = K = 1024 fits). Larger problems return T2S_ERR_TOO_LARGE and
+ *    enqueue nothing.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *    once per device); make that first call before any stream capture begins.
+ *  - All calls on a device share the one array, which keeps the last call's contents. Each
+ *    call rewrites every byte it reads, so nothing needs clearing between calls. Calls
+ *    that can overlap on the GPU (for example on two streams without ordering between
+ *    them) race on the array and may return wrong results: order them.
+ *  - Otherwise the contract, results and return codes are those of t2s_gemm_f32_tf32x3.
+ */
+#define T2S_TF32X3_NOALLOC_MAX_SCRATCH ((size_t)32 << 20)
+int t2s_gemm_f32_tf32x3_noalloc(int64_t M, int64_t N, int64_t K, const float *A,
+                                const float *B, float *C, t2s_stream_t stream);
 
 /* Static description of a return code. Never NULL. */
 const char *t2s_status_string(int status);

@@ -22,6 +22,8 @@ T2S_ERR_INVALID = 1
 T2S_ERR_CUDA = 2
 T2S_ERR_TIMEOUT = 3
 T2S_ERR_WORKSPACE = 4
+T2S_ERR_TOO_LARGE = 5
+T2S_TF32X3_NOALLOC_MAX_SCRATCH = 32 << 20
 T2S_MAX_DIM = 1 << 30
 
 #: Every function the header declares, with (argtypes, restype).
@@ -32,6 +34,7 @@ SIGNATURES = {
     "t2s_gemm_f32_smem32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_tf32x3_workspace_size": ([_i64, _i64, _i64], _sz),
     "t2s_gemm_f32_tf32x3": ([_i64, _i64, _i64, _p, _p, _p, _p, _sz, _p], _i),
+    "t2s_gemm_f32_tf32x3_noalloc": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_status_string": ([_i], ctypes.c_char_p),
     "t2s_device_status": ([_p], _i),
     "t2s_last_cuda_error": ([], _i),
@@ -86,6 +89,11 @@ def t2s_gemm_f32_tf32x3_workspace_size(M, N, K) -> int:
 
 def t2s_gemm_f32_tf32x3(M, N, K, A, B, C, workspace, workspace_bytes, stream=0) -> int:
     return lib().t2s_gemm_f32_tf32x3(M, N, K, A, B, C, workspace, workspace_bytes, stream)
+
+
+def t2s_gemm_f32_tf32x3_noalloc(M, N, K, A, B, C, stream=0) -> int:
+    """3xTF32 product with the library's built-in scratch array (no allocation)."""
+    return lib().t2s_gemm_f32_tf32x3_noalloc(M, N, K, A, B, C, stream)
 
 
 def t2s_status_string(status: int) -> str:

@@ -107,6 +107,8 @@ __global__ void wait_selftest_kernel(unsigned* status, uint64_t limit_ns) {
 
 }  // namespace
 
+void set_last_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
   return cudaGetLastError();
@@ -159,6 +161,7 @@ const char* t2s_status_string(int status) {
     case T2S_ERR_CUDA: return "CUDA error (see t2s_last_cuda_error)";
     case T2S_ERR_TIMEOUT: return "a kernel gave up a bounded barrier wait";
     case T2S_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case T2S_ERR_TOO_LARGE: return "problem needs more scratch than the built-in 32 MiB array";
     default: return "unknown status";
   }
 }

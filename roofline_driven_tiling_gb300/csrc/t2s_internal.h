@@ -31,9 +31,7 @@ cudaError_t launch_ffma(const Problem& p);
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tf32x3(const Problem& p, void* workspace);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
+// Records a CUDA error for t2s_last_cuda_error() on this host thread.
+void set_last_cuda_error(cudaError_t e);
 
-// Tensor-map encoding through the driver entry point (no link-time libcuda).
-// Returns cudaSuccess or the error from looking up the driver function; the
-// CUresult of the encode itself is returned through `cu_result`.
-struct CUtensorMap_st;
 }  // namespace t2s
