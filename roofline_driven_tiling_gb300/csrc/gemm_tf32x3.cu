@@ -11,17 +11,23 @@
 //      A_big, A_small : M x Kp      (A is already K-major: a row-wise copy)
 //      B_big, B_small : N x Kp      (B is K x N row-major: transposed through shared memory)
 //    so that every tensor-map stride is a multiple of 128 bytes whatever K and N are.
-// 2. Product kernel. One CTA per 128 x BN tile of C, 192 threads:
+// 2. Product kernel, persistent: one CTA of 192 threads per SM walks 128 x BN tiles of C.
 //      warp 0     -- TMA producer: per K block, one box of each of the four planes;
 //      warp 1     -- allocates TMEM, one lane issues tcgen05.mma kind::tf32 (M=128, N=BN,
 //                    K=8), three per k step into one FP32 accumulator in TMEM, in the order
 //                    small*big, big*small, big*big; tcgen05.commit frees each ring slot;
-//      warps 2..5 -- epilogue: tcgen05.ld of their 32 TMEM lanes (rows), stores to C.
+//      warps 2..  -- epilogue: tcgen05.ld of their 32 TMEM lanes (rows), stores to C.
+//    TMEM holds two accumulators. The tensor core accumulates one K chunk (256 values) from
+//    zero; the epilogue warps add each chunk's partial sums into FP32 registers with
+//    round-to-nearest while the next chunk's MMAs run. The tensor core's internal FP32
+//    accumulation does not round to nearest: summed over all of K in TMEM its error grows
+//    faster than K and leaves the 1e-6 K max|a| max|b| bound at K = 8192; chunking keeps
+//    that error to 256 values and lets it average out across chunks.
 //    Shared-memory operands use the canonical K-major layout with the 128-byte (BK = 32) or
 //    64-byte (BK = 16) swizzle the TMA writes, described to the tensor core by matrix
 //    descriptors.
 // The missing small*small term is below 2^-22 relative; the tensor core's own summation
-// order makes the result differ from the FP32 definition by rounding only.
+// order within a chunk makes the result differ from the FP32 definition by rounding only.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -151,6 +157,18 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// 16 consecutive 32-bit TMEM columns of the warp's 32 lanes: thread t gets lane base + t.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // 32 consecutive 32-bit TMEM columns of the warp's 32 lanes: thread t gets lane base + t.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -168,20 +186,32 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // ------------------------------------------------------------------ product kernel
-template <int BN_, int BK_, int STAGES_>
+template <int BN_, int BK_, int STAGES_, int CHUNK_K_>
 struct Tf32Config {
   static constexpr int BM = 128, BN = BN_, BK = BK_, STAGES = STAGES_;
   static constexpr int MMA_K = 8;  // K of one kind::tf32 instruction
   static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "UMMA N for M = 128");
   static_assert(BK == 16 || BK == 32, "64- or 128-byte swizzled K-major rows");
+  // K values accumulated inside the tensor core before the partial sum is added, with
+  // round-to-nearest, into the FP32 sums the epilogue warps keep in registers.
+  static constexpr int CHUNK_KB = CHUNK_K_ / BK;
+  static_assert(CHUNK_K_ % BK == 0 && CHUNK_KB >= 1, "chunk of whole K blocks");
   static constexpr int ROW_BYTES = BK * 4;
   static constexpr int A_BYTES = BM * ROW_BYTES;
   static constexpr int B_BYTES = BN * ROW_BYTES;
   static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atom alignment");
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-  static constexpr int THREADS = 192;
-  static constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+  // Epilogue: 4 warps (one per TMEM lane quarter) per 128 columns of the tile.
+  static constexpr int EPI_WARPS = BN > 128 ? 8 : 4;
+  static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
+  static_assert(EPI_COLS % 16 == 0, "epilogue reads 16 columns at a time");
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  // 10 warps leave 3 warps on some SM sub-partitions: keep them within its registers.
+  static constexpr int MAX_REGS = THREADS > 256 ? 168 : 255;
+  // Two accumulators of BN FP32 columns each (double buffer), a power of two >= 32.
+  static constexpr uint32_t ACC_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
   // Matrix-descriptor swizzle code (bits 61..63): 2 = 128-byte, 4 = 64-byte.
   static constexpr uint64_t LAYOUT = BK == 32 ? 2 : 4;
   // Stride between 8-row core groups: 8 rows of ROW_BYTES.
@@ -196,7 +226,7 @@ struct Tf32Config {
 // Shared-memory matrix descriptor of a K-major swizzled operand starting at `addr`:
 // start address >> 4 (bits 0..13), leading-dimension offset (unused for swizzled K-major,
 // 16 bytes), stride-dimension offset SBO >> 4 (bits 32..45), the fixed 0b001 at bits 46..48,
-// base offset 0 (atoms are 1024-byte aligned), swizzle code at bits 61..63.
+// base offset 0 (atoms are aligned to their repeat), swizzle code at bits 61..63.
 template <class Cfg>
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
   return static_cast<uint64_t>((addr & 0x3ffffu) >> 4) | (static_cast<uint64_t>(1) << 16) |
@@ -204,8 +234,30 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
          (Cfg::LAYOUT << 61);
 }
 
+// Tile `t` of the grouped raster order (8 tile-rows sweep the columns together).
+__device__ __forceinline__ void tile_origin(int t, int tiles_m, int tiles_n, int bm, int bn,
+                                            int& m0, int& n0) {
+  constexpr int kGroup = 8;
+  const int per_group = kGroup * tiles_n;
+  const int first_m = (t / per_group) * kGroup;
+  const int gsz = min(tiles_m - first_m, kGroup);
+  m0 = (first_m + (t % per_group) % gsz) * bm;
+  n0 = ((t % per_group) / gsz) * bn;
+}
+
+// Persistent: CTA b takes tiles b, b + gridDim.x, ... Roles:
+//   warp 0  TMA producer (lane 0 issues) over the ring of STAGES slots, across tiles;
+//   warp 1  TMEM allocation; lane 0 issues the MMAs. Each K chunk of a tile is accumulated
+//           from zero into TMEM accumulator c % 2 (c counts chunks across tiles);
+//   warps 2 .. 2 + EPI_WARPS - 1  epilogue: add each chunk's partial sums into FP32
+//           registers with round-to-nearest (the tensor core's own accumulation is not
+//           round-to-nearest, and its error would grow with K), release the accumulator,
+//           and store the sums after the tile's last chunk.
+// Barriers: full[s] / empty[s] per ring slot; acc_full[b] (a chunk's MMAs are done) and
+// acc_empty[b] (the epilogue has read it) per accumulator. A fresh barrier counts its
+// "previous" phase (parity 1) as complete, so first uses wait on parity 1 and pass.
 template <class Cfg>
-__global__ void __launch_bounds__(Cfg::THREADS, 1)
+__global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
     tf32x3_kernel(const __grid_constant__ CUtensorMap tmAb, const __grid_constant__ CUtensorMap tmAs,
                   const __grid_constant__ CUtensorMap tmBb, const __grid_constant__ CUtensorMap tmBs,
                   float* __restrict__ C, int M, int N, int nkb, int tiles_m, int tiles_n,
@@ -213,29 +265,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sBar = base + S * Cfg::STAGE_BYTES;  // full[S], empty[S], acc_full
-  const uint32_t accBar = sBar + 16u * S;
-  const uint32_t sSlot = accBar + 8u;                  // TMEM address written by tcgen05.alloc
-  const uint32_t sAbort = sSlot + 4u;
+  const uint32_t sBar = base + S * Cfg::STAGE_BYTES;
   auto full = [&](int s) { return sBar + 8u * s; };
   auto empty = [&](int s) { return sBar + 8u * (S + s); };
+  const uint32_t accFull = sBar + 16u * S;          // [2]
+  const uint32_t accEmpty = accFull + 16u;          // [2]
+  const uint32_t mmaDone = accEmpty + 16u;
+  const uint32_t sSlot = mmaDone + 8u;              // TMEM address written by tcgen05.alloc
+  const uint32_t sAbort = sSlot + 4u;
   auto stage = [&](int s) { return base + static_cast<uint32_t>(s) * Cfg::STAGE_BYTES; };
 
-  constexpr int kGroup = 8;
-  const int tile = blockIdx.x;
-  const int per_group = kGroup * tiles_n;
-  const int first_m = (tile / per_group) * kGroup;
-  const int gsz = min(tiles_m - first_m, kGroup);
-  const int m0 = (first_m + (tile % per_group) % gsz) * Cfg::BM;
-  const int n0 = ((tile % per_group) / gsz) * Cfg::BN;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = tiles_m * tiles_n;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    mbar_init(accBar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accFull + 8u * b, 1);
+      mbar_init(accEmpty + 8u * b, Cfg::EPI_WARPS);  // lane 0 of each epilogue warp
+    }
+    mbar_init(mmaDone, 1);
     asm volatile("st.shared.u32 [%0], 0;" ::"r"(sAbort) : "memory");
     mbar_fence_init();
   }
@@ -252,17 +303,29 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   uint32_t tmem;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(sSlot) : "memory");
 
-  auto set_abort = [&]() { asm volatile("st.shared.u32 [%0], 1;" ::"r"(sAbort) : "memory"); };
+  auto aborted = [&]() {
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(sAbort) : "memory");
+    return v != 0u;
+  };
+  auto set_abort = [&]() { asm volatile("st.volatile.shared.u32 [%0], 1;" ::"r"(sAbort) : "memory"); };
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (lane 0 issues)
-    int issued = 0;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % S;
-      int ok = 1;
-      if (lane == 0) {
-        if (kb >= S) ok = mbar_wait_bounded(empty(s), static_cast<uint32_t>(kb / S - 1) & 1u, status);
-        if (ok) {
+    if (lane == 0) {
+      int64_t g = 0;  // running K-block index over all tiles of this CTA
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+        int m0, n0;
+        tile_origin(t, tiles_m, tiles_n, Cfg::BM, Cfg::BN, m0, n0);
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+          const int s = static_cast<int>(g % S);
+          const uint32_t par = (static_cast<uint32_t>(g / S) & 1u) ^ 1u;
+          if (aborted() || !mbar_wait_bounded(empty(s), par, status)) {
+            set_abort();
+            ok = false;
+            break;
+          }
           const uint32_t st = stage(s);
           const int k0 = kb * Cfg::BK;
           mbar_arrive_expect_tx(full(s), Cfg::STAGE_BYTES);
@@ -270,77 +333,118 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           tma_load_2d(st + Cfg::A_BYTES, &tmAs, k0, m0, full(s));
           tma_load_2d(st + 2 * Cfg::A_BYTES, &tmBb, k0, n0, full(s));
           tma_load_2d(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES, &tmBs, k0, n0, full(s));
-        } else {
-          set_abort();
         }
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      issued = kb + 1;
-      __syncwarp();
-    }
-    // Do not leave while copies into this CTA's shared memory are in flight.
-    if (lane == 0) {
-      for (int kb = issued > S ? issued - S : 0; kb < issued; ++kb)
-        if (!mbar_wait_bounded(full(kb % S), static_cast<uint32_t>(kb / S) & 1u, status)) break;
+      // Do not leave while copies into this CTA's shared memory are in flight.
+      for (int64_t j = g > S ? g - S : 0; j < g; ++j)
+        if (!mbar_wait_bounded(full(static_cast<int>(j % S)), static_cast<uint32_t>(j / S) & 1u,
+                               status))
+          break;
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (lane 0 issues)
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % S;
-      int ok = 1;
-      if (lane == 0) {
-        ok = mbar_wait_bounded(full(s), static_cast<uint32_t>(kb / S) & 1u, status);
-        if (ok) {
-          tc_fence_after();
-          const uint32_t st = stage(s);
-#pragma unroll
-          for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k) {
-            const uint32_t off = k * Cfg::MMA_K * 4;  // 32 bytes per k step inside the atom
-            const uint64_t a_big = smem_desc<Cfg>(st + off);
-            const uint64_t a_small = smem_desc<Cfg>(st + Cfg::A_BYTES + off);
-            const uint64_t b_big = smem_desc<Cfg>(st + 2 * Cfg::A_BYTES + off);
-            const uint64_t b_small = smem_desc<Cfg>(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES + off);
-            mma_tf32(tmem, a_small, b_big, Cfg::IDESC, (kb | k) != 0 ? 1u : 0u);
-            mma_tf32(tmem, a_big, b_small, Cfg::IDESC, 1u);
-            mma_tf32(tmem, a_big, b_big, Cfg::IDESC, 1u);
+    if (lane == 0) {
+      int64_t g = 0;   // K blocks consumed (ring position)
+      int64_t cc = 0;  // chunks issued (accumulator double buffer)
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+        for (int kb0 = 0; ok && kb0 < nkb; kb0 += Cfg::CHUNK_KB, ++cc) {
+          const int b = static_cast<int>(cc & 1);
+          const uint32_t acc = tmem + static_cast<uint32_t>(b) * Cfg::ACC_COLS;
+          // The epilogue must have read this accumulator's previous chunk.
+          if (aborted() ||
+              !mbar_wait_bounded(accEmpty + 8u * b, (static_cast<uint32_t>(cc >> 1) & 1u) ^ 1u,
+                                 status)) {
+            set_abort();
+            ok = false;
+            break;
           }
-          mma_commit(empty(s));
-        } else {
-          set_abort();
+          tc_fence_after();
+          const int kb1 = min(kb0 + Cfg::CHUNK_KB, nkb);
+          for (int kb = kb0; kb < kb1; ++kb, ++g) {
+            const int s = static_cast<int>(g % S);
+            if (aborted() || !mbar_wait_bounded(full(s), static_cast<uint32_t>(g / S) & 1u, status)) {
+              set_abort();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t st = stage(s);
+#pragma unroll
+            for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k) {
+              const uint32_t off = k * Cfg::MMA_K * 4;  // 32 bytes per k step inside the atom
+              const uint64_t a_big = smem_desc<Cfg>(st + off);
+              const uint64_t a_small = smem_desc<Cfg>(st + Cfg::A_BYTES + off);
+              const uint64_t b_big = smem_desc<Cfg>(st + 2 * Cfg::A_BYTES + off);
+              const uint64_t b_small = smem_desc<Cfg>(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES + off);
+              // The chunk's first MMA overwrites the accumulator (starts the partial sum at 0).
+              mma_tf32(acc, a_small, b_big, Cfg::IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
+              mma_tf32(acc, a_big, b_small, Cfg::IDESC, 1u);
+              mma_tf32(acc, a_big, b_big, Cfg::IDESC, 1u);
+            }
+            mma_commit(empty(s));  // frees the ring slot when these MMAs are done
+          }
+          if (ok) mma_commit(accFull + 8u * b);  // the chunk's partial sums are complete
         }
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      __syncwarp();
+      // Every MMA issued above must finish before TMEM can be released.
+      mma_commit(mmaDone);
+      mbar_wait_bounded(mmaDone, 0u, status);
     }
-    if (lane == 0) mma_commit(accBar);  // arrives when every MMA issued above is done
     __syncwarp();
   } else {
-    // ------------------------------------------------ epilogue: TMEM -> registers -> C
-    const bool done = mbar_wait_bounded(accBar, 0u, status);
-    uint32_t aborted;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(aborted) : "r"(sAbort) : "memory");
-    if (__all_sync(0xffffffffu, done && aborted == 0u)) {
-      tc_fence_after();
-      const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q + 31
-      const int row = m0 + 32 * q + lane;
-      float* crow = C + static_cast<int64_t>(row) * N;
-#pragma unroll 1
-      for (int c = 0; c < Cfg::BN; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c), r);
-        if (row < M) {
-          const int col0 = n0 + c;
-          if (vec_store && col0 + 32 <= N) {
+    // ------------------------------------------------ epilogue: TMEM -> FP32 sums -> C
+    const int e = warp - 2;
+    const int q = warp & 3;                        // TMEM lanes 32q .. 32q + 31 (rows)
+    const int col_base = (e >> 2) * Cfg::EPI_COLS;  // this warp's columns of the tile
+    int64_t cc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+      int m0, n0;
+      tile_origin(t, tiles_m, tiles_n, Cfg::BM, Cfg::BN, m0, n0);
+      float sum[Cfg::EPI_COLS];
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(crow + col0 + j) =
-                  make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                              __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+      for (int c = 0; c < Cfg::EPI_COLS; ++c) sum[c] = 0.0f;
+      for (int kb0 = 0; kb0 < nkb; kb0 += Cfg::CHUNK_KB, ++cc) {
+        const int b = static_cast<int>(cc & 1);
+        const bool done = !aborted() &&
+                          mbar_wait_bounded(accFull + 8u * b, static_cast<uint32_t>(cc >> 1) & 1u, status);
+        if (!__all_sync(0xffffffffu, done)) {
+          if (lane == 0) set_abort();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                               static_cast<uint32_t>(b) * Cfg::ACC_COLS +
+                               static_cast<uint32_t>(col_base);
+#pragma unroll
+        for (int c = 0; c < Cfg::EPI_COLS; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(tbase + static_cast<uint32_t>(c), r);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sum[c + i] = __fadd_rn(sum[c + i], __uint_as_float(r[i]));
+        }
+        // All of this warp's TMEM reads of accumulator b are complete (tcgen05.ld waited).
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(accEmpty + 8u * b);
+      }
+      if (!ok) break;
+      const int row = m0 + 32 * q + lane;
+      if (row < M) {
+        float* crow = C + static_cast<int64_t>(row) * N;
+        const int col0 = n0 + col_base;
+#pragma unroll
+        for (int c = 0; c < Cfg::EPI_COLS; c += 4) {
+          if (vec_store && col0 + c + 4 <= N) {
+            *reinterpret_cast<float4*>(crow + col0 + c) =
+                make_float4(sum[c], sum[c + 1], sum[c + 2], sum[c + 3]);
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < N) crow[col0 + j] = __uint_as_float(r[j]);
+            for (int i = 0; i < 4; ++i)
+              if (col0 + c + i < N) crow[col0 + c + i] = sum[c + i];
           }
         }
       }
@@ -351,9 +455,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    // Every MMA must be finished before its accumulator columns are released.
-    if (lane == 0) mbar_wait_bounded(accBar, 0u, status);
-    __syncwarp();
     tmem_dealloc(tmem, Cfg::TMEM_COLS);
   }
 }
@@ -373,18 +474,27 @@ cudaError_t run_tf32x3(const Problem& p, float* a_big, float* a_small, float* b_
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Cfg::SMEM_BYTES)) != cudaSuccess)
     return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int64_t tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
   const int64_t tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
-  if (tiles_m * tiles_n > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int64_t tiles = tiles_m * tiles_n;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
   const int vec_store = (p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) ? 1 : 0;
-  kern<<<static_cast<unsigned>(tiles_m * tiles_n), Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(
       tAb, tAs, tBb, tBs, p.C, static_cast<int>(p.M), static_cast<int>(p.N),
       static_cast<int>(Kp / Cfg::BK), static_cast<int>(tiles_m), static_cast<int>(tiles_n),
       p.status, vec_store);
   return cudaGetLastError();
 }
 
-using Tf32Default = Tf32Config<128, 32, 3>;
+// 128 x 128 tiles, BK = 32, 3 stages of 64 KB; 4 epilogue warps.
+using Tf32Narrow = Tf32Config<128, 32, 3, 256>;
+// 128 x 256 tiles, BK = 16, 4 stages of 48 KB; 8 epilogue warps. Half the A traffic per
+// FLOP of the narrow tile, used when there are enough tiles to keep every SM busy.
+using Tf32Wide = Tf32Config<256, 16, 4, 256>;
 
 }  // namespace
 
@@ -423,7 +533,10 @@ cudaError_t launch_tf32x3(const Problem& p, void* workspace) {
     split_transpose_kernel<<<grid, dim3(32, 8), 0, p.stream>>>(p.B, b_big, b_small, p.K, p.N, Kp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  return run_tf32x3<Tf32Default>(p, a_big, a_small, b_big, b_small, Kp);
+  const int64_t wide_tiles = ((p.M + 127) / 128) * ((p.N + 255) / 256);
+  if (wide_tiles >= 2 * static_cast<int64_t>(sms) && p.K >= 256)
+    return run_tf32x3<Tf32Wide>(p, a_big, a_small, b_big, b_small, Kp);
+  return run_tf32x3<Tf32Narrow>(p, a_big, a_small, b_big, b_small, Kp);
 }
 
 }  // namespace t2s

@@ -51,28 +51,46 @@
 #include "t2s_internal.h"
 #include "t2s_tmap.h"
 
+// Tuning knobs of the 128 x 128 configuration (defaults are the measured best).
 #ifndef BIG_AV
 #define BIG_AV 2
+#endif
+#ifndef BIG_BK
+#define BIG_BK 32
+#endif
+#ifndef BIG_STAGES
+#define BIG_STAGES 3
+#endif
+#ifndef FFMA_KG_UNROLL
+#define FFMA_KG_UNROLL 4
+#endif
+#ifndef FFMA_SMALL_CFG
+#define FFMA_SMALL_CFG 2
 #endif
 
 namespace t2s {
 namespace {
 
-template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_, int AV_>
+template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_, int AV_, int TM_,
+          int TN_, int KG_UNROLL_>
 struct FfmaConfig {
   static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
   static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
-  static constexpr int AV = AV_;         // k values per shared load of A (1, 2 or 4)
-  static constexpr int TM = 8, TN = 16;  // per-thread C tile
-  static constexpr int LM = 8, LN = 4;   // lanes along m and n (LM x LN = 32)
+  static constexpr int AV = AV_;          // k values per shared load of A (1, 2 or 4)
+  static constexpr int TM = TM_, TN = TN_;  // per-thread C tile
+  static constexpr int KG_UNROLL = KG_UNROLL_;  // groups of 8 k unrolled together
+  static constexpr int LM = 8, LN = 4;    // lanes along m and n (LM x LN = 32)
   static constexpr int WM = LM * TM, WN = LN * TN;
   static_assert(BM == WARPS_M * WM && BN == WARPS_N * WN, "tile / warp mismatch");
+  static_assert(TN % 4 == 0 && TM >= 1, "columns come in float4 chunks");
   static_assert(BK == 8 || BK == 16 || BK == 32, "A rows must be 32, 64 or 128 bytes");
   static_assert((AV == 1 || AV == 2 || AV == 4) && 8 % AV == 0, "A load width");
   static constexpr int WARPS = WARPS_M * WARPS_N;
   static constexpr int THREADS = WARPS * 32;
-  // Two warps per SM sub-partition at most: every thread may use up to 255 registers.
-  static constexpr int MIN_BLOCKS = 8 / WARPS > 0 ? 8 / WARPS : 1;
+  // Warps per SM the register file should hold: two per SM sub-partition for the
+  // 128-accumulator tile (up to 255 registers), more for smaller tiles.
+  static constexpr int TARGET_WARPS = TM * TN >= 128 ? 8 : TM * TN >= 64 ? 12 : 16;
+  static constexpr int MIN_BLOCKS = TARGET_WARPS / WARPS > 0 ? TARGET_WARPS / WARPS : 1;
   static constexpr int A_ROW_BYTES = BK * 4;
   static constexpr int SWZ_MASK = A_ROW_BYTES / 16 - 1;  // 7 (128 B), 3 (64 B), 1 (32 B)
   static constexpr int A_STAGE_BYTES = BM * BK * 4;
@@ -224,7 +242,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
     }
     const uint32_t a_base = a_stage(s) + a_row0;
     const uint32_t b_base = b_stage(s) + b_col0;
-#pragma unroll 1
+#pragma unroll Cfg::KG_UNROLL
     for (int kg = 0; kg < Cfg::BK / 8; ++kg) {
       // 8 k values = two 16-byte chunks of each A row, swizzled.
       const uint32_t c0 = ((2u * kg) ^ xr) << 4, c1 = ((2u * kg + 1u) ^ xr) << 4;
@@ -322,13 +340,19 @@ cudaError_t run(const Problem& p) {
   return cudaGetLastError();
 }
 
-// 128 x 128 CTA tile, 4 warps (2 x 2 of 64 x 64), BK = 32, 3 stages: 96 KB of ring per
-// CTA, two CTAs (8 warps) per SM.
-using Big = FfmaConfig<128, 128, 32, 3, 2, 2, BIG_AV>;
-// 64 x 128 tiles for products too small to give every SM two 128 x 128 tiles.
-using Mid = FfmaConfig<64, 128, 32, 3, 1, 2, 2>;
-// 64 x 64 tiles, one warp, for the smallest products.
-using Small = FfmaConfig<64, 64, 32, 3, 1, 1, 2>;
+// 128 x 128 CTA tile, 4 warps (2 x 2 of 64 x 64), 8 x 16 per thread, BK = 32, 3 stages:
+// 96 KB of ring per CTA, two CTAs (8 warps) per SM. The k loop is fully unrolled over a K
+// block when K is long enough to pay for the larger code.
+using Big = FfmaConfig<128, 128, BIG_BK, BIG_STAGES, 2, 2, BIG_AV, 8, 16, FFMA_KG_UNROLL>;
+using BigShortK = FfmaConfig<128, 128, 32, 3, 2, 2, 2, 8, 16, 1>;
+// Smaller tiles for products too small to give every SM two 128 x 128 tiles.
+using Mid = FfmaConfig<64, 128, 32, 3, 1, 2, 2, 8, 16, 1>;
+using Small = FfmaConfig<64, 64, 32, 3, 1, 1, 2, 8, 16, 1>;
+// 8 x 8 and 4 x 8 per thread: more warps for small products. 4 x 8 (64 x 64 CTA tiles of
+// 4 warps) measured fastest below 2048^2 outputs: 32.4 TFLOP/s at 1024^3 against 22.2 for
+// 8 x 16 and 31.5 for 8 x 8.
+using Small88 = FfmaConfig<64, 64, 16, 4, 1, 2, 2, 8, 8, 1>;
+using Small48 = FfmaConfig<64, 64, 16, 4, 2, 2, 2, 4, 8, 1>;
 
 bool tma_ok(const Problem& p) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.A), b = reinterpret_cast<uintptr_t>(p.B);
@@ -350,9 +374,14 @@ cudaError_t launch_ffma(const Problem& p) {
   if (e != cudaSuccess) return e;
   const int64_t big_tiles = ((p.M + 127) / 128) * ((p.N + 127) / 128);
   const int64_t mid_tiles = ((p.M + 63) / 64) * ((p.N + 127) / 128);
-  if (big_tiles >= 2 * static_cast<int64_t>(sms)) return run_any<Big>(p);
+  if (big_tiles >= 2 * static_cast<int64_t>(sms))
+    return p.K >= 256 ? run_any<Big>(p) : run_any<BigShortK>(p);
   if (mid_tiles >= static_cast<int64_t>(sms)) return run_any<Mid>(p);
-  return run_any<Small>(p);
+  switch (FFMA_SMALL_CFG) {
+    case 1: return run_any<Small88>(p);
+    case 2: return run_any<Small48>(p);
+    default: return run_any<Small>(p);
+  }
 }
 
 }  // namespace t2s

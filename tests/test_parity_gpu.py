@@ -306,3 +306,20 @@ def test_tf32x3_workspace_checks():
         binding.T2S_ERR_WORKSPACE
     assert f(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), ws.data_ptr(), need, s) == binding.T2S_OK
     assert binding.t2s_device_status(s) == binding.T2S_OK
+
+
+@pytest.mark.parametrize("shape", inputs.SWEEP + [(256, 256, 65536), (130, 70, 20000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tf32x3_sweep_and_long_k_sampled(shape):
+    """The tolerance must hold at every sweep shape and for long K, where an accumulation
+    that does not round to nearest drifts further with every added term."""
+    M, N, K = shape
+    A, B = inputs.uniform_pair(M, N, K, 5)
+    C = binding.gemm(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), kernel="tf32x3")
+    assert binding.device_status() == binding.T2S_OK
+    C = C.cpu().numpy()
+    rows, cols = sample_positions(M, N, np.random.default_rng(M + K))
+    got = C[rows, cols]
+    for mode in (oracle.FMA, oracle.MUL_ADD):
+        ref = oracle.sgemm_at(A, B, rows, cols, mode)
+        assert float(np.max(np.abs(got - ref))) <= tolerance(A, B)
