@@ -91,6 +91,26 @@ int t2s_gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B
                  float *C, t2s_stream_t stream);
 
 /*
+ * The product of t2s_gemm_f32 for matrices in HOST memory (row-major, same layout),
+ * staged through device buffers the caller owns: dA (M*K floats), dB (K*N), dC (M*N).
+ * The library copies B, then streams A in row blocks and runs the product of each block
+ * as soon as it has arrived, copying every finished block of C back while later blocks
+ * compute (host-to-device and device-to-host copies on their own streams). The result is
+ * bit-identical to t2s_gemm_f32.
+ *  - hA, hB, hC should be page-locked (cudaHostAlloc, cudaHostRegister) for the copies to
+ *    run asynchronously and overlap; pageable memory gives the same result, serialised.
+ *  - Asynchronous: returns once everything is enqueued; hC is complete, and hA, hB, dA,
+ *    dB, dC may be reused, after `stream` has been synchronised.
+ *  - Allocates no device memory. The first call on a device creates three streams and
+ *    twenty events that the library keeps for later calls; calls from several host
+ *    threads are serialised while they enqueue.
+ *  - Errors: T2S_ERR_INVALID as for t2s_gemm_f32 (a NULL buffer for a non-empty matrix,
+ *    dC equal to dA or dB); T2S_ERR_CUDA if a copy, event or launch fails.
+ */
+int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *hA, const float *hB,
+                      float *hC, float *dA, float *dB, float *dC, t2s_stream_t stream);
+
+/*
  * Comparison point: one thread per C element, k loop over global memory,
  * 16 x 16 thread blocks (page "GEMM 커널 테스트 코드 작성 및 최적화 (1024^3 크기
  * 실험)", sections "Naive GEMM 커널 동작 방식" and "쓰레드 매핑"). Uses fmaf, so

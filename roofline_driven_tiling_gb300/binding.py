@@ -30,6 +30,7 @@ T2S_MAX_DIM = 1 << 30
 _i64, _p, _i, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "t2s_gemm_f32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
+    "t2s_gemm_f32_host": ([_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_naive": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_smem32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_tf32x3_workspace_size": ([_i64, _i64, _i64], _sz),
@@ -73,6 +74,10 @@ def lib():
 # ---- the C ABI, same names ------------------------------------------------------------
 def t2s_gemm_f32(M, N, K, A, B, C, stream=0) -> int:
     return lib().t2s_gemm_f32(M, N, K, A, B, C, stream)
+
+
+def t2s_gemm_f32_host(M, N, K, hA, hB, hC, dA, dB, dC, stream=0) -> int:
+    return lib().t2s_gemm_f32_host(M, N, K, hA, hB, hC, dA, dB, dC, stream)
 
 
 def t2s_gemm_f32_naive(M, N, K, A, B, C, stream=0) -> int:

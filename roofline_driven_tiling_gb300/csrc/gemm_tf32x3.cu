@@ -202,10 +202,12 @@ struct Tf32Config {
   static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atom alignment");
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-  // Epilogue: 4 warps (one per TMEM lane quarter) per 128 columns of the tile.
-  static constexpr int EPI_WARPS = BN > 128 ? 8 : 4;
-  static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
-  static_assert(EPI_COLS % 16 == 0, "epilogue reads 16 columns at a time");
+  // Epilogue: groups of 4 warps (one per TMEM lane quarter), each group owning an equal
+  // share of at most 128 of the tile's columns.
+  static constexpr int EPI_GROUPS = (BN + 127) / 128;
+  static constexpr int EPI_WARPS = 4 * EPI_GROUPS;
+  static constexpr int EPI_COLS = BN / EPI_GROUPS;
+  static_assert(BN % EPI_GROUPS == 0 && EPI_COLS % 16 == 0, "epilogue reads 16 columns at a time");
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   // 10 warps leave 3 warps on some SM sub-partitions: keep them within its registers.
   static constexpr int MAX_REGS = THREADS > 256 ? 168 : 255;
@@ -490,11 +492,12 @@ cudaError_t run_tf32x3(const Problem& p, float* a_big, float* a_small, float* b_
   return cudaGetLastError();
 }
 
-// 128 x 128 tiles, BK = 32, 3 stages of 64 KB; 4 epilogue warps.
-using Tf32Narrow = Tf32Config<128, 32, 3, 256>;
-// 128 x 256 tiles, BK = 16, 4 stages of 48 KB; 8 epilogue warps. Half the A traffic per
-// FLOP of the narrow tile, used when there are enough tiles to keep every SM busy.
-using Tf32Wide = Tf32Config<256, 16, 4, 256>;
+// Tile widths BN (M is 128): wider tiles read A less often per FLOP; the dispatcher picks
+// the width whose tile count spreads evenly over the SMs.
+using Tf32N128 = Tf32Config<128, 32, 3, 256>;  // 3 stages of 64 KB, 4 epilogue warps
+using Tf32N192 = Tf32Config<192, 16, 4, 256>;  // 4 stages of 40 KB, 8 epilogue warps
+using Tf32N224 = Tf32Config<224, 16, 4, 256>;  // 4 stages of 44 KB, 8 epilogue warps
+using Tf32N256 = Tf32Config<256, 16, 4, 256>;  // 4 stages of 48 KB, 8 epilogue warps
 
 }  // namespace
 
@@ -533,10 +536,33 @@ cudaError_t launch_tf32x3(const Problem& p, void* workspace) {
     split_transpose_kernel<<<grid, dim3(32, 8), 0, p.stream>>>(p.B, b_big, b_small, p.K, p.N, Kp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  const int64_t wide_tiles = ((p.M + 127) / 128) * ((p.N + 255) / 256);
-  if (wide_tiles >= 2 * static_cast<int64_t>(sms) && p.K >= 256)
-    return run_tf32x3<Tf32Wide>(p, a_big, a_small, b_big, b_small, Kp);
-  return run_tf32x3<Tf32Narrow>(p, a_big, a_small, b_big, b_small, Kp);
+  // Persistent CTAs take tiles in rounds of `sms`; the cost of a width is its number of
+  // rounds times its width, weighted by the per-tile efficiency measured on GB300 (narrow
+  // tiles re-read A more often: 128-wide tiles run about 15 % slower per FLOP than 256).
+  const int widths[4] = {128, 192, 224, 256};
+  const double weight[4] = {1.15, 1.03, 1.01, 1.0};
+  const int64_t tm = (p.M + 127) / 128;
+  int best = 0;
+  double best_cost = 0.0;
+  for (int i = 0; i < 4; ++i) {
+    const int64_t tiles = tm * ((p.N + widths[i] - 1) / widths[i]);
+    const int64_t rounds = (tiles + sms - 1) / sms;
+    const double cost = static_cast<double>(rounds) * widths[i] * weight[i];
+    if (i == 0 || cost < best_cost) {
+      best = i;
+      best_cost = cost;
+    }
+  }
+  if (p.K < 256) best = 0;  // one short chunk: the wide epilogue does not pay
+#ifdef TF32X3_FORCE_WIDTH
+  best = TF32X3_FORCE_WIDTH;
+#endif
+  switch (best) {
+    case 1: return run_tf32x3<Tf32N192>(p, a_big, a_small, b_big, b_small, Kp);
+    case 2: return run_tf32x3<Tf32N224>(p, a_big, a_small, b_big, b_small, Kp);
+    case 3: return run_tf32x3<Tf32N256>(p, a_big, a_small, b_big, b_small, Kp);
+    default: return run_tf32x3<Tf32N128>(p, a_big, a_small, b_big, b_small, Kp);
+  }
 }
 
 }  // namespace t2s

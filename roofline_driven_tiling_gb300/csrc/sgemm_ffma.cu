@@ -67,6 +67,9 @@
 #ifndef FFMA_SMALL_CFG
 #define FFMA_SMALL_CFG 2
 #endif
+#ifndef FFMA_FORCE_CFG
+#define FFMA_FORCE_CFG -1
+#endif
 
 namespace t2s {
 namespace {
@@ -372,11 +375,24 @@ cudaError_t launch_ffma(const Problem& p) {
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  switch (FFMA_FORCE_CFG) {
+    case 0: return run_any<Big>(p);
+    case 1: return run_any<BigShortK>(p);
+    case 2: return run_any<Mid>(p);
+    case 3: return run_any<Small>(p);
+    case 4: return run_any<Small88>(p);
+    case 5: return run_any<Small48>(p);
+    default: break;
+  }
+  // Thresholds from measurements on GB300 (152 SMs): the fully unrolled 128 x 128 kernel
+  // pays off once every SM sees two full waves of tile pairs; with fewer tiles the compact
+  // loop is faster, and below ~1.5 tiles per SM 64-row tiles spread the work further.
   const int64_t big_tiles = ((p.M + 127) / 128) * ((p.N + 127) / 128);
   const int64_t mid_tiles = ((p.M + 63) / 64) * ((p.N + 127) / 128);
-  if (big_tiles >= 2 * static_cast<int64_t>(sms))
-    return p.K >= 256 ? run_any<Big>(p) : run_any<BigShortK>(p);
-  if (mid_tiles >= static_cast<int64_t>(sms)) return run_any<Mid>(p);
+  const int64_t s64 = static_cast<int64_t>(sms);
+  if (big_tiles >= 4 * s64 && p.K >= 256) return run_any<Big>(p);
+  if (2 * big_tiles >= 3 * s64) return run_any<BigShortK>(p);
+  if (mid_tiles >= s64) return run_any<Mid>(p);
   switch (FFMA_SMALL_CFG) {
     case 1: return run_any<Small88>(p);
     case 2: return run_any<Small48>(p);

@@ -95,3 +95,19 @@ def test_tf32x3_workspace_size(lib):
 
 def test_version(lib):
     assert binding.t2s_version() >= 100
+
+
+def test_host_pipeline_rejects_bad_arguments(lib):
+    f = binding.t2s_gemm_f32_host
+    fake = 1 << 20
+    ok = dict(hA=fake, hB=fake + 4096, hC=fake + 8192, dA=fake + 12288, dB=fake + 16384,
+              dC=fake + 20480)
+    def call(M, N, K, **kw):
+        a = dict(ok, **kw)
+        return f(M, N, K, a["hA"], a["hB"], a["hC"], a["dA"], a["dB"], a["dC"], 0)
+    assert call(-1, 4, 4) == binding.T2S_ERR_INVALID
+    assert call(4, 4, binding.T2S_MAX_DIM + 1) == binding.T2S_ERR_INVALID
+    for name in ok:
+        assert call(4, 4, 4, **{name: 0}) == binding.T2S_ERR_INVALID, name
+    assert call(4, 4, 4, dC=ok["dA"]) == binding.T2S_ERR_INVALID
+    assert call(0, 4, 4) == binding.T2S_OK  # nothing to do

@@ -323,3 +323,35 @@ def test_tf32x3_sweep_and_long_k_sampled(shape):
     for mode in (oracle.FMA, oracle.MUL_ADD):
         ref = oracle.sgemm_at(A, B, rows, cols, mode)
         assert float(np.max(np.abs(got - ref))) <= tolerance(A, B)
+
+
+
+# ------------------------------------------------------------------ host-memory entry point
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (1000, 1003, 997), (1537, 260, 129),
+                                   (3, 5, 0), (600, 17, 33)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_host_pipeline_equals_device_entry(shape):
+    """Row-blocked, copy-overlapped product of host matrices: the bits of t2s_gemm_f32."""
+    M, N, K = shape
+    A = inputs.uniform(M, K, 31 + M)
+    B = inputs.uniform(K, N, 37 + N)
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC = torch.full((M, N), float("nan")).pin_memory()
+    dA = torch.empty((M, K), device="cuda")
+    dB = torch.empty((K, N), device="cuda")
+    dC = torch.empty((M, N), device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    rc = binding.t2s_gemm_f32_host(M, N, K, hA.data_ptr(), hB.data_ptr(), hC.data_ptr(),
+                                   dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), s)
+    assert rc == binding.T2S_OK, binding.status_string(rc)
+    assert binding.t2s_device_status(s) == binding.T2S_OK
+    got = hC.numpy()
+    if K == 0:
+        assert np.all(got.view(np.uint32) == 0)
+        return
+    want = binding.gemm(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()).cpu().numpy()
+    assert bits_equal(got, want), mismatch(got, want)
+    rows, cols = sample_positions(M, N, np.random.default_rng(7))
+    ref = oracle.sgemm_at(A, B, rows, cols, oracle.FMA)
+    assert bits_equal(got[rows, cols], ref)
