@@ -17,6 +17,10 @@
 namespace t2s {
 namespace {
 
+#ifndef T2S_PIPE_MIN_ROWS
+#define T2S_PIPE_MIN_ROWS 1024
+#endif
+
 constexpr int kMaxDevices = 64;
 constexpr int kMaxBlocks = 8;
 
@@ -88,8 +92,9 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
   if (e != cudaSuccess) return fail(e);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  // Row blocks of at least 512 rows, at most kMaxBlocks of them.
-  int nb = static_cast<int>(M / 512);
+  // Row blocks of at least T2S_PIPE_MIN_ROWS rows (1024 measured best at 3072^3 to 4096^3),
+  // at most kMaxBlocks of them.
+  int nb = static_cast<int>(M / T2S_PIPE_MIN_ROWS);
   nb = nb < 1 ? 1 : nb > kMaxBlocks ? kMaxBlocks : nb;
   const int64_t rows_per = (M + nb - 1) / nb;
 

@@ -355,3 +355,34 @@ def test_host_pipeline_equals_device_entry(shape):
     rows, cols = sample_positions(M, N, np.random.default_rng(7))
     ref = oracle.sgemm_at(A, B, rows, cols, oracle.FMA)
     assert bits_equal(got[rows, cols], ref)
+
+
+# ------------------------------------------------------------------ special values
+def special_inputs(M, N, K, seed):
+    """Uniform values with infinities, NaNs, signed zeros, subnormals and large magnitudes
+    planted at random positions."""
+    rng = np.random.default_rng(seed)
+    A = inputs.uniform(M, K, seed)
+    B = inputs.uniform(K, N, seed + 1)
+    specials = np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e-40, -3e-39, 1e30, -2e30,
+                         np.float32(1.4e-45)], dtype=np.float32)
+    for X in (A, B):
+        idx = rng.choice(X.size, size=max(1, X.size // 200), replace=False)
+        X.ravel()[idx] = rng.choice(specials, size=idx.size)
+    return A, B
+
+
+@pytest.mark.parametrize("kernel", FFMA_KERNELS)
+@pytest.mark.parametrize("shift", [0, 1], ids=["aligned", "misaligned"])
+def test_special_values_match_fma_oracle(kernel, shift):
+    """IEEE fused multiply-adds in the oracle's order give the same infinities, signed
+    zeros, subnormal results and NaN positions; finite results agree bit for bit."""
+    if kernel != "ffma" and shift:
+        pytest.skip("alignment only selects a load path of the product kernel")
+    M, N, K = 131, 257, 203
+    A, B = special_inputs(M, N, K, 77)
+    C = run(kernel, A, B, shift=shift)
+    want = oracle.sgemm(A, B, oracle.FMA)
+    assert np.array_equal(np.isnan(C), np.isnan(want))
+    keep = ~np.isnan(want)
+    assert bits_equal(C[keep], want[keep]), mismatch(C[keep], want[keep])
