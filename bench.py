@@ -340,6 +340,7 @@ def run_ours(args):
     if not args.skip_extras:
         line["tf32x3"] = extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws)
         line["also_1024"] = extra_1024(lib, dev, stream, flush, args, ws)
+        line["memory_roof"] = extra_vector_add(lib, dev, stream, flush, args)
 
     if rank == 0 and ws == 1 and not args.skip_cpu:
         rate, info = cpu_oracle_rate(A, B, float(os.environ.get("T2S_CPU_SECONDS", "12")))
@@ -404,6 +405,35 @@ def extra_1024(lib, dev, stream, flush, args, ws):
         out[name] = {"ms": t * 1e3, "tflops": rl.gemm_flops(n, n, n) / t / 1e12,
                      "frac_fp32_peak": rl.gemm_flops(n, n, n) / t / 1e12 / rl.fp32_peak_tflops()}
     return out
+
+
+def extra_vector_add(lib, dev, stream, flush, args):
+    """Vector add z = x + y over 2^28 floats (3 GB moved per call): the bandwidth slope of
+    the roofline (AI = 1/12 FLOP/B), measured with the same timing rules."""
+    import torch
+    from roofline_driven_tiling_gb300 import binding
+    from roofline_driven_tiling_gb300 import roofline as rl
+    n = 1 << 28
+    x = torch.empty(n, dtype=torch.float32, device=dev).uniform_(-1, 1)
+    y = torch.empty(n, dtype=torch.float32, device=dev).uniform_(-1, 1)
+    z = torch.empty(n, dtype=torch.float32, device=dev)
+    sp = stream.cuda_stream
+
+    def step():
+        rc = lib.t2s_vector_add_f32(n, x.data_ptr(), y.data_ptr(), z.data_ptr(), sp)
+        if rc != 0:
+            raise binding.T2SError(rc, "t2s_vector_add_f32")
+
+    times = time_steps(step, max(args.steps // 5, 5), 3, stream, flush)
+    t = sum(times) / len(times) / 1e3
+    nbytes = rl.vector_add_bytes(n)
+    gbs = nbytes / t / 1e9
+    peak = float(measured_peaks().get("hbm_gbs", 6792.4))
+    return {"workload": "z = x + y, 2^28 fp32 elements (12 bytes moved per element)",
+            "kernel": "t2s_vector_add_f32 (32-byte loads and stores)",
+            "ms": t * 1e3, "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak,
+            "bound": "hbm", "ai": rl.arithmetic_intensity(rl.vector_add_flops(n), nbytes),
+            "tflops": n / t / 1e12}
 
 
 def main(argv=None):

@@ -177,6 +177,18 @@ int t2s_gemm_f32_tf32x3(int64_t M, int64_t N, int64_t K, const float *A,
 int t2s_gemm_f32_tf32x3_noalloc(int64_t M, int64_t N, int64_t K, const float *A,
                                 const float *B, float *C, t2s_stream_t stream);
 
+/*
+ * Memory-roof probe: z[i] = x[i] + y[i] for i < n, FP32, one IEEE add (round to nearest)
+ * per element. This is the memory-bound example of page "4주차: Roofline과 Tiling", section
+ * "1. Arithmetic Intensity" ("Vector Add": N FLOPs for 12N bytes moved, AI = 1/12 FLOP/B);
+ * its measured bandwidth is the slope of the roofline on which the GEMM kernels are placed.
+ * x, y, z are device pointers (4-byte aligned; 32-byte alignment of all three selects the
+ * widest loads); z must not overlap x or y (exact aliasing is rejected). Asynchronous on
+ * `stream`; n == 0 is a no-op. Returns T2S_OK, T2S_ERR_INVALID or T2S_ERR_CUDA.
+ */
+int t2s_vector_add_f32(int64_t n, const float *x, const float *y, float *z,
+                       t2s_stream_t stream);
+
 /* Static description of a return code. Never NULL. */
 const char *t2s_status_string(int status);
 

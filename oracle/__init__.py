@@ -65,7 +65,19 @@ class Oracle:
         lib.t2s_oracle_num_threads.restype = ip
         lib.t2s_oracle_set_num_threads.argtypes = [ip]
         lib.t2s_oracle_set_num_threads.restype = None
+        lib.t2s_oracle_vector_add.argtypes = [i64, fp, fp, fp]
+        lib.t2s_oracle_vector_add.restype = ip
         self.lib = lib
+
+    def vector_add(self, x: np.ndarray, y: np.ndarray) -> np.ndarray:
+        """z = x + y elementwise (float32, one rounding per element)."""
+        x, y = _f32(x).ravel(), _f32(y).ravel()
+        if x.shape != y.shape:
+            raise ValueError("x and y differ in length")
+        z = np.empty_like(x)
+        if self.lib.t2s_oracle_vector_add(x.size, x.ctypes.data, y.ctypes.data, z.ctypes.data) != 0:
+            raise ValueError("oracle rejected the arguments")
+        return z
 
     def sgemm(self, A: np.ndarray, B: np.ndarray, mode: int = MUL_ADD) -> np.ndarray:
         """Full product C = A x B (float32, row-major)."""
@@ -139,6 +151,10 @@ def sgemm_at(A, B, rows, cols, mode: int = MUL_ADD) -> np.ndarray:
 
 def sgemm_rows(A, B, r0: int, r1: int, mode: int = MUL_ADD) -> np.ndarray:
     return default().sgemm_rows(A, B, r0, r1, mode)
+
+
+def vector_add(x, y) -> np.ndarray:
+    return default().vector_add(x, y)
 
 
 def num_threads() -> int:

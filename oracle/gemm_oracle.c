@@ -147,3 +147,19 @@ int t2s_oracle_sgemm_rows(int64_t M, int64_t N, int64_t K, const float *A,
     }
     return 0;
 }
+
+/*
+ * Vector add z = x + y, the memory-bound example of page "4주차: Roofline과 Tiling",
+ * section "1. Arithmetic Intensity", example "Vector Add": one FP32 add per element,
+ * reading x and y and writing z (12 bytes per element, AI = 1/12 FLOP/B).
+ * Returns 0, or -1 if n is negative.
+ */
+int t2s_oracle_vector_add(int64_t n, const float *x, const float *y, float *z)
+{
+    if (n < 0) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        z[i] = x[i] + y[i];
+    }
+    return 0;
+}

@@ -36,6 +36,7 @@ SIGNATURES = {
     "t2s_gemm_f32_tf32x3_workspace_size": ([_i64, _i64, _i64], _sz),
     "t2s_gemm_f32_tf32x3": ([_i64, _i64, _i64, _p, _p, _p, _p, _sz, _p], _i),
     "t2s_gemm_f32_tf32x3_noalloc": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
+    "t2s_vector_add_f32": ([_i64, _p, _p, _p, _p], _i),
     "t2s_status_string": ([_i], ctypes.c_char_p),
     "t2s_device_status": ([_p], _i),
     "t2s_last_cuda_error": ([], _i),
@@ -99,6 +100,10 @@ def t2s_gemm_f32_tf32x3(M, N, K, A, B, C, workspace, workspace_bytes, stream=0) 
 def t2s_gemm_f32_tf32x3_noalloc(M, N, K, A, B, C, stream=0) -> int:
     """3xTF32 product with the library's built-in scratch array (no allocation)."""
     return lib().t2s_gemm_f32_tf32x3_noalloc(M, N, K, A, B, C, stream)
+
+
+def t2s_vector_add_f32(n, x, y, z, stream=0) -> int:
+    return lib().t2s_vector_add_f32(n, x, y, z, stream)
 
 
 def t2s_status_string(status: int) -> str:

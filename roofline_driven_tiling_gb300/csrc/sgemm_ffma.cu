@@ -67,6 +67,9 @@
 #ifndef FFMA_SMALL_CFG
 #define FFMA_SMALL_CFG 2
 #endif
+#ifndef FFMA_J_OUTER
+#define FFMA_J_OUTER 1
+#endif
 #ifndef FFMA_FORCE_CFG
 #define FFMA_FORCE_CFG -1
 #endif
@@ -263,12 +266,47 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
           const uint32_t b_row = b_kg + (kv * Cfg::AV + kk) * (Cfg::BN * 4);
 #pragma unroll
           for (int j = 0; j < Cfg::TN / 4; ++j) lds128_pairs(b_row + j * 64, b[2 * j], b[2 * j + 1]);
+#if FFMA_J_OUTER == 1
+          // Column pairs outer, rows inner: consecutive FMAs share the B pair. Measured 3 %
+          // faster than rows outer at 4096^3 and 8192^3 (hoisting the {a, a} moves alone
+          // changes nothing, so the gain is in operand reuse, not in the moves).
+          uint64_t ap[Cfg::TM];
+#pragma unroll
+          for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[i][kk]);
+#pragma unroll
+          for (int j = 0; j < Cfg::TN / 2; ++j)
+#pragma unroll
+            for (int i = 0; i < Cfg::TM; ++i) ffma2(acc[i][j], ap[i], b[j]);
+#elif FFMA_J_OUTER == 2
+          uint64_t ap[Cfg::TM];
+#pragma unroll
+          for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[i][kk]);
+#pragma unroll
+          for (int i = 0; i < Cfg::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < Cfg::TN / 2; ++j) ffma2(acc[i][j], ap[i], b[j]);
+#elif FFMA_J_OUTER == 3
+          // 2 x 2 blocks of (row, column pair)
+          uint64_t ap[Cfg::TM];
+#pragma unroll
+          for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[i][kk]);
+#pragma unroll
+          for (int j = 0; j < Cfg::TN / 2; j += 2)
+#pragma unroll
+            for (int i = 0; i < Cfg::TM; i += 2) {
+              ffma2(acc[i][j], ap[i], b[j]);
+              ffma2(acc[i + 1][j], ap[i + 1], b[j]);
+              ffma2(acc[i][j + 1], ap[i], b[j + 1]);
+              ffma2(acc[i + 1][j + 1], ap[i + 1], b[j + 1]);
+            }
+#else
 #pragma unroll
           for (int i = 0; i < Cfg::TM; ++i) {
             const uint64_t ap = pack_dup(a[i][kk]);
 #pragma unroll
             for (int j = 0; j < Cfg::TN / 2; ++j) ffma2(acc[i][j], ap, b[j]);
           }
+#endif
         }
       }
     }

@@ -111,3 +111,13 @@ def test_host_pipeline_rejects_bad_arguments(lib):
         assert call(4, 4, 4, **{name: 0}) == binding.T2S_ERR_INVALID, name
     assert call(4, 4, 4, dC=ok["dA"]) == binding.T2S_ERR_INVALID
     assert call(0, 4, 4) == binding.T2S_OK  # nothing to do
+
+
+def test_vector_add_rejects_bad_arguments(lib):
+    f = binding.t2s_vector_add_f32
+    fake = 1 << 20
+    assert f(-1, fake, fake + 64, fake + 128) == binding.T2S_ERR_INVALID
+    assert f(8, 0, fake + 64, fake + 128) == binding.T2S_ERR_INVALID
+    assert f(8, fake + 2, fake + 64, fake + 128) == binding.T2S_ERR_INVALID
+    assert f(8, fake, fake + 64, fake) == binding.T2S_ERR_INVALID  # z aliases x
+    assert f(0, 0, 0, 0) == binding.T2S_OK

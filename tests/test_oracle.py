@@ -217,3 +217,24 @@ def test_planted_mistake_is_caught(name, oracle_source, tmp_path):
     mutant = oracle.Oracle(lib)
     failed = [c.__name__ for c in BATTERY if not c(mutant)[0]]
     assert failed, "planted mistake %r passed every pin" % name
+
+
+# ----------------------------------------------------------------------------
+# Vector add (the memory-roof probe's operation)
+# ----------------------------------------------------------------------------
+
+def test_vector_add_exact_and_special():
+    o = oracle.default()
+    # Dyadic values: every sum is exact, so it equals the float64 sum.
+    x = inputs.dyadic(1, 1001, seed=3).ravel()
+    y = inputs.dyadic(1, 1001, seed=4).ravel()
+    z = o.vector_add(x, y)
+    assert np.array_equal(z.astype(np.float64), x.astype(np.float64) + y.astype(np.float64))
+    # One rounding: 1 + 2^-24 is a tie and rounds to the even 1.0; 1 + 3 * 2^-24 rounds up.
+    z = o.vector_add(np.array([1.0, 1.0], np.float32),
+                     np.array([2.0 ** -24, 3 * 2.0 ** -24], np.float32))
+    assert z[0] == np.float32(1.0) and z[1] == np.float32(1.0 + 2.0 ** -22)
+    z = o.vector_add(np.array([np.inf, -0.0, 3e38], np.float32),
+                     np.array([-np.inf, -0.0, 3e38], np.float32))
+    assert np.isnan(z[0]) and np.signbit(z[1]) and z[1] == 0 and np.isinf(z[2])
+    assert o.vector_add(np.zeros(0, np.float32), np.zeros(0, np.float32)).size == 0

@@ -386,3 +386,23 @@ def test_special_values_match_fma_oracle(kernel, shift):
     assert np.array_equal(np.isnan(C), np.isnan(want))
     keep = ~np.isnan(want)
     assert bits_equal(C[keep], want[keep]), mismatch(C[keep], want[keep])
+
+
+# ------------------------------------------------------------------ vector add (memory roof)
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 31, 1000, 4099, 1 << 20, (1 << 22) + 13])
+@pytest.mark.parametrize("shift", [0, 1, 4], ids=["align32", "align4", "align16"])
+def test_vector_add_matches_oracle(n, shift):
+    x = inputs.uniform(1, n, 41 + n).ravel()
+    y = inputs.uniform(1, n, 43 + n).ravel()
+    if n > 8:
+        x[3], y[5], x[7], y[7] = np.inf, np.nan, -0.0, -0.0
+    dx, dy = Guarded(x, np.nan, shift), Guarded(y, np.nan, shift)
+    dz = Guarded(np.full(n, C_SENTINEL, np.float32), C_SENTINEL, shift)
+    s = torch.cuda.current_stream().cuda_stream
+    assert binding.t2s_vector_add_f32(n, dx.ptr, dy.ptr, dz.ptr, s) == binding.T2S_OK
+    assert binding.t2s_device_status(s) == binding.T2S_OK
+    assert dz.guards_intact(C_SENTINEL)
+    got, want = dz.data(), oracle.vector_add(x, y)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    keep = ~np.isnan(want)
+    assert bits_equal(got[keep], want[keep])
