@@ -64,9 +64,6 @@
 #ifndef FFMA_KG_UNROLL
 #define FFMA_KG_UNROLL 4
 #endif
-#ifndef FFMA_SMALL_CFG
-#define FFMA_SMALL_CFG 2
-#endif
 #ifndef FFMA_J_OUTER
 #define FFMA_J_OUTER 1
 #endif
@@ -386,13 +383,11 @@ cudaError_t run(const Problem& p) {
 // block when K is long enough to pay for the larger code.
 using Big = FfmaConfig<128, 128, BIG_BK, BIG_STAGES, 2, 2, BIG_AV, 8, 16, FFMA_KG_UNROLL>;
 using BigShortK = FfmaConfig<128, 128, 32, 3, 2, 2, 2, 8, 16, 1>;
-// Smaller tiles for products too small to give every SM two 128 x 128 tiles.
+// 64 x 128 tiles for products too small to give every SM two 128 x 128 tiles.
 using Mid = FfmaConfig<64, 128, 32, 3, 1, 2, 2, 8, 16, 1>;
-using Small = FfmaConfig<64, 64, 32, 3, 1, 1, 2, 8, 16, 1>;
-// 8 x 8 and 4 x 8 per thread: more warps for small products. 4 x 8 (64 x 64 CTA tiles of
-// 4 warps) measured fastest below 2048^2 outputs: 32.4 TFLOP/s at 1024^3 against 22.2 for
-// 8 x 16 and 31.5 for 8 x 8.
-using Small88 = FfmaConfig<64, 64, 16, 4, 1, 2, 2, 8, 8, 1>;
+// 4 x 8 per thread (64 x 64 CTA tiles of 4 warps): more warps for small products. Measured
+// fastest below ~1.5 tiles of 64 x 128 per SM: 32.4 TFLOP/s at 1024^3 against 22.2 for 64 x 64
+// tiles of 8 x 16 per thread and 31.5 for 8 x 8.
 using Small48 = FfmaConfig<64, 64, 16, 4, 2, 2, 2, 4, 8, 1>;
 
 bool tma_ok(const Problem& p) {
@@ -417,9 +412,7 @@ cudaError_t launch_ffma(const Problem& p) {
     case 0: return run_any<Big>(p);
     case 1: return run_any<BigShortK>(p);
     case 2: return run_any<Mid>(p);
-    case 3: return run_any<Small>(p);
-    case 4: return run_any<Small88>(p);
-    case 5: return run_any<Small48>(p);
+    case 3: return run_any<Small48>(p);
     default: break;
   }
   // Thresholds from measurements on GB300 (152 SMs): the fully unrolled 128 x 128 kernel
@@ -431,11 +424,7 @@ cudaError_t launch_ffma(const Problem& p) {
   if (big_tiles >= 4 * s64 && p.K >= 256) return run_any<Big>(p);
   if (2 * big_tiles >= 3 * s64) return run_any<BigShortK>(p);
   if (mid_tiles >= s64) return run_any<Mid>(p);
-  switch (FFMA_SMALL_CFG) {
-    case 1: return run_any<Small88>(p);
-    case 2: return run_any<Small48>(p);
-    default: return run_any<Small>(p);
-  }
+  return run_any<Small48>(p);
 }
 
 }  // namespace t2s

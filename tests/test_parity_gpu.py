@@ -406,3 +406,28 @@ def test_vector_add_matches_oracle(n, shift):
     assert np.array_equal(np.isnan(got), np.isnan(want))
     keep = ~np.isnan(want)
     assert bits_equal(got[keep], want[keep])
+
+
+# ------------------------------------------------------------------ every product configuration
+# One shape per configuration the dispatcher picks on a 152-SM GB300 (tile counts in the
+# comments), each on the TMA path (aligned) and the cp.async path (K and N not multiples of 4).
+DISPATCH_SHAPES = {
+    "big_4096": (4096, 4096, 1024),        # 1024 tiles of 128^2 >= 4 x 152, K >= 256
+    "big_short_k": (2048, 2048, 128),      # 256 tiles of 128^2 >= 1.5 x 152
+    "mid_1536": (1536, 1536, 512),         # 144 tiles of 128^2, 288 of 64 x 128
+    "small48_640": (640, 700, 300),        # 10 x 6 tiles of 64 x 128: 4 x 8 per thread
+}
+
+
+@pytest.mark.parametrize("ragged", [False, True], ids=["tma", "cpasync"])
+@pytest.mark.parametrize("name", sorted(DISPATCH_SHAPES))
+def test_every_configuration(name, ragged):
+    M, N, K = DISPATCH_SHAPES[name]
+    if ragged:
+        N, K = N - 1, K - 3
+    A = inputs.uniform(M, K, 61 + M)
+    B = inputs.uniform(K, N, 67 + N)
+    C = run("ffma", A, B)
+    rows, cols = sample_positions(M, N, np.random.default_rng(K))
+    want = oracle.sgemm_at(A, B, rows, cols, oracle.FMA)
+    assert bits_equal(C[rows, cols], want), mismatch(C[rows, cols], want)
