@@ -129,6 +129,31 @@ int t2s_gemm_f32_smem32(int64_t M, int64_t N, int64_t K, const float *A,
                         const float *B, float *C, t2s_stream_t stream);
 
 /*
+ * Split-K product for small or short-K problems (item "split-K for small and low-K shapes"
+ * of the tiling plan; page "4주차: Roofline과 Tiling", item 8 of "이번 주차 핵심": tiles that
+ * are too large for the problem leave the machine idle). K is cut into `splits` chunks of
+ * ceil(K / splits) values rounded up to 32; each chunk's product is computed by the product
+ * kernel into its own plane of `workspace` (M x N floats per plane), and the planes are then
+ * added into C in chunk order. Each chunk is summed in ascending k with fused multiply-adds,
+ * so the result differs from t2s_gemm_f32 only by the order of the chunk sums: it is
+ * deterministic and within max |C - C_fp32| <= 1e-6 * K * max|a| * max|b|, but not
+ * bit-identical.
+ *  - splits: 1..64 chunks requested, or <= 0 for the library's choice (no split when the
+ *    product already gives every SM 1.5 tiles of 128 x 128; otherwise about four such tiles
+ *    per SM, chunks of at least 64 values, at most 16 chunks). With a single chunk the call
+ *    is t2s_gemm_f32.
+ *  - workspace: a DEVICE buffer, 256-byte aligned, of at least
+ *    t2s_gemm_f32_splitk_workspace_size(M, N, K, splits) bytes (0 if no split is made), owned
+ *    by the caller and untouched until the stream has run the call.
+ *  - Returns T2S_ERR_INVALID for splits > 64, T2S_ERR_WORKSPACE for a missing, small or
+ *    misaligned workspace, otherwise as t2s_gemm_f32.
+ */
+size_t t2s_gemm_f32_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int splits);
+int t2s_gemm_f32_splitk(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
+                        float *C, int splits, void *workspace, size_t workspace_bytes,
+                        t2s_stream_t stream);
+
+/*
  * Tensor-core variant: error-compensated 3xTF32 on tcgen05 tensor cores with
  * TMEM accumulators. Each operand x is split into big = tf32(x) and
  * small = tf32(x - big); C accumulates small*big + big*small + big*big in FP32.

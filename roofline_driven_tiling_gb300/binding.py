@@ -33,6 +33,8 @@ SIGNATURES = {
     "t2s_gemm_f32_host": ([_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_naive": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_smem32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
+    "t2s_gemm_f32_splitk_workspace_size": ([_i64, _i64, _i64, _i], _sz),
+    "t2s_gemm_f32_splitk": ([_i64, _i64, _i64, _p, _p, _p, _i, _p, _sz, _p], _i),
     "t2s_gemm_f32_tf32x3_workspace_size": ([_i64, _i64, _i64], _sz),
     "t2s_gemm_f32_tf32x3": ([_i64, _i64, _i64, _p, _p, _p, _p, _sz, _p], _i),
     "t2s_gemm_f32_tf32x3_noalloc": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
@@ -87,6 +89,14 @@ def t2s_gemm_f32_naive(M, N, K, A, B, C, stream=0) -> int:
 
 def t2s_gemm_f32_smem32(M, N, K, A, B, C, stream=0) -> int:
     return lib().t2s_gemm_f32_smem32(M, N, K, A, B, C, stream)
+
+
+def t2s_gemm_f32_splitk_workspace_size(M, N, K, splits=0) -> int:
+    return lib().t2s_gemm_f32_splitk_workspace_size(M, N, K, splits)
+
+
+def t2s_gemm_f32_splitk(M, N, K, A, B, C, splits, workspace, workspace_bytes, stream=0) -> int:
+    return lib().t2s_gemm_f32_splitk(M, N, K, A, B, C, splits, workspace, workspace_bytes, stream)
 
 
 def t2s_gemm_f32_tf32x3_workspace_size(M, N, K) -> int:

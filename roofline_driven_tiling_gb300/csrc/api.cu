@@ -135,6 +135,34 @@ int t2s_gemm_f32_smem32(int64_t M, int64_t N, int64_t K, const float* A, const f
   return gemm_common(launch_smem32, M, N, K, A, B, C, stream);
 }
 
+size_t t2s_gemm_f32_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int splits) {
+  if (M < 0 || N < 0 || K < 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return 0;
+  if (splits > 64) return 0;
+  if (splits <= 0) splits = splitk_auto(M, N, K);
+  const int planes = K > 0 ? splitk_planes(K, splits) : 1;
+  return planes <= 1 ? 0 : static_cast<size_t>(planes) * M * N * sizeof(float);
+}
+
+int t2s_gemm_f32_splitk(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+                        int splits, void* workspace, size_t workspace_bytes, t2s_stream_t stream) {
+  if (splits > 64) return T2S_ERR_INVALID;
+  Problem p{};
+  bool noop = false;
+  const int rc = prepare(M, N, K, A, B, C, stream, &p, &noop);
+  if (rc != T2S_OK || noop) return rc;
+  if (K == 0) return zero_fill(p);
+  if (splits <= 0) splits = splitk_auto(M, N, K);
+  const int planes = splitk_planes(K, splits);
+  if (planes > 1) {
+    const size_t need = static_cast<size_t>(planes) * M * N * sizeof(float);
+    if (workspace == nullptr || workspace_bytes < need) return T2S_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return T2S_ERR_WORKSPACE;
+  }
+  const cudaError_t e = planes > 1 ? launch_ffma_splitk(p, splits, static_cast<float*>(workspace))
+                                   : launch_ffma(p);
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
 size_t t2s_gemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return 0;
   return tf32x3_workspace_bytes(M, N, K);

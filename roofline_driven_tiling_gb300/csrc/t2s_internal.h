@@ -28,6 +28,11 @@ struct Problem {
 cudaError_t launch_naive(const Problem& p);
 cudaError_t launch_smem32(const Problem& p);
 cudaError_t launch_ffma(const Problem& p);
+// Split K: `splits` requested chunks (>= 1); partial products in `workspace`
+// (splitk_planes(K, splits) planes of M x N floats), summed into p.C in plane order.
+int splitk_auto(int64_t M, int64_t N, int64_t K);
+int splitk_planes(int64_t K, int splits);
+cudaError_t launch_ffma_splitk(const Problem& p, int splits, float* workspace);
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tf32x3(const Problem& p, void* workspace);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);

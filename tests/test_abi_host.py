@@ -121,3 +121,16 @@ def test_vector_add_rejects_bad_arguments(lib):
     assert f(8, fake + 2, fake + 64, fake + 128) == binding.T2S_ERR_INVALID
     assert f(8, fake, fake + 64, fake) == binding.T2S_ERR_INVALID  # z aliases x
     assert f(0, 0, 0, 0) == binding.T2S_OK
+
+
+def test_splitk_workspace_size_and_arguments(lib):
+    ws = binding.t2s_gemm_f32_splitk_workspace_size
+    assert ws(1024, 512, 4096, 4) == 4 * 1024 * 512 * 4
+    assert ws(1024, 512, 4096, 1) == 0  # one chunk: no partial planes
+    assert ws(16, 16, 40, 8) == 2 * 16 * 16 * 4  # chunks round up to 32 values: 2 planes
+    assert ws(16, 16, 40, 65) == 0 and ws(-1, 2, 3, 2) == 0
+    fake = 1 << 20
+    assert binding.t2s_gemm_f32_splitk(4, 4, 4, fake, fake + 64, fake + 128, 65, fake, 1 << 20, 0) == \
+        binding.T2S_ERR_INVALID
+    assert binding.t2s_gemm_f32_splitk(-1, 4, 4, fake, fake + 64, fake + 128, 2, fake, 1 << 20, 0) == \
+        binding.T2S_ERR_INVALID

@@ -431,3 +431,71 @@ def test_every_configuration(name, ragged):
     rows, cols = sample_positions(M, N, np.random.default_rng(K))
     want = oracle.sgemm_at(A, B, rows, cols, oracle.FMA)
     assert bits_equal(C[rows, cols], want), mismatch(C[rows, cols], want)
+
+
+# ------------------------------------------------------------------ split K
+def run_splitk(A, B, splits, shift=0):
+    M, K = A.shape
+    N = B.shape[1]
+    dA = Guarded(A, np.nan, shift)
+    dB = Guarded(B, np.nan, shift)
+    dC = Guarded(np.full((M, N), C_SENTINEL, np.float32), C_SENTINEL, shift)
+    need = binding.t2s_gemm_f32_splitk_workspace_size(M, N, K, splits)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    rc = binding.t2s_gemm_f32_splitk(M, N, K, dA.ptr, dB.ptr, dC.ptr, splits, ws.data_ptr(),
+                                     ws.numel(), s)
+    assert rc == binding.T2S_OK, binding.status_string(rc)
+    assert binding.t2s_device_status(s) == binding.T2S_OK
+    assert dC.guards_intact(C_SENTINEL)
+    return dC.data()
+
+
+@pytest.mark.parametrize("shape,splits", [((1024, 1024, 1024), 0), ((512, 512, 512), 0),
+                                          ((256, 256, 4096), 0), ((1000, 1003, 997), 0),
+                                          ((300, 130, 1000), 3), ((64, 64, 2048), 64),
+                                          ((129, 257, 33), 2)],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_splitk_within_tolerance(shape, splits):
+    M, N, K = shape
+    A = inputs.uniform(M, K, 71 + M)
+    B = inputs.uniform(K, N, 73 + N)
+    C = run_splitk(A, B, splits)
+    for mode in (oracle.FMA, oracle.MUL_ADD):
+        ref = oracle.sgemm(A, B, mode)
+        assert float(np.max(np.abs(C - ref))) <= tolerance(A, B)
+    assert bits_equal(run_splitk(A, B, splits), C)  # deterministic
+
+
+def test_splitk_one_chunk_is_the_product():
+    A, B = inputs.uniform_pair(300, 200, 500, 15)
+    assert bits_equal(run_splitk(A, B, 1), run("ffma", A, B))
+
+
+def test_splitk_integer_pattern_exact_and_misaligned():
+    A, B = inputs.integer_pattern(512, 512, 1024)
+    C = run_splitk(A, B, 4)
+    assert bits_equal(C, oracle.sgemm(A, B, oracle.FMA))  # exact sums in any order
+    A, B = inputs.uniform_pair(257, 131, 999, 16)
+    C = run_splitk(A, B, 5, shift=1)
+    assert float(np.max(np.abs(C - oracle.sgemm(A, B, oracle.MUL_ADD)))) <= tolerance(A, B)
+
+
+def test_splitk_workspace_checks():
+    M, N, K = 256, 256, 1024
+    dA = torch.zeros((M, K), device="cuda")
+    dB = torch.zeros((K, N), device="cuda")
+    dC = torch.zeros((M, N), device="cuda")
+    need = binding.t2s_gemm_f32_splitk_workspace_size(M, N, K, 4)
+    assert need == 4 * M * N * 4
+    ws = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    f = binding.t2s_gemm_f32_splitk
+    args = (M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), 4)
+    assert f(*args, 0, need, s) == binding.T2S_ERR_WORKSPACE
+    assert f(*args, ws.data_ptr(), need - 4, s) == binding.T2S_ERR_WORKSPACE
+    assert f(*args, ws.data_ptr() + 4, need, s) == binding.T2S_ERR_WORKSPACE
+    assert f(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), 65, ws.data_ptr(), need, s) == \
+        binding.T2S_ERR_INVALID
+    assert f(*args, ws.data_ptr(), need, s) == binding.T2S_OK
+    assert binding.t2s_device_status(s) == binding.T2S_OK
