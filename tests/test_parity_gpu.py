@@ -328,7 +328,8 @@ def test_tf32x3_sweep_and_long_k_sampled(shape):
 
 # ------------------------------------------------------------------ host-memory entry point
 @pytest.mark.parametrize("shape", [(4096, 4096, 4096), (1000, 1003, 997), (1537, 260, 129),
-                                   (3, 5, 0), (600, 17, 33)],
+                                   (3, 5, 0), (600, 17, 33), (2100, 130, 1001), (2048, 96, 600),
+                                   (3072, 64, 4096)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_host_pipeline_equals_device_entry(shape):
     """Row-blocked, copy-overlapped product of host matrices: the bits of t2s_gemm_f32."""
