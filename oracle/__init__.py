@@ -67,6 +67,12 @@ class Oracle:
         lib.t2s_oracle_set_num_threads.restype = None
         lib.t2s_oracle_vector_add.argtypes = [i64, fp, fp, fp]
         lib.t2s_oracle_vector_add.restype = ip
+        lib.t2s_oracle_bf16_to_f32.argtypes = [i64, fp, fp]
+        lib.t2s_oracle_bf16_to_f32.restype = ip
+        lib.t2s_oracle_dgemm.argtypes = [i64, i64, i64, fp, fp, fp, ip]
+        lib.t2s_oracle_dgemm.restype = ip
+        lib.t2s_oracle_dgemm_at.argtypes = [i64, i64, i64, fp, fp, i64, fp, fp, fp, ip]
+        lib.t2s_oracle_dgemm_at.restype = ip
         self.lib = lib
 
     def vector_add(self, x: np.ndarray, y: np.ndarray) -> np.ndarray:
@@ -120,10 +126,65 @@ class Oracle:
         return out
 
 
+    def bf16_to_f32(self, bits: np.ndarray) -> np.ndarray:
+        """Widen bfloat16 bit patterns (uint16) to the float32 values they encode."""
+        bits = np.ascontiguousarray(bits)
+        if bits.dtype != np.uint16:
+            raise TypeError("bfloat16 inputs must be uint16 bit patterns, got %s" % bits.dtype)
+        out = np.empty(bits.shape, dtype=np.float32)
+        if self.lib.t2s_oracle_bf16_to_f32(bits.size, bits.ctypes.data, out.ctypes.data) != 0:
+            raise ValueError("oracle rejected the arguments")
+        return out
+
+    def gemm_bf16(self, A_bits: np.ndarray, B_bits: np.ndarray) -> np.ndarray:
+        """C (float32) = A x B for bfloat16 A, B: the FP32 definition on the widened values."""
+        return self.sgemm(self.bf16_to_f32(A_bits), self.bf16_to_f32(B_bits), MUL_ADD)
+
+    def gemm_bf16_at(self, A_bits, B_bits, rows, cols) -> np.ndarray:
+        """Elements C[rows[s], cols[s]] of the bfloat16 product, one by one."""
+        return self.sgemm_at(self.bf16_to_f32(A_bits), self.bf16_to_f32(B_bits), rows, cols,
+                             MUL_ADD)
+
+    def dgemm(self, A: np.ndarray, B: np.ndarray, mode: int = MUL_ADD) -> np.ndarray:
+        """Full FP64 product C = A x B (float64, row-major)."""
+        A, B = _f64(A), _f64(B)
+        M, N, K = _shapes(A, B)
+        C = np.empty((M, N), dtype=np.float64)
+        rc = self.lib.t2s_oracle_dgemm(M, N, K, A.ctypes.data, B.ctypes.data, C.ctypes.data,
+                                       mode)
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments")
+        return C
+
+    def dgemm_at(self, A: np.ndarray, B: np.ndarray, rows, cols,
+                 mode: int = MUL_ADD) -> np.ndarray:
+        """Elements C[rows[s], cols[s]] of the FP64 product, one by one."""
+        A, B = _f64(A), _f64(B)
+        M, N, K = _shapes(A, B)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        if rows.shape != cols.shape or rows.ndim != 1:
+            raise ValueError("rows and cols must be 1-D and of equal length")
+        out = np.empty(rows.shape[0], dtype=np.float64)
+        rc = self.lib.t2s_oracle_dgemm_at(M, N, K, A.ctypes.data, B.ctypes.data,
+                                          rows.shape[0], rows.ctypes.data, cols.ctypes.data,
+                                          out.ctypes.data, mode)
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments")
+        return out
+
+
 def _f32(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x)
     if x.dtype != np.float32:
         raise TypeError("oracle inputs must be float32, got %s" % x.dtype)
+    return x
+
+
+def _f64(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.float64:
+        raise TypeError("FP64 oracle inputs must be float64, got %s" % x.dtype)
     return x
 
 
@@ -155,6 +216,26 @@ def sgemm_rows(A, B, r0: int, r1: int, mode: int = MUL_ADD) -> np.ndarray:
 
 def vector_add(x, y) -> np.ndarray:
     return default().vector_add(x, y)
+
+
+def bf16_to_f32(bits) -> np.ndarray:
+    return default().bf16_to_f32(bits)
+
+
+def gemm_bf16(A_bits, B_bits) -> np.ndarray:
+    return default().gemm_bf16(A_bits, B_bits)
+
+
+def gemm_bf16_at(A_bits, B_bits, rows, cols) -> np.ndarray:
+    return default().gemm_bf16_at(A_bits, B_bits, rows, cols)
+
+
+def dgemm(A, B, mode: int = MUL_ADD) -> np.ndarray:
+    return default().dgemm(A, B, mode)
+
+
+def dgemm_at(A, B, rows, cols, mode: int = MUL_ADD) -> np.ndarray:
+    return default().dgemm_at(A, B, rows, cols, mode)
 
 
 def num_threads() -> int:

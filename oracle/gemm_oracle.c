@@ -41,6 +41,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <string.h>
 
 #ifdef _OPENMP
 #include <omp.h>
@@ -160,6 +161,89 @@ int t2s_oracle_vector_add(int64_t n, const float *x, const float *y, float *z)
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
         z[i] = x[i] + y[i];
+    }
+    return 0;
+}
+
+/*
+ * Element types other than FP32. The pages write both kernels for a template element
+ * type T (page "GEMM 커널 테스트 코드 작성 및 최적화 (1024^3 크기 실험)", sections
+ * "Naive GEMM 커널 동작 방식" and "Shared Memory Tiled GEMM 연산 방식"); the oracle
+ * gives the same definition for two more types.
+ *
+ * bfloat16 operands. A bfloat16 number is stored as the upper 16 bits of the IEEE
+ * binary32 encoding of the same number: 1 sign bit, the 8 binary32 exponent bits and the
+ * top 7 fraction bits (the format of Google's TPUs and of Intel's "BFLOAT16 - Hardware
+ * Numerics Definition", 2018). Widening to binary32 is therefore exact: the 16 bits become
+ * the high half of the binary32 encoding and the low half is zero. The product of two
+ * bfloat16 numbers has at most 16 significant bits and fits binary32 exactly, so the
+ * definition with bfloat16 inputs and an FP32 accumulator is the FP32 definition above
+ * applied to the widened inputs (and MUL_ADD and FMA agree on it).
+ * Returns 0, or -1 if n is negative.
+ */
+int t2s_oracle_bf16_to_f32(int64_t n, const uint16_t *x, float *y)
+{
+    if (n < 0) return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const uint32_t bits = (uint32_t)x[i] << 16;
+        memcpy(&y[i], &bits, sizeof(float));
+    }
+    return 0;
+}
+
+/* One FP64 output element: the definition at the top with T = double. */
+static double dot_row_col_f64(int64_t N, int64_t K, const double *A, const double *B,
+                              int64_t i, int64_t j, int mode)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double a = A[i * K + k];
+        const double b = B[k * N + j];
+        if (mode == T2S_ORACLE_FMA) {
+            acc = fma(a, b, acc);
+        } else {
+            const double p = a * b; /* rounded to FP64 here */
+            acc = acc + p;          /* and rounded again here */
+        }
+    }
+    return acc;
+}
+
+/*
+ * FP64 full product: C (M x N) = A (M x K) x B (K x N), row-major binary64, one FP64
+ * accumulator per element in ascending k (the FP32 definition with T = double).
+ * Returns 0, or -1 if a dimension is negative or mode is unknown.
+ */
+int t2s_oracle_dgemm(int64_t M, int64_t N, int64_t K, const double *A, const double *B,
+                     double *C, int mode)
+{
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (mode != T2S_ORACLE_MUL_ADD && mode != T2S_ORACLE_FMA) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            C[i * N + j] = dot_row_col_f64(N, K, A, B, i, j, mode);
+        }
+    }
+    return 0;
+}
+
+/*
+ * FP64 sampled product: out[s] = C[rows[s], cols[s]], each by the FP64 definition.
+ * Returns 0, or -1 on a bad argument (negative sizes, an index out of range, unknown mode).
+ */
+int t2s_oracle_dgemm_at(int64_t M, int64_t N, int64_t K, const double *A, const double *B,
+                        int64_t n_samples, const int64_t *rows, const int64_t *cols,
+                        double *out, int mode)
+{
+    if (M < 0 || N < 0 || K < 0 || n_samples < 0) return -1;
+    if (mode != T2S_ORACLE_MUL_ADD && mode != T2S_ORACLE_FMA) return -1;
+    for (int64_t s = 0; s < n_samples; ++s) {
+        if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t s = 0; s < n_samples; ++s) {
+        out[s] = dot_row_col_f64(N, K, A, B, rows[s], cols[s], mode);
     }
     return 0;
 }

@@ -87,6 +87,36 @@ def dyadic(rows: int, cols: int, seed: int, denom: int = 16, span: int = 32) -> 
     return (j.astype(np.float64) / denom).astype(np.float32).reshape(rows, cols)
 
 
+def uniform_f64(rows: int, cols: int, seed: int) -> np.ndarray:
+    """rows x cols float64 matrix, i.i.d. on the 2**-52 grid of [-1, 1): output s of the
+    stream gives ``(u >> 11) * 2**-52 - 1`` (53 random bits, exact in binary64)."""
+    n = int(rows) * int(cols)
+    out = np.empty(n, dtype=np.float64)
+    chunk = 1 << 24
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        u = splitmix64(seed, e - s, start=s)
+        hi = (u >> np.uint64(11)).astype(np.int64)  # 53 random bits, < 2**53
+        out[s:e] = hi.astype(np.float64) * 2.0 ** -52 - 1.0
+    return out.reshape(rows, cols)
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """uint16 bfloat16 bit patterns of float32 values that bfloat16 holds exactly (the upper
+    half of each binary32 encoding). Raises ValueError for a value bfloat16 cannot hold."""
+    v = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    if np.any(v & np.uint32(0xFFFF)):
+        raise ValueError("a value is not representable in bfloat16")
+    return (v >> np.uint32(16)).astype(np.uint16)
+
+
+def uniform_bf16(rows: int, cols: int, seed: int) -> np.ndarray:
+    """rows x cols bfloat16 bit patterns: the ``uniform`` values with the low 16 bits of each
+    binary32 encoding cleared (the value moved toward zero onto the bfloat16 grid)."""
+    v = uniform(rows, cols, seed).view(np.uint32)
+    return (v >> np.uint32(16)).astype(np.uint16)
+
+
 # The workloads: (name, M, N, K, kind, config number).
 CONFIGS = {
     "c1_int_256": (256, 256, 256, "integer", 1),

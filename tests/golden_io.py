@@ -22,19 +22,33 @@ def page_figures() -> dict:
     return out
 
 
-def rounding_cases() -> list:
-    """[(name, A, B, C_mul_add, C_fma)] from rounding_cases.txt, as float32 arrays."""
+def rounding_cases(fname: str = "rounding_cases.txt", dtype=np.float32) -> list:
+    """[(name, A, B, C_mul_add, C_fma)] from a rounding-case fixture, as arrays of `dtype`."""
     cases = []
-    with open(os.path.join(GOLDEN, "rounding_cases.txt"), encoding="utf-8") as f:
+    with open(os.path.join(GOLDEN, fname), encoding="utf-8") as f:
         for line in f:
             line = line.strip()
             if not line or line.startswith("#"):
                 continue
             name, dims, a, b, c0, c1 = (t.strip() for t in line.split("|"))
             M, N, K = (int(t) for t in dims.split())
-            A = np.array([float.fromhex(t) for t in a.split()], dtype=np.float32).reshape(M, K)
-            B = np.array([float.fromhex(t) for t in b.split()], dtype=np.float32).reshape(K, N)
-            C0 = np.array([float.fromhex(t) for t in c0.split()], dtype=np.float32).reshape(M, N)
-            C1 = np.array([float.fromhex(t) for t in c1.split()], dtype=np.float32).reshape(M, N)
+            A = np.array([float.fromhex(t) for t in a.split()], dtype=dtype).reshape(M, K)
+            B = np.array([float.fromhex(t) for t in b.split()], dtype=dtype).reshape(K, N)
+            C0 = np.array([float.fromhex(t) for t in c0.split()], dtype=dtype).reshape(M, N)
+            C1 = np.array([float.fromhex(t) for t in c1.split()], dtype=dtype).reshape(M, N)
             cases.append((name, A, B, C0, C1))
     return cases
+
+
+def bf16_values() -> list:
+    """[(bits, value)] from bf16_values.txt; value is a Python float (inf / nan included)."""
+    out = []
+    with open(os.path.join(GOLDEN, "bf16_values.txt"), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            bits, value, _ = (t.strip() for t in line.split("|", 2))
+            v = {"inf": float("inf"), "-inf": float("-inf"), "nan": float("nan")}.get(value)
+            out.append((int(bits, 16), float.fromhex(value) if v is None else v))
+    return out
