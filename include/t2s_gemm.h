@@ -1,7 +1,8 @@
 /*
  * t2s_gemm.h -- C ABI of the GB300 (sm_103a) FP32 matrix-multiply library.
  *
- * Operation (all entry points): C = A x B in IEEE binary32, row-major, dense.
+ * Operation (all entry points): C = A x B in IEEE binary32, row-major, dense
+ * (t2s_gemm_bf16_f32 takes bfloat16 A and B and writes a binary32 C).
  *
  *   A is M x K, element (row, k)   at A[row * K + k]
  *   B is K x N, element (k, col)   at B[k * N + col]
@@ -201,6 +202,31 @@ int t2s_gemm_f32_tf32x3(int64_t M, int64_t N, int64_t K, const float *A,
 #define T2S_TF32X3_NOALLOC_MAX_SCRATCH ((size_t)32 << 20)
 int t2s_gemm_f32_tf32x3_noalloc(int64_t M, int64_t N, int64_t K, const float *A,
                                 const float *B, float *C, t2s_stream_t stream);
+
+/*
+ * BF16 element type on the tcgen05 tensor cores: C (FP32) = A x B with A and B in bfloat16.
+ * The pages write their kernels for a template element type T (page "GEMM 커널 테스트 코드
+ * 작성 및 최적화 (1024^3 크기 실험)", sections "Naive GEMM 커널 동작 방식" and "Shared
+ * Memory Tiled GEMM 연산 방식"); this is the 16-bit instance on GB300's tensor cores, with FP32
+ * accumulation (tcgen05.mma kind::f16, BF16 operands).
+ *
+ * Layout: A is M x K and B is K x N, row-major, dense, as uint16_t bit patterns of IEEE-style
+ * bfloat16 (the upper 16 bits of a binary32); C is M x N row-major FP32. Every product of two
+ * bfloat16 values is exact in FP32, so C differs from the FP32 definition applied to the
+ * bfloat16 values only in the order of the FP32 additions: exact wherever all products and
+ * partial sums are (for example small integers); otherwise
+ * max |C - sum_k a*b| <= 1e-6 * K * max|a| * max|b|.
+ *
+ * A and B must be 2-byte aligned, C 4-byte aligned. When K % 8 == 0 and A is 16-byte aligned,
+ * A is read in place; otherwise it is first copied into a padded plane of the workspace.
+ * `workspace` is a DEVICE buffer, 256-byte aligned, of at least
+ * t2s_gemm_bf16_f32_workspace_size(M, N, K) bytes, owned by the caller, holding B transposed
+ * (and A padded); it must not overlap A, B or C and must stay untouched until the stream has
+ * run the call. Otherwise the common contract and return codes above apply.
+ */
+size_t t2s_gemm_bf16_f32_workspace_size(int64_t M, int64_t N, int64_t K);
+int t2s_gemm_bf16_f32(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B,
+                      float *C, void *workspace, size_t workspace_bytes, t2s_stream_t stream);
 
 /*
  * Memory-roof probe: z[i] = x[i] + y[i] for i < n, FP32, one IEEE add (round to nearest)

@@ -43,24 +43,33 @@ cudaError_t status_word(unsigned** out) {
   return cudaSuccess;
 }
 
-bool misaligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; }
+bool misaligned(const void* p, uintptr_t bytes) {
+  return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) != 0;
+}
 
-// Checks the common contract; on success fills `p` and returns T2S_OK. `*noop` is set
-// when there is nothing to compute (M == 0 or N == 0).
-int prepare(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
-            t2s_stream_t stream, Problem* p, bool* noop) {
+// The checks every GEMM entry point shares, for operands of `ab_bytes`-byte elements (A, B)
+// and an FP32 C. Sets `*noop` when there is nothing to compute (M == 0 or N == 0).
+int validate(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
+             uintptr_t ab_bytes, bool* noop) {
   if (M < 0 || N < 0 || K < 0) return T2S_ERR_INVALID;
   if (M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return T2S_ERR_INVALID;
   const bool has_a = M > 0 && K > 0, has_b = K > 0 && N > 0, has_c = M > 0 && N > 0;
   if ((has_a && A == nullptr) || (has_b && B == nullptr) || (has_c && C == nullptr))
     return T2S_ERR_INVALID;
-  if ((has_a && misaligned4(A)) || (has_b && misaligned4(B)) || (has_c && misaligned4(C)))
+  if ((has_a && misaligned(A, ab_bytes)) || (has_b && misaligned(B, ab_bytes)) ||
+      (has_c && misaligned(C, 4)))
     return T2S_ERR_INVALID;
-  if (has_c && ((has_a && static_cast<const void*>(C) == A) ||
-                (has_b && static_cast<const void*>(C) == B)))
-    return T2S_ERR_INVALID;
+  if (has_c && ((has_a && C == A) || (has_b && C == B))) return T2S_ERR_INVALID;
   *noop = !has_c;
-  if (*noop) return T2S_OK;
+  return T2S_OK;
+}
+
+// Checks the common contract; on success fills `p` and returns T2S_OK. `*noop` is set
+// when there is nothing to compute (M == 0 or N == 0).
+int prepare(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+            t2s_stream_t stream, Problem* p, bool* noop) {
+  const int rc = validate(M, N, K, A, B, C, 4, noop);
+  if (rc != T2S_OK || *noop) return rc;
   p->M = M;
   p->N = N;
   p->K = K;
@@ -179,6 +188,32 @@ int t2s_gemm_f32_tf32x3(int64_t M, int64_t N, int64_t K, const float* A, const f
   if (workspace == nullptr || workspace_bytes < need) return T2S_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return T2S_ERR_WORKSPACE;
   const cudaError_t e = launch_tf32x3(p, workspace);
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
+size_t t2s_gemm_bf16_f32_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return 0;
+  return bf16_workspace_bytes(M, N, K);
+}
+
+int t2s_gemm_bf16_f32(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
+                      float* C, void* workspace, size_t workspace_bytes, t2s_stream_t stream) {
+  bool noop = false;
+  const int rc = validate(M, N, K, A, B, C, 2, &noop);
+  if (rc != T2S_OK || noop) return rc;
+  Problem p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.C = C;
+  p.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = status_word(&p.status);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (K == 0) return zero_fill(p);
+  const size_t need = bf16_workspace_bytes(M, N, K);
+  if (workspace == nullptr || workspace_bytes < need) return T2S_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return T2S_ERR_WORKSPACE;
+  e = launch_bf16(M, N, K, A, B, C, workspace, p.stream, p.status);
   return e == cudaSuccess ? T2S_OK : fail_cuda(e);
 }
 

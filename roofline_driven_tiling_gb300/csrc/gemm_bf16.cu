@@ -1,0 +1,145 @@
+// gemm_bf16.cu -- C (FP32) = A x B with BF16 inputs on the tcgen05 tensor cores.
+//
+// The element type of the operands is a template parameter on the pages' kernels; this is
+// the 16-bit case on the tensor cores of GB300 (kind::f16 with BF16 operands, FP32
+// accumulation). Products of two BF16 values are exact in FP32, so the result differs from
+// the FP32 definition applied to the BF16 values (converted exactly to FP32) only by the
+// order of the FP32 additions.
+//
+// 1. Pre-pass: B (K x N, row-major) is transposed into an N x Kp plane (Kp = ceil(K / 64) x 64,
+//    zeros beyond K), K-major as the tensor core reads it. A (M x K, row-major) is already
+//    K-major and is read in place when its rows are a multiple of 16 bytes (K % 8 == 0) and
+//    it is 16-byte aligned; otherwise it is copied into an M x Kp plane first.
+// 2. The persistent tcgen05 kernel of tc_gemm.cuh: one MMA (M = 128, N = BN, K = 16) per k
+//    step, K chunks of 512 accumulated in TMEM and added into FP32 registers with
+//    round-to-nearest by the epilogue warps.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "t2s_device.cuh"
+#include "t2s_internal.h"
+#include "t2s_tmap.h"
+#include "tc_gemm.cuh"
+
+namespace t2s {
+namespace {
+
+constexpr int64_t kKPad16 = 64;
+
+int64_t padded_k16(int64_t K) { return (K + kKPad16 - 1) / kKPad16 * kKPad16; }
+
+size_t up256b(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// B (K x N bf16, row-major) -> Bt (N x Kp bf16), zeros for k >= K; 32 x 32 tiles through
+// shared memory so that reads (along n) and writes (along k) are coalesced.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ B,
+                                                             uint16_t* __restrict__ Bt, int64_t K,
+                                                             int64_t N, int64_t Kp) {
+  __shared__ uint16_t tile[32][34];
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 32;
+  for (int64_t kt = blockIdx.y; kt * 32 < Kp; kt += gridDim.y) {
+    const int64_t k0 = kt * 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t k = k0 + ty + 8 * i, n = n0 + tx;
+      tile[ty + 8 * i][tx] = (k < K && n < N) ? B[k * N + n] : static_cast<uint16_t>(0);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t n = n0 + ty + 8 * i, k = k0 + tx;
+      if (n < N) Bt[n * Kp + k] = tile[tx][ty + 8 * i];
+    }
+    __syncthreads();
+  }
+}
+
+// A (M x K bf16) -> Ap (M x Kp bf16), zeros for k >= K.
+__global__ void __launch_bounds__(256) pad_rows_bf16_kernel(const uint16_t* __restrict__ A,
+                                                            uint16_t* __restrict__ Ap, int64_t M,
+                                                            int64_t K, int64_t Kp) {
+  const int64_t total = M * Kp;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / Kp, k = i % Kp;
+    Ap[i] = k < K ? A[row * K + k] : static_cast<uint16_t>(0);
+  }
+}
+
+// Tile widths BN (M is 128), BK = 64 (128-byte rows): wider tiles read A less per FLOP.
+using Bf16N128 = tc::TcConfig<tc::kBf16, 128, 64, 6, 512>;  // 6 stages of 32 KB
+using Bf16N192 = tc::TcConfig<tc::kBf16, 192, 64, 4, 512>;  // 4 stages of 40 KB
+using Bf16N224 = tc::TcConfig<tc::kBf16, 224, 64, 4, 512>;  // 4 stages of 44 KB
+using Bf16N256 = tc::TcConfig<tc::kBf16, 256, 64, 4, 512>;  // 4 stages of 48 KB
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// Bt plane (N x Kp) and, when A cannot be read in place, an A plane (M x Kp): 2 bytes each,
+// both counted so the size does not depend on the pointers.
+size_t bf16_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int64_t Kp = padded_k16(K);
+  return up256b(static_cast<size_t>(N) * Kp * 2) + up256b(static_cast<size_t>(M) * Kp * 2);
+}
+
+cudaError_t launch_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
+                        float* C, void* workspace, cudaStream_t stream, unsigned* status) {
+  const int64_t Kp = padded_k16(K);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  uint16_t* bt = reinterpret_cast<uint16_t*>(w);
+  uint16_t* ap = reinterpret_cast<uint16_t*>(w + up256b(static_cast<size_t>(N) * Kp * 2));
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  {
+    const int64_t gy = Kp / 32;
+    const dim3 grid(static_cast<unsigned>((N + 31) / 32),
+                    static_cast<unsigned>(gy < 65535 ? gy : 65535));
+    transpose_bf16_kernel<<<grid, dim3(32, 8), 0, stream>>>(B, bt, K, N, Kp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const bool a_in_place = K % 8 == 0 && aligned16(A);
+  const uint16_t* a = A;
+  int64_t lda = K;
+  if (!a_in_place) {
+    const int64_t work = M * Kp;
+    const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(sms) * 16);
+    pad_rows_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(A, ap, M, K, Kp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    a = ap;
+    lda = Kp;
+  }
+  Problem p{M, N, K, nullptr, nullptr, C, stream, status};
+  // Width by balanced persistent rounds, as for the 3xTF32 kernel.
+  const int widths[4] = {128, 192, 224, 256};
+  const double weight[4] = {1.15, 1.03, 1.01, 1.0};
+  const int64_t tm = (M + 127) / 128;
+  int best = 0;
+  double best_cost = 0.0;
+  for (int i = 0; i < 4; ++i) {
+    const int64_t tiles = tm * ((N + widths[i] - 1) / widths[i]);
+    const int64_t rounds = (tiles + sms - 1) / sms;
+    const double cost = static_cast<double>(rounds) * widths[i] * weight[i];
+    if (i == 0 || cost < best_cost) {
+      best = i;
+      best_cost = cost;
+    }
+  }
+#ifdef BF16_FORCE_WIDTH
+  best = BF16_FORCE_WIDTH;
+#endif
+  switch (best) {
+    case 1: return tc::run_tc<Bf16N192>(p, a, nullptr, bt, nullptr, lda, Kp, Kp);
+    case 2: return tc::run_tc<Bf16N224>(p, a, nullptr, bt, nullptr, lda, Kp, Kp);
+    case 3: return tc::run_tc<Bf16N256>(p, a, nullptr, bt, nullptr, lda, Kp, Kp);
+    default: return tc::run_tc<Bf16N128>(p, a, nullptr, bt, nullptr, lda, Kp, Kp);
+  }
+}
+
+}  // namespace t2s

@@ -35,6 +35,10 @@ int splitk_planes(int64_t K, int splits);
 cudaError_t launch_ffma_splitk(const Problem& p, int splits, float* workspace);
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tf32x3(const Problem& p, void* workspace);
+// BF16 operands (uint16_t bit patterns), FP32 C; workspace for the transposed/padded planes.
+size_t bf16_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
+                        float* C, void* workspace, cudaStream_t stream, unsigned* status);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
 // Records a CUDA error for t2s_last_cuda_error() on this host thread.
 void set_last_cuda_error(cudaError_t e);

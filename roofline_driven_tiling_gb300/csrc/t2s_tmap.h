@@ -18,4 +18,8 @@ namespace t2s {
 cudaError_t encode_tmap_f32_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
                                uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
+// The same for a row-major matrix of 16-bit BF16 elements (row stride = cols * 2 bytes).
+cudaError_t encode_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                                uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle);
+
 }  // namespace t2s

@@ -134,3 +134,20 @@ def test_splitk_workspace_size_and_arguments(lib):
         binding.T2S_ERR_INVALID
     assert binding.t2s_gemm_f32_splitk(-1, 4, 4, fake, fake + 64, fake + 128, 2, fake, 1 << 20, 0) == \
         binding.T2S_ERR_INVALID
+
+
+def test_bf16_workspace_size_and_arguments(lib):
+    ws = binding.t2s_gemm_bf16_f32_workspace_size
+    # B transposed (N x Kp) and a padded A plane (M x Kp), 2 bytes each, Kp = K rounded up to
+    # 64, each plane 256-byte padded.
+    assert ws(4096, 4096, 4096) == 2 * 2 * 4096 * 4096
+    assert ws(128, 64, 997) == 2 * 128 * 1024 + 2 * 64 * 1024
+    assert ws(0, 0, 0) == 0 and ws(-1, 2, 3) == 0
+    assert ws(3, 5, 7) % 256 == 0
+    fake = 1 << 20
+    f = binding.t2s_gemm_bf16_f32
+    assert f(-1, 4, 4, fake, fake + 64, fake + 4096, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
+    assert f(4, 4, 4, fake + 1, fake + 64, fake + 4096, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
+    assert f(4, 4, 4, fake, fake + 64, fake + 4098, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
+    assert f(4, 4, 4, fake, fake + 64, fake, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
+    assert f(0, 4, 4, 0, fake + 64, 0, 0, 0, 0) == binding.T2S_OK  # M = 0: nothing to do
