@@ -39,9 +39,11 @@ L2_FLUSH_BYTES = 256 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FFMA_PROFILE = os.path.join(ROOT, "profiles", "sgemm_ffma_4096.md")
 TF32X3_PROFILE = os.path.join(ROOT, "profiles", "gemm_tf32x3_4096.md")
+BF16_PROFILE = os.path.join(ROOT, "profiles", "gemm_bf16_4096.md")
 KERNEL_SOURCES = {
     "ffma": ["sgemm_ffma.cu", "t2s_device.cuh"],
-    "tf32x3": ["gemm_tf32x3.cu", "t2s_device.cuh"],
+    "tf32x3": ["gemm_tf32x3.cu", "tc_gemm.cuh", "t2s_device.cuh"],
+    "bf16": ["gemm_bf16.cu", "tc_gemm.cuh", "t2s_device.cuh"],
 }
 
 
@@ -339,6 +341,7 @@ def run_ours(args):
     # ---- reported separately: 3xTF32 tensor-core kernel and the 1024^3 shape
     if not args.skip_extras:
         line["tf32x3"] = extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws)
+        line["bf16"] = extra_bf16(lib, M, N, K, stream, flush, args, dev)
         line["also_1024"] = extra_1024(lib, dev, stream, flush, args, ws)
         line["memory_roof"] = extra_vector_add(lib, dev, stream, flush, args)
 
@@ -385,6 +388,44 @@ def extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws):
                          "frac": 3 * flops / t / 1e12 / tf32_peak, "unit": UNIT,
                          "peak_basis": "measured bf16 burst x 1.1/2.25 (nominal tf32:bf16)",
                          "traffic": profile_traffic(TF32X3_PROFILE, "tf32x3")}}
+
+
+def extra_bf16(lib, M, N, K, stream, flush, args, dev):
+    """The BF16-operand product (FP32 accumulation) on the same shape, against the measured
+    dense bf16 tensor peak; the call's B transpose pre-pass is inside the timed region."""
+    import torch
+    from roofline_driven_tiling_gb300 import binding, inputs
+    from roofline_driven_tiling_gb300 import roofline as rl
+    Ab = inputs.uniform_bf16(M, K, inputs.SEED_A_BASE + WORKLOAD["config_no"])
+    Bb = inputs.uniform_bf16(K, N, inputs.SEED_B_BASE + WORKLOAD["config_no"])
+    dA = torch.from_numpy(Ab.view(np.int16)).to(dev)
+    dB = torch.from_numpy(Bb.view(np.int16)).to(dev)
+    dC = torch.empty((M, N), dtype=torch.float32, device=dev)
+    need = lib.t2s_gemm_bf16_f32_workspace_size(M, N, K)
+    wsbuf = torch.empty(need, dtype=torch.uint8, device=dev)
+    sp = stream.cuda_stream
+
+    def step():
+        rc = lib.t2s_gemm_bf16_f32(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
+                                   wsbuf.data_ptr(), need, sp)
+        if rc != 0:
+            raise binding.T2SError(rc, "t2s_gemm_bf16_f32")
+
+    try:
+        times = time_steps(step, args.steps, max(args.warmup, 3), stream, flush)
+    except binding.T2SError as e:
+        return {"unavailable": str(e)}
+    flops = rl.gemm_flops(M, N, K)
+    t = sum(times) / len(times) / 1e3
+    peak = float(measured_peaks().get("bf16_tflops", 1898.5))
+    return {"value": flops / t / 1e12, "unit": UNIT, "ms_per_step": t * 1e3,
+            "workload": "%dx%dx%d, bfloat16 A and B (uniform values cut to bfloat16), FP32 C"
+                        % (M, N, K),
+            "kernel": "t2s_gemm_bf16_f32 (B transpose pre-pass + tcgen05 kind::f16, FP32 acc.)",
+            "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peak,
+                         "frac": flops / t / 1e12 / peak, "unit": UNIT,
+                         "peak_basis": "measured cuBLAS bf16 burst",
+                         "traffic": profile_traffic(BF16_PROFILE, "bf16")}}
 
 
 def extra_1024(lib, dev, stream, flush, args, ws):

@@ -70,11 +70,15 @@ __global__ void __launch_bounds__(256) pad_rows_bf16_kernel(const uint16_t* __re
   }
 }
 
+#ifndef BF16_CHUNK_K
+#define BF16_CHUNK_K 512
+#endif
+
 // Tile widths BN (M is 128), BK = 64 (128-byte rows): wider tiles read A less per FLOP.
-using Bf16N128 = tc::TcConfig<tc::kBf16, 128, 64, 6, 512>;  // 6 stages of 32 KB
-using Bf16N192 = tc::TcConfig<tc::kBf16, 192, 64, 4, 512>;  // 4 stages of 40 KB
-using Bf16N224 = tc::TcConfig<tc::kBf16, 224, 64, 4, 512>;  // 4 stages of 44 KB
-using Bf16N256 = tc::TcConfig<tc::kBf16, 256, 64, 4, 512>;  // 4 stages of 48 KB
+using Bf16N128 = tc::TcConfig<tc::kBf16, 128, 64, 6, BF16_CHUNK_K>;  // 6 stages of 32 KB
+using Bf16N192 = tc::TcConfig<tc::kBf16, 192, 64, 4, BF16_CHUNK_K>;  // 4 stages of 40 KB
+using Bf16N224 = tc::TcConfig<tc::kBf16, 224, 64, 4, BF16_CHUNK_K>;  // 4 stages of 44 KB
+using Bf16N256 = tc::TcConfig<tc::kBf16, 256, 64, 4, BF16_CHUNK_K>;  // 4 stages of 48 KB
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
