@@ -342,6 +342,7 @@ def run_ours(args):
     if not args.skip_extras:
         line["tf32x3"] = extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws)
         line["bf16"] = extra_bf16(lib, M, N, K, stream, flush, args, dev)
+        line["f64"] = extra_f64(lib, stream, flush, args, dev)
         line["also_1024"] = extra_1024(lib, dev, stream, flush, args, ws)
         line["memory_roof"] = extra_vector_add(lib, dev, stream, flush, args)
 
@@ -426,6 +427,34 @@ def extra_bf16(lib, M, N, K, stream, flush, args, dev):
                          "frac": flops / t / 1e12 / peak, "unit": UNIT,
                          "peak_basis": "measured cuBLAS bf16 burst",
                          "traffic": profile_traffic(BF16_PROFILE, "bf16")}}
+
+
+def extra_f64(lib, stream, flush, args, dev):
+    """The FP64 kernels at 2048^3 (uniform binary64 inputs) against the FP64 CUDA-core rate
+    (DFMA units x 2 FLOP x SMs x clock; the units per SM are the measured probe figure)."""
+    import torch
+    from roofline_driven_tiling_gb300 import binding, inputs
+    from roofline_driven_tiling_gb300 import roofline as rl
+    n = 2048
+    dA = torch.from_numpy(inputs.uniform_f64(n, n, 5001)).to(dev)
+    dB = torch.from_numpy(inputs.uniform_f64(n, n, 5002)).to(dev)
+    dC = torch.empty((n, n), dtype=torch.float64, device=dev)
+    sp = stream.cuda_stream
+    out = {"workload": "dgemm 2048^3 fp64, uniform on [-1, 1) (L2 flushed per step)",
+           "peak_tflops": rl.fp64_peak_tflops(), "peak_basis": rl.FP64_PEAK_BASIS}
+    for name in ("ffma", "smem32", "naive"):
+        fn = getattr(lib, binding.KERNELS_F64[name])
+
+        def step(fn=fn):
+            rc = fn(n, n, n, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sp)
+            if rc != 0:
+                raise binding.T2SError(rc, binding.KERNELS_F64[name])
+
+        times = time_steps(step, max(3, min(args.steps // 10, 10)), 3, stream, flush)
+        t = sum(times) / len(times) / 1e3
+        tf = rl.gemm_flops(n, n, n) / t / 1e12
+        out[name] = {"ms": t * 1e3, "tflops": tf, "frac": tf / rl.fp64_peak_tflops()}
+    return out
 
 
 def extra_1024(lib, dev, stream, flush, args, ws):

@@ -2,7 +2,8 @@
  * t2s_gemm.h -- C ABI of the GB300 (sm_103a) FP32 matrix-multiply library.
  *
  * Operation (all entry points): C = A x B in IEEE binary32, row-major, dense
- * (t2s_gemm_bf16_f32 takes bfloat16 A and B and writes a binary32 C).
+ * (t2s_gemm_bf16_f32 takes bfloat16 A and B and writes a binary32 C; the t2s_gemm_f64
+ * entry points work in binary64 throughout).
  *
  *   A is M x K, element (row, k)   at A[row * K + k]
  *   B is K x N, element (k, col)   at B[k * N + col]
@@ -227,6 +228,28 @@ int t2s_gemm_f32_tf32x3_noalloc(int64_t M, int64_t N, int64_t K, const float *A,
 size_t t2s_gemm_bf16_f32_workspace_size(int64_t M, int64_t N, int64_t K);
 int t2s_gemm_bf16_f32(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B,
                       float *C, void *workspace, size_t workspace_bytes, t2s_stream_t stream);
+
+/*
+ * FP64 element type on the CUDA cores: C = A x B in IEEE binary64, the same layout and
+ * definition as the FP32 entry points with T = double (page "GEMM 커널 테스트 코드 작성 및
+ * 최적화 (1024^3 크기 실험)": both kernels there are templates over the element type).
+ *  - t2s_gemm_f64: the product; 32 x 32 CTA tiles staged through shared memory in 16-deep K
+ *    tiles, 2 x 2 register blocks per thread (page "4주차: Roofline과 Tiling", section
+ *    "3. Tiling"), sized for balance across the SMs: GB300's FP64 rate (2 FMA per SM per
+ *    clock) is reached at any tiling.
+ *  - t2s_gemm_f64_naive: one thread per C element, k loop over global memory, 16 x 16 blocks.
+ *  - t2s_gemm_f64_smem32: 32 x 32 shared-memory tiles, one C element per thread.
+ * All three sum each element with one IEEE fused multiply-add (fma) per k in ascending k, so
+ * they are bit-identical to each other and to the definition evaluated with fma(), for every
+ * input. Pointers must be 8-byte aligned; otherwise the common contract and return codes
+ * above apply (K == 0 sets C to +0.0).
+ */
+int t2s_gemm_f64(int64_t M, int64_t N, int64_t K, const double *A, const double *B,
+                 double *C, t2s_stream_t stream);
+int t2s_gemm_f64_naive(int64_t M, int64_t N, int64_t K, const double *A, const double *B,
+                       double *C, t2s_stream_t stream);
+int t2s_gemm_f64_smem32(int64_t M, int64_t N, int64_t K, const double *A, const double *B,
+                        double *C, t2s_stream_t stream);
 
 /*
  * Memory-roof probe: z[i] = x[i] + y[i] for i < n, FP32, one IEEE add (round to nearest)

@@ -38,6 +38,9 @@ SIGNATURES = {
     "t2s_gemm_f32_tf32x3_workspace_size": ([_i64, _i64, _i64], _sz),
     "t2s_gemm_f32_tf32x3": ([_i64, _i64, _i64, _p, _p, _p, _p, _sz, _p], _i),
     "t2s_gemm_f32_tf32x3_noalloc": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
+    "t2s_gemm_f64": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
+    "t2s_gemm_f64_naive": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
+    "t2s_gemm_f64_smem32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_bf16_f32_workspace_size": ([_i64, _i64, _i64], _sz),
     "t2s_gemm_bf16_f32": ([_i64, _i64, _i64, _p, _p, _p, _p, _sz, _p], _i),
     "t2s_vector_add_f32": ([_i64, _p, _p, _p, _p], _i),
@@ -112,6 +115,18 @@ def t2s_gemm_f32_tf32x3(M, N, K, A, B, C, workspace, workspace_bytes, stream=0) 
 def t2s_gemm_f32_tf32x3_noalloc(M, N, K, A, B, C, stream=0) -> int:
     """3xTF32 product with the library's built-in scratch array (no allocation)."""
     return lib().t2s_gemm_f32_tf32x3_noalloc(M, N, K, A, B, C, stream)
+
+
+def t2s_gemm_f64(M, N, K, A, B, C, stream=0) -> int:
+    return lib().t2s_gemm_f64(M, N, K, A, B, C, stream)
+
+
+def t2s_gemm_f64_naive(M, N, K, A, B, C, stream=0) -> int:
+    return lib().t2s_gemm_f64_naive(M, N, K, A, B, C, stream)
+
+
+def t2s_gemm_f64_smem32(M, N, K, A, B, C, stream=0) -> int:
+    return lib().t2s_gemm_f64_smem32(M, N, K, A, B, C, stream)
 
 
 def t2s_gemm_bf16_f32_workspace_size(M, N, K) -> int:
@@ -196,6 +211,39 @@ def gemm(A, B, out=None, kernel: str = "ffma", workspace=None, stream=None):
         rc = fn(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(), stream)
     if rc != T2S_OK:
         raise T2SError(rc, KERNELS[kernel])
+    return out
+
+
+KERNELS_F64 = {
+    "ffma": "t2s_gemm_f64",
+    "naive": "t2s_gemm_f64_naive",
+    "smem32": "t2s_gemm_f64_smem32",
+}
+
+
+def gemm_f64(A, B, out=None, kernel: str = "ffma", stream=None):
+    """C = A @ B for float64 CUDA tensors (row-major); `kernel` as for ``gemm``."""
+    import torch
+    for t, name in ((A, "A"), (B, "B")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float64:
+            raise TypeError("%s must be a float64 CUDA tensor" % name)
+        if t.dim() != 2 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous 2-D (row-major) tensor" % name)
+    if A.shape[1] != B.shape[0]:
+        raise ValueError("shape mismatch: A %s, B %s" % (tuple(A.shape), tuple(B.shape)))
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float64, device=A.device)
+    if (not isinstance(out, torch.Tensor) or out.dtype != torch.float64 or not out.is_cuda
+            or not out.is_contiguous() or tuple(out.shape) != (M, N)):
+        raise ValueError("out must be a contiguous float64 CUDA tensor of %d x %d" % (M, N))
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device).cuda_stream
+    name = KERNELS_F64[kernel]
+    rc = getattr(lib(), name)(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(), stream)
+    if rc != T2S_OK:
+        raise T2SError(rc, name)
     return out
 
 

@@ -48,16 +48,17 @@ bool misaligned(const void* p, uintptr_t bytes) {
 }
 
 // The checks every GEMM entry point shares, for operands of `ab_bytes`-byte elements (A, B)
-// and an FP32 C. Sets `*noop` when there is nothing to compute (M == 0 or N == 0).
+// and a C of `c_bytes`-byte elements. Sets `*noop` when there is nothing to compute (M == 0
+// or N == 0).
 int validate(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
-             uintptr_t ab_bytes, bool* noop) {
+             uintptr_t ab_bytes, bool* noop, uintptr_t c_bytes = 4) {
   if (M < 0 || N < 0 || K < 0) return T2S_ERR_INVALID;
   if (M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return T2S_ERR_INVALID;
   const bool has_a = M > 0 && K > 0, has_b = K > 0 && N > 0, has_c = M > 0 && N > 0;
   if ((has_a && A == nullptr) || (has_b && B == nullptr) || (has_c && C == nullptr))
     return T2S_ERR_INVALID;
   if ((has_a && misaligned(A, ab_bytes)) || (has_b && misaligned(B, ab_bytes)) ||
-      (has_c && misaligned(C, 4)))
+      (has_c && misaligned(C, c_bytes)))
     return T2S_ERR_INVALID;
   if (has_c && ((has_a && C == A) || (has_b && C == B))) return T2S_ERR_INVALID;
   *noop = !has_c;
@@ -215,6 +216,49 @@ int t2s_gemm_bf16_f32(int64_t M, int64_t N, int64_t K, const uint16_t* A, const 
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return T2S_ERR_WORKSPACE;
   e = launch_bf16(M, N, K, A, B, C, workspace, p.stream, p.status);
   return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
+}  // extern "C"
+
+namespace t2s {
+namespace {
+
+using LauncherF64 = cudaError_t (*)(int64_t, int64_t, int64_t, const double*, const double*,
+                                    double*, cudaStream_t);
+
+int gemm_f64_common(LauncherF64 launch, int64_t M, int64_t N, int64_t K, const double* A,
+                    const double* B, double* C, t2s_stream_t stream) {
+  bool noop = false;
+  const int rc = validate(M, N, K, A, B, C, 8, &noop, 8);
+  if (rc != T2S_OK || noop) return rc;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (K == 0) {
+    e = cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * sizeof(double), s);
+  } else {
+    e = launch(M, N, K, A, B, C, s);
+  }
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
+}  // namespace
+}  // namespace t2s
+
+extern "C" {
+
+int t2s_gemm_f64(int64_t M, int64_t N, int64_t K, const double* A, const double* B, double* C,
+                 t2s_stream_t stream) {
+  return t2s::gemm_f64_common(t2s::launch_dgemm, M, N, K, A, B, C, stream);
+}
+
+int t2s_gemm_f64_naive(int64_t M, int64_t N, int64_t K, const double* A, const double* B,
+                       double* C, t2s_stream_t stream) {
+  return t2s::gemm_f64_common(t2s::launch_naive_f64, M, N, K, A, B, C, stream);
+}
+
+int t2s_gemm_f64_smem32(int64_t M, int64_t N, int64_t K, const double* A, const double* B,
+                        double* C, t2s_stream_t stream) {
+  return t2s::gemm_f64_common(t2s::launch_smem32_f64, M, N, K, A, B, C, stream);
 }
 
 const char* t2s_status_string(int status) {

@@ -39,6 +39,13 @@ cudaError_t launch_tf32x3(const Problem& p, void* workspace);
 size_t bf16_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
                         float* C, void* workspace, cudaStream_t stream, unsigned* status);
+// FP64 (binary64) kernels: product, naive and 32 x 32 shared-memory comparison points.
+cudaError_t launch_dgemm(int64_t M, int64_t N, int64_t K, const double* A, const double* B,
+                         double* C, cudaStream_t stream);
+cudaError_t launch_naive_f64(int64_t M, int64_t N, int64_t K, const double* A, const double* B,
+                             double* C, cudaStream_t stream);
+cudaError_t launch_smem32_f64(int64_t M, int64_t N, int64_t K, const double* A, const double* B,
+                              double* C, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
 // Records a CUDA error for t2s_last_cuda_error() on this host thread.
 void set_last_cuda_error(cudaError_t e);

@@ -89,6 +89,18 @@ def fp32_peak_tflops(sms: int = GB300_SMS, mhz: float = GB300_SM_MAX_MHZ,
     return sms * lanes * 2.0 * mhz * 1e6 / 1e12
 
 
+#: FP64 fused multiply-adds per SM per clock on GB300: NVIDIA's nominal 1.25 TFLOP/s FP64 for
+#: the whole GPU is 152 SMs x 2 FMA x 2 FLOP x 2.07 GHz = 1.26 TFLOP/s.
+FP64_FMA_PER_SM_CLK = 2
+FP64_PEAK_BASIS = "152 SMs x 2 FP64 FMA/clk x 2 FLOP x 2070 MHz (nominal 1.25 TFLOP/s)"
+
+
+def fp64_peak_tflops(sms: int = GB300_SMS, mhz: float = GB300_SM_MAX_MHZ,
+                     fma_per_clk: int = FP64_FMA_PER_SM_CLK) -> float:
+    """FP64 CUDA-core peak: SMs x FP64 FMAs per clock x 2 FLOPs x clock, in TFLOP/s."""
+    return sms * fma_per_clk * 2.0 * mhz * 1e6 / 1e12
+
+
 def place(flops: float, seconds: float, nbytes: float, peak_tflops: float,
           bw_gbs: float) -> dict:
     """Place one measured point on the roofline.

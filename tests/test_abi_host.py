@@ -151,3 +151,15 @@ def test_bf16_workspace_size_and_arguments(lib):
     assert f(4, 4, 4, fake, fake + 64, fake + 4098, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
     assert f(4, 4, 4, fake, fake + 64, fake, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
     assert f(0, 4, 4, 0, fake + 64, 0, 0, 0, 0) == binding.T2S_OK  # M = 0: nothing to do
+
+
+@pytest.mark.parametrize("fn", ["t2s_gemm_f64", "t2s_gemm_f64_naive", "t2s_gemm_f64_smem32"])
+def test_f64_entries_reject_bad_arguments(lib, fn):
+    f = getattr(binding, fn)
+    fake = 1 << 20
+    assert f(-1, 4, 4, fake, fake + 256, fake + 512, 0) == binding.T2S_ERR_INVALID
+    assert f(4, 4, 4, fake + 4, fake + 256, fake + 512, 0) == binding.T2S_ERR_INVALID  # 4-aligned
+    assert f(4, 4, 4, fake, fake + 256, fake + 516, 0) == binding.T2S_ERR_INVALID
+    assert f(4, 4, 4, fake, fake + 256, fake, 0) == binding.T2S_ERR_INVALID  # C == A
+    assert f(4, 4, 4, 0, fake + 256, fake + 512, 0) == binding.T2S_ERR_INVALID  # NULL A
+    assert f(0, 4, 4, 0, fake + 256, 0, 0) == binding.T2S_OK  # M = 0: nothing to do
