@@ -6,12 +6,14 @@
 // the FP32 definition applied to the BF16 values (converted exactly to FP32) only by the
 // order of the FP32 additions.
 //
-// 1. Pre-pass: B (K x N, row-major) is transposed into an N x Kp plane (Kp = ceil(K / 64) x 64,
-//    zeros beyond K), K-major as the tensor core reads it. A (M x K, row-major) is already
-//    K-major and is read in place when its rows are a multiple of 16 bytes (K % 8 == 0) and
-//    it is 16-byte aligned; otherwise it is copied into an M x Kp plane first.
+// 1. Operands. A (M x K, row-major) is K-major for the tensor core and is read in place by TMA
+//    when its rows are a multiple of 16 bytes (K % 8 == 0) and it is 16-byte aligned;
+//    otherwise it is first copied into an M x Kp plane (Kp = ceil(K / 64) x 64, zeros beyond
+//    K). B (K x N, row-major) is MN-major for the tensor core; when N % 8 == 0 and B is
+//    16-byte aligned it too is read in place (128-byte-swizzled MN-major atoms), otherwise it
+//    is first transposed into an N x Kp K-major plane.
 // 2. The persistent tcgen05 kernel of tc_gemm.cuh: one MMA (M = 128, N = BN, K = 16) per k
-//    step, K chunks of 512 accumulated in TMEM and added into FP32 registers with
+//    step, K chunks of 2048 accumulated in TMEM and added into FP32 registers with
 //    round-to-nearest by the epilogue warps.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -71,7 +73,7 @@ __global__ void __launch_bounds__(256) pad_rows_bf16_kernel(const uint16_t* __re
 }
 
 #ifndef BF16_CHUNK_K
-#define BF16_CHUNK_K 512
+#define BF16_CHUNK_K 2048
 #endif
 
 // Tile widths BN (M is 128), BK = 64 (128-byte rows): wider tiles read A less per FLOP.
@@ -80,7 +82,41 @@ using Bf16N192 = tc::TcConfig<tc::kBf16, 192, 64, 4, BF16_CHUNK_K>;  // 4 stages
 using Bf16N224 = tc::TcConfig<tc::kBf16, 224, 64, 4, BF16_CHUNK_K>;  // 4 stages of 44 KB
 using Bf16N256 = tc::TcConfig<tc::kBf16, 256, 64, 4, BF16_CHUNK_K>;  // 4 stages of 48 KB
 
+// B read in place (MN-major): the width must be whole 64-column atoms.
+using Bf16MnN128 = tc::TcConfig<tc::kBf16, 128, 64, 6, BF16_CHUNK_K, true>;
+using Bf16MnN192 = tc::TcConfig<tc::kBf16, 192, 64, 4, BF16_CHUNK_K, true>;
+#ifndef BF16_MN256_BK
+#define BF16_MN256_BK 64
+#define BF16_MN256_STAGES 4
+#endif
+using Bf16MnN256 = tc::TcConfig<tc::kBf16, 256, BF16_MN256_BK, BF16_MN256_STAGES, BF16_CHUNK_K, true>;
+// Pairs of CTAs on two SMs running 256-row tiles with .cta_group::2 MMAs; each CTA stages its
+// 128 rows of A and half of the B tile (stages of 24 KB and 32 KB).
+#ifndef BF16_PAIR256_STAGES
+#define BF16_PAIR256_STAGES 6
+#endif
+using Bf16PairN128 = tc::TcConfig<tc::kBf16, 128, 64, 8, BF16_CHUNK_K, true, true>;
+using Bf16PairN256 = tc::TcConfig<tc::kBf16, 256, 64, BF16_PAIR256_STAGES, BF16_CHUNK_K, true, true>;
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Index of the width (of `n` candidates) with the fewest balanced persistent rounds, weighted
+// for the narrower tiles' extra operand traffic.
+int pick_width(int64_t M, int64_t N, int sms, const int* widths, const double* weight, int n) {
+  const int64_t tm = (M + 127) / 128;
+  int best = 0;
+  double best_cost = 0.0;
+  for (int i = 0; i < n; ++i) {
+    const int64_t tiles = tm * ((N + widths[i] - 1) / widths[i]);
+    const int64_t rounds = (tiles + sms - 1) / sms;
+    const double cost = static_cast<double>(rounds) * widths[i] * weight[i];
+    if (i == 0 || cost < best_cost) {
+      best = i;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
 
 }  // namespace
 
@@ -101,13 +137,6 @@ cudaError_t launch_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, cons
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  {
-    const int64_t gy = Kp / 32;
-    const dim3 grid(static_cast<unsigned>((N + 31) / 32),
-                    static_cast<unsigned>(gy < 65535 ? gy : 65535));
-    transpose_bf16_kernel<<<grid, dim3(32, 8), 0, stream>>>(B, bt, K, N, Kp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
   const bool a_in_place = K % 8 == 0 && aligned16(A);
   const uint16_t* a = A;
   int64_t lda = K;
@@ -120,23 +149,44 @@ cudaError_t launch_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, cons
     lda = Kp;
   }
   Problem p{M, N, K, nullptr, nullptr, C, stream, status};
+  if (N % 8 == 0 && aligned16(B)) {
+    // Weights: measured time of one persistent round per unit of width, relative to 256
+    // (4096^3: 24.7, 26.8 and 29.9 us per round at widths 128, 192, 256).
+    const int widths[3] = {128, 192, 256};
+    const double weight[3] = {1.65, 1.19, 1.0};
+    int best = pick_width(M, N, sms, widths, weight, 3);
+#ifdef BF16_FORCE_WIDTH
+    best = BF16_FORCE_WIDTH;
+#endif
+#ifndef BF16_NO_PAIR
+    // Pairs need two tile rows; 192 columns are three boxes and cannot be split in two.
+    if (M > 128) {
+      switch (best) {
+        case 1: return tc::run_tc<Bf16MnN192>(p, a, nullptr, B, nullptr, lda, N, Kp);
+        case 2: return tc::run_tc<Bf16PairN256>(p, a, nullptr, B, nullptr, lda, N, Kp);
+        default: return tc::run_tc<Bf16PairN128>(p, a, nullptr, B, nullptr, lda, N, Kp);
+      }
+    }
+#endif
+    switch (best) {
+      case 1: return tc::run_tc<Bf16MnN192>(p, a, nullptr, B, nullptr, lda, N, Kp);
+      case 2: return tc::run_tc<Bf16MnN256>(p, a, nullptr, B, nullptr, lda, N, Kp);
+      default: return tc::run_tc<Bf16MnN128>(p, a, nullptr, B, nullptr, lda, N, Kp);
+    }
+  }
+  {
+    const int64_t gy = Kp / 32;
+    const dim3 grid(static_cast<unsigned>((N + 31) / 32),
+                    static_cast<unsigned>(gy < 65535 ? gy : 65535));
+    transpose_bf16_kernel<<<grid, dim3(32, 8), 0, stream>>>(B, bt, K, N, Kp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   // Width by balanced persistent rounds, as for the 3xTF32 kernel.
   const int widths[4] = {128, 192, 224, 256};
   const double weight[4] = {1.15, 1.03, 1.01, 1.0};
-  const int64_t tm = (M + 127) / 128;
-  int best = 0;
-  double best_cost = 0.0;
-  for (int i = 0; i < 4; ++i) {
-    const int64_t tiles = tm * ((N + widths[i] - 1) / widths[i]);
-    const int64_t rounds = (tiles + sms - 1) / sms;
-    const double cost = static_cast<double>(rounds) * widths[i] * weight[i];
-    if (i == 0 || cost < best_cost) {
-      best = i;
-      best_cost = cost;
-    }
-  }
-#ifdef BF16_FORCE_WIDTH
-  best = BF16_FORCE_WIDTH;
+  int best = pick_width(M, N, sms, widths, weight, 4);
+#ifdef BF16_FORCE_WIDTH_T
+  best = BF16_FORCE_WIDTH_T;
 #endif
   switch (best) {
     case 1: return tc::run_tc<Bf16N192>(p, a, nullptr, bt, nullptr, lda, Kp, Kp);

@@ -20,16 +20,35 @@ namespace t2s {
 namespace tc {
 
 // ------------------------------------------------------------------ tcgen05 helpers
+// G = 1: the CTA's own tensor core; G = 2: a pair of CTAs (a cluster of two on two SMs) that
+// allocate TMEM together and run MMAs of twice the rows, issued by the CTA of rank 0. Every
+// tcgen05 instruction of a kernel uses the same G.
+template <int G>
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (G == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     slot_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     slot_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
 }
 
+template <int G>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if constexpr (G == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  } else {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  }
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -39,33 +58,87 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, both K-major; `accumulate` = 0 overwrites D.
+// D[tmem] (+)= A[smem] * B[smem]^T; `accumulate` = 0 overwrites D.
 // KIND 0: kind::tf32; KIND 1: kind::f16 (the formats in the instruction descriptor say BF16).
-template <int KIND>
+template <int KIND, int G>
 __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {
-  if constexpr (KIND == 0) {
+  if constexpr (KIND == 0 && G == 1) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
-  } else {
+  } else if constexpr (KIND == 1 && G == 1) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
+  } else if constexpr (KIND == 0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
   }
 }
 
 // Arrives once on the mbarrier when all tcgen05.mma issued so far by this thread are done.
+template <int G>
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
+  if constexpr (G == 1) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+  } else {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+  }
+}
+
+// The same, arriving on the mbarrier at offset `bar` of both CTAs of the pair.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(0x3))
+      : "memory");
+}
+
+// Shared::cluster address of the same shared-memory offset in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrives once on an mbarrier given by its shared::cluster address (possibly another CTA's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
+}
+
+// TMA 2-D tile load into this CTA's shared memory whose completion is counted on an mbarrier
+// of either CTA of the pair (given by its shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                                 int32_t y, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
 }
 
 // 16 consecutive 32-bit TMEM columns of the warp's 32 lanes: thread t gets lane base + t.
@@ -101,9 +174,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // plane per operand, one MMA per k step); both accumulate in FP32.
 enum TcKind : int { kTf32x3 = 0, kBf16 = 1 };
 
-template <int KIND_, int BN_, int BK_, int STAGES_, int CHUNK_K_>
+// B_MN: B is read in its own row-major K x N layout (MN-major for the tensor core, BF16 only)
+// instead of as an N x K transposed plane.
+// PAIR: CTAs run in clusters of two on two SMs that compute one 256-row tile together with
+// tcgen05 .cta_group::2 MMAs (issued by rank 0): each CTA stages its 128 rows of A and half of
+// B's columns, and accumulates its 128 rows in its own TMEM. Each SM thus receives half of
+// the B tile instead of all of it.
+template <int KIND_, int BN_, int BK_, int STAGES_, int CHUNK_K_, bool B_MN_ = false,
+          bool PAIR_ = false>
 struct TcConfig {
   static constexpr int KIND = KIND_;
+  static constexpr bool B_MN = B_MN_;
+  static constexpr bool PAIR = PAIR_;
   static constexpr int BM = 128, BN = BN_, BK = BK_, STAGES = STAGES_;
   static constexpr int ELEM = KIND == kTf32x3 ? 4 : 2;    // bytes per operand element
   static constexpr int MMA_K = KIND == kTf32x3 ? 8 : 16;  // K of one instruction (32 bytes)
@@ -115,8 +197,17 @@ struct TcConfig {
   static constexpr int CHUNK_KB = CHUNK_K_ / BK;
   static_assert(CHUNK_K_ % BK == 0 && CHUNK_KB >= 1, "chunk of whole K blocks");
   static constexpr int ROW_BYTES = BK * ELEM;
+  static_assert(!B_MN || (KIND == kBf16 && BN % 64 == 0),
+                "MN-major B: BF16 in whole 64-column (128-byte) swizzle atoms");
+  // MN-major B arrives as BN / 64 TMA boxes of BK K-rows x 64 columns (128 bytes), one after
+  // another; a box is a column of 128-byte swizzle atoms (8 K-rows x 64 columns each).
+  static constexpr int B_BOX_BYTES = BK * 128;
+  static constexpr int B_BOXES = B_MN ? BN / 64 : 1;
+  static_assert(!PAIR || (B_MN && B_BOXES % 2 == 0), "pairs split an even number of B boxes");
+  static constexpr int G = PAIR ? 2 : 1;                  // CTAs per MMA
+  static constexpr int B_BOXES_CTA = B_BOXES / G;          // B boxes this CTA stages
   static constexpr int A_BYTES = BM * ROW_BYTES;
-  static constexpr int B_BYTES = BN * ROW_BYTES;
+  static constexpr int B_BYTES = BN / G * ROW_BYTES;  // this CTA's share of the B tile
   static constexpr int STAGE_BYTES = PLANES * (A_BYTES + B_BYTES);
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atom alignment");
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
@@ -139,9 +230,12 @@ struct TcConfig {
   // Instruction descriptor: D = F32 (bits 4..5 = 1), A and B = TF32 (2) or BF16 (1) at bits
   // 7..9 and 10..12, both K-major (bits 15, 16 = 0), N >> 3 at bits 17..22, M >> 4 at 24..28.
   static constexpr uint32_t FMT = KIND == kTf32x3 ? 2u : 1u;
+  // Bit 16 = 1: B is MN-major.
+  // M of one MMA: 128 rows per CTA.
   static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) |
+                                    (static_cast<uint32_t>(B_MN ? 1u : 0u) << 16) |
                                     (static_cast<uint32_t>(BN >> 3) << 17) |
-                                    (static_cast<uint32_t>(BM >> 4) << 24);
+                                    (static_cast<uint32_t>(G * BM >> 4) << 24);
 };
 
 // Shared-memory matrix descriptor of a K-major swizzled operand starting at `addr`:
@@ -155,6 +249,19 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
          (Cfg::LAYOUT << 61);
 }
 
+// Descriptor of an MN-major operand in 128-byte-swizzled atoms (64 BF16 columns x 8 K-rows):
+// leading-dimension offset = byte stride between atoms along N (one TMA box, BK x 128 bytes),
+// stride-dimension offset = byte stride between 8-row K groups (1024). These roles were
+// established on the device with a single-CTA product of known integers (the swapped
+// assignment gives wrong sums).
+template <class Cfg>
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3ffffu) >> 4) |
+         (static_cast<uint64_t>(Cfg::B_BOX_BYTES >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
 // Tile `t` of the grouped raster order (8 tile-rows sweep the columns together).
 __device__ __forceinline__ void tile_origin(int t, int tiles_m, int tiles_n, int bm, int bn,
                                             int& m0, int& n0) {
@@ -166,7 +273,8 @@ __device__ __forceinline__ void tile_origin(int t, int tiles_m, int tiles_n, int
   n0 = ((t % per_group) / gsz) * bn;
 }
 
-// Persistent: CTA b takes tiles b, b + gridDim.x, ... Roles:
+// Persistent: CTA b takes tiles b, b + gridDim.x, ... (PAIR: cluster c takes tile pairs c,
+// c + clusters, ...). Roles:
 //   warp 0  TMA producer (lane 0 issues) over the ring of STAGES slots, across tiles;
 //   warp 1  TMEM allocation; lane 0 issues the MMAs. Each K chunk of a tile is accumulated
 //           from zero into TMEM accumulator c % 2 (c counts chunks across tiles);
@@ -197,7 +305,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
   auto stage = [&](int s) { return base + static_cast<uint32_t>(s) * Cfg::STAGE_BYTES; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles = tiles_m * tiles_n;
+  // Work units: single tiles, or (PAIR) 256-row tiles, rows 128 * rank .. of which belong to
+  // the CTA of that rank in its cluster of two.
+  const int rank = Cfg::PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit0 = Cfg::PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int unit_step = Cfg::PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+  const int units_m = Cfg::PAIR ? (tiles_m + 1) / 2 : tiles_m;
+  const int units = units_m * tiles_n;
+  auto origin = [&](int u, int& m0, int& n0) {
+    tile_origin(u, units_m, tiles_n, Cfg::BM, Cfg::BN, m0, n0);
+    if (Cfg::PAIR) m0 = m0 * 2 + rank * Cfg::BM;
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
@@ -205,7 +323,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accFull + 8u * b, 1);
-      mbar_init(accEmpty + 8u * b, Cfg::EPI_WARPS);  // lane 0 of each epilogue warp
+      // Lane 0 of each epilogue warp (PAIR: of both CTAs; only rank 0's barrier is used).
+      mbar_init(accEmpty + 8u * b, Cfg::G * Cfg::EPI_WARPS);
     }
     mbar_init(mmaDone, 1);
     asm volatile("st.shared.u32 [%0], 0;" ::"r"(sAbort) : "memory");
@@ -219,9 +338,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
       tma_prefetch_desc(&tmBs);
     }
   }
-  if (warp == 1) tmem_alloc(sSlot, Cfg::TMEM_COLS);
+  if (warp == 1) tmem_alloc<Cfg::G>(sSlot, Cfg::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
+  // The peer CTA's copies, commits and arrivals target this CTA's barriers: initialise them
+  // first.
+  if constexpr (Cfg::PAIR) cluster_sync_all();
   tc_fence_after();
   uint32_t tmem;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(sSlot) : "memory");
@@ -238,9 +360,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
     if (lane == 0) {
       int64_t g = 0;  // running K-block index over all tiles of this CTA
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+      for (int u = unit0; ok && u < units; u += unit_step) {
         int m0, n0;
-        tile_origin(t, tiles_m, tiles_n, Cfg::BM, Cfg::BN, m0, n0);
+        origin(u, m0, n0);
         for (int kb = 0; kb < nkb; ++kb, ++g) {
           const int s = static_cast<int>(g % S);
           const uint32_t par = (static_cast<uint32_t>(g / S) & 1u) ^ 1u;
@@ -251,30 +373,49 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
           }
           const uint32_t st = stage(s);
           const int k0 = kb * Cfg::BK;
-          mbar_arrive_expect_tx(full(s), Cfg::STAGE_BYTES);
           // Stage layout: A planes, then B planes.
+          if constexpr (Cfg::PAIR) {
+            // Both CTAs' copies complete on rank 0's barrier, where the MMAs wait.
+            const uint32_t bar0 = map_to_rank(full(s), 0);
+            if (rank == 0) mbar_arrive_expect_tx(full(s), 2 * Cfg::STAGE_BYTES);
+            tma_load_2d_pair(st, &tmAb, k0, m0, bar0);
+#pragma unroll
+            for (int j = 0; j < Cfg::B_BOXES_CTA; ++j)
+              tma_load_2d_pair(st + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &tmBb,
+                               n0 + (Cfg::BN / 2) * rank + 64 * j, k0, bar0);
+            continue;
+          }
+          mbar_arrive_expect_tx(full(s), Cfg::STAGE_BYTES);
           tma_load_2d(st, &tmAb, k0, m0, full(s));
-          tma_load_2d(st + Cfg::PLANES * Cfg::A_BYTES, &tmBb, k0, n0, full(s));
+          if constexpr (Cfg::B_MN) {
+#pragma unroll
+            for (int j = 0; j < Cfg::B_BOXES; ++j)
+              tma_load_2d(st + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &tmBb, n0 + 64 * j, k0, full(s));
+          } else {
+            tma_load_2d(st + Cfg::PLANES * Cfg::A_BYTES, &tmBb, k0, n0, full(s));
+          }
           if (Cfg::PLANES == 2) {
             tma_load_2d(st + Cfg::A_BYTES, &tmAs, k0, m0, full(s));
             tma_load_2d(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES, &tmBs, k0, n0, full(s));
           }
         }
       }
-      // Do not leave while copies into this CTA's shared memory are in flight.
-      for (int64_t j = g > S ? g - S : 0; j < g; ++j)
-        if (!mbar_wait_bounded(full(static_cast<int>(j % S)), static_cast<uint32_t>(j / S) & 1u,
-                               status))
-          break;
+      // Do not leave while copies into this CTA's shared memory are in flight (PAIR: while
+      // they may still be unread by the MMAs; rank 0's commits free both CTAs' slots).
+      for (int64_t j = g > S ? g - S : 0; j < g; ++j) {
+        const int s = static_cast<int>(j % S);
+        const uint32_t par = static_cast<uint32_t>(j / S) & 1u;
+        if (!mbar_wait_bounded(Cfg::PAIR ? empty(s) : full(s), par, status)) break;
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer (lane 0 issues)
-    if (lane == 0) {
+    // ------------------------------------------------ MMA issuer (lane 0 of rank 0 issues)
+    if (lane == 0 && rank == 0) {
       int64_t g = 0;   // K blocks consumed (ring position)
       int64_t cc = 0;  // chunks issued (accumulator double buffer)
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+      for (int u = unit0; ok && u < units; u += unit_step) {
         for (int kb0 = 0; ok && kb0 < nkb; kb0 += Cfg::CHUNK_KB, ++cc) {
           const int b = static_cast<int>(cc & 1);
           const uint32_t acc = tmem + static_cast<uint32_t>(b) * Cfg::ACC_COLS;
@@ -301,26 +442,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
             for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k) {
               const uint32_t off = k * Cfg::MMA_K * Cfg::ELEM;  // 32 bytes per k step
               const uint64_t a_big = smem_desc<Cfg>(st + off);
-              const uint64_t b_big = smem_desc<Cfg>(st + Cfg::PLANES * Cfg::A_BYTES + off);
+              // MN-major B: a k step is MMA_K whole 128-byte K-rows further on.
+              const uint64_t b_big =
+                  Cfg::B_MN ? smem_desc_mn<Cfg>(st + Cfg::A_BYTES + k * Cfg::MMA_K * 128)
+                            : smem_desc<Cfg>(st + Cfg::PLANES * Cfg::A_BYTES + off);
               // The chunk's first MMA overwrites the accumulator (starts the partial sum at 0).
               const uint32_t acc_in = (kb != kb0 || k != 0) ? 1u : 0u;
               if constexpr (Cfg::KIND == kTf32x3) {
                 const uint64_t a_small = smem_desc<Cfg>(st + Cfg::A_BYTES + off);
                 const uint64_t b_small = smem_desc<Cfg>(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES + off);
-                mma_issue<Cfg::KIND>(acc, a_small, b_big, Cfg::IDESC, acc_in);
-                mma_issue<Cfg::KIND>(acc, a_big, b_small, Cfg::IDESC, 1u);
-                mma_issue<Cfg::KIND>(acc, a_big, b_big, Cfg::IDESC, 1u);
+                mma_issue<Cfg::KIND, Cfg::G>(acc, a_small, b_big, Cfg::IDESC, acc_in);
+                mma_issue<Cfg::KIND, Cfg::G>(acc, a_big, b_small, Cfg::IDESC, 1u);
+                mma_issue<Cfg::KIND, Cfg::G>(acc, a_big, b_big, Cfg::IDESC, 1u);
               } else {
-                mma_issue<Cfg::KIND>(acc, a_big, b_big, Cfg::IDESC, acc_in);
+                mma_issue<Cfg::KIND, Cfg::G>(acc, a_big, b_big, Cfg::IDESC, acc_in);
               }
             }
-            mma_commit(empty(s));  // frees the ring slot when these MMAs are done
+            // Frees the ring slot when these MMAs are done (PAIR: in both CTAs).
+            if constexpr (Cfg::PAIR) {
+              mma_commit_pair(empty(s));
+            } else {
+              mma_commit<1>(empty(s));
+            }
           }
-          if (ok) mma_commit(accFull + 8u * b);  // the chunk's partial sums are complete
+          // The chunk's partial sums are complete (PAIR: in both CTAs' TMEM).
+          if (ok) {
+            if constexpr (Cfg::PAIR) {
+              mma_commit_pair(accFull + 8u * b);
+            } else {
+              mma_commit<1>(accFull + 8u * b);
+            }
+          }
         }
       }
       // Every MMA issued above must finish before TMEM can be released.
-      mma_commit(mmaDone);
+      mma_commit<Cfg::G>(mmaDone);
       mbar_wait_bounded(mmaDone, 0u, status);
     }
     __syncwarp();
@@ -331,9 +487,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
     const int col_base = (e >> 2) * Cfg::EPI_COLS;  // this warp's columns of the tile
     int64_t cc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+    for (int u = unit0; ok && u < units; u += unit_step) {
       int m0, n0;
-      tile_origin(t, tiles_m, tiles_n, Cfg::BM, Cfg::BN, m0, n0);
+      origin(u, m0, n0);
       float sum[Cfg::EPI_COLS];
 #pragma unroll
       for (int c = 0; c < Cfg::EPI_COLS; ++c) sum[c] = 0.0f;
@@ -360,7 +516,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
         // All of this warp's TMEM reads of accumulator b are complete (tcgen05.ld waited).
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(accEmpty + 8u * b);
+        if (lane == 0) {
+          if constexpr (Cfg::PAIR) {
+            mbar_arrive_cluster(map_to_rank(accEmpty + 8u * b, 0));  // rank 0 issues the MMAs
+          } else {
+            mbar_arrive(accEmpty + 8u * b);
+          }
+        }
       }
       if (!ok) break;
       const int row = m0 + 32 * q + lane;
@@ -384,15 +546,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
 
   tc_fence_before();
   __syncthreads();
+  // Neither CTA of a pair may exit, or release TMEM, while the other can still use its shared
+  // memory, its barriers or its TMEM.
+  if constexpr (Cfg::PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    tmem_dealloc<Cfg::G>(tmem, Cfg::TMEM_COLS);
   }
 }
 
 // Runs the product over operand planes (K-major, `lda` / `ldb` elements per row, K padded or
 // not): a0/b0 the (big) planes, a1/b1 the small planes for 3xTF32 (ignored for BF16). Every
-// row stride must be a multiple of 16 bytes; K beyond the plane width reads as zeros.
+// row stride must be a multiple of 16 bytes; K beyond the plane width reads as zeros. With
+// Cfg::B_MN, b0 is B itself, K rows of `ldb` (= N) elements. `Kp` is K rounded up to BK.
 template <class Cfg>
 cudaError_t run_tc(const Problem& p, const void* a0, const void* a1, const void* b0,
                    const void* b1, int64_t lda, int64_t ldb, int64_t Kp) {
@@ -407,7 +573,13 @@ cudaError_t run_tc(const Problem& p, const void* a0, const void* a1, const void*
   };
   cudaError_t e;
   if ((e = enc(&tAb, a0, lda, p.M, Cfg::BM)) != cudaSuccess) return e;
-  if ((e = enc(&tBb, b0, ldb, p.N, Cfg::BN)) != cudaSuccess) return e;
+  if constexpr (Cfg::B_MN) {
+    if ((e = encode_tmap_bf16_2d(&tBb, b0, ldb, p.K, 64, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        cudaSuccess)
+      return e;
+  } else {
+    if ((e = enc(&tBb, b0, ldb, p.N, Cfg::BN)) != cudaSuccess) return e;
+  }
   if (Cfg::PLANES == 2) {
     if ((e = enc(&tAs, a1, lda, p.M, Cfg::BM)) != cudaSuccess) return e;
     if ((e = enc(&tBs, b1, ldb, p.N, Cfg::BN)) != cudaSuccess) return e;
@@ -423,13 +595,39 @@ cudaError_t run_tc(const Problem& p, const void* a0, const void* a1, const void*
   const int64_t tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
   const int64_t tiles = tiles_m * tiles_n;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
   const int vec_store = (p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) ? 1 : 0;
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(
-      tAb, tAs, tBb, tBs, p.C, static_cast<int>(p.M), static_cast<int>(p.N),
-      static_cast<int>(Kp / Cfg::BK), static_cast<int>(tiles_m), static_cast<int>(tiles_n),
-      p.status, vec_store);
-  return cudaGetLastError();
+  const int M32 = static_cast<int>(p.M), N32 = static_cast<int>(p.N);
+  const int nkb = static_cast<int>(Kp / Cfg::BK), tm = static_cast<int>(tiles_m),
+            tn = static_cast<int>(tiles_n);
+  if constexpr (Cfg::PAIR) {
+    // One cluster of two CTAs per 256-row tile, at most as many clusters as can be resident
+    // at once (persistent).
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = p.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int64_t units = ((tiles_m + 1) / 2) * tiles_n;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (units < sms / 2 ? units : sms / 2)));
+    int resident = 0;
+    if ((e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg)) != cudaSuccess) return e;
+    if (resident < 1) return cudaErrorInvalidConfiguration;
+    const int64_t clusters = units < resident ? units : resident;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    return cudaLaunchKernelEx(&cfg, kern, tAb, tAs, tBb, tBs, p.C, M32, N32, nkb, tm, tn,
+                              p.status, vec_store);
+  } else {
+    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(tAb, tAs, tBb, tBs, p.C, M32, N32,
+                                                            nkb, tm, tn, p.status, vec_store);
+    return cudaGetLastError();
+  }
 }
 
 

@@ -191,3 +191,33 @@ def test_bf16_contract_checks():
     assert torch.all(dC == 0) and not torch.any(torch.signbit(dC))
     assert f(M, N, K, a, b, c, w, need, s) == binding.T2S_OK
     assert binding.t2s_device_status(s) == binding.T2S_OK
+
+
+@pytest.mark.parametrize("shape", [(128, 64, 64), (300, 200, 130), (129, 8, 1000), (77, 72, 37),
+                                   (513, 392, 520), (256, 264, 4096), (1000, 1000, 1000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bf16_b_read_in_place(shape):
+    """N % 8 == 0 and B 16-byte aligned: B is read in place as MN-major atoms (no transpose);
+    ragged N leaves a partly empty last 64-column box."""
+    M, N, K = shape
+    Ab, Bb = inputs.uniform_bf16(M, K, 61 + M), inputs.uniform_bf16(K, N, 67 + N)
+    C = run_bf16(Ab, Bb)
+    assert float(np.max(np.abs(C - oracle.gemm_bf16(Ab, Bb)))) <= tolerance(Ab, Bb)
+    A, B = inputs.integer_pattern(M, N, K)
+    Ab, Bb = inputs.to_bf16_bits(A), inputs.to_bf16_bits(B)
+    assert bits_equal(run_bf16(Ab, Bb), oracle.gemm_bf16(Ab, Bb))
+
+
+@pytest.mark.parametrize("shape", [(389, 512, 256), (129, 256, 136), (300, 64, 200),
+                                   (1280, 1024, 2048), (3 * 128, 320, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bf16_paired_tiles(shape):
+    """M > 128 with B read in place runs clusters of two CTAs on vertically adjacent tiles that
+    share B: an odd number of tile rows leaves the last pair's second tile beyond M."""
+    M, N, K = shape
+    Ab, Bb = inputs.uniform_bf16(M, K, 71 + M), inputs.uniform_bf16(K, N, 73 + N)
+    C = run_bf16(Ab, Bb)
+    assert float(np.max(np.abs(C - oracle.gemm_bf16(Ab, Bb)))) <= tolerance(Ab, Bb)
+    A, B = inputs.integer_pattern(M, N, K)
+    Ab, Bb = inputs.to_bf16_bits(A), inputs.to_bf16_bits(B)
+    assert bits_equal(run_bf16(Ab, Bb), oracle.gemm_bf16(Ab, Bb))
