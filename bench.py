@@ -40,10 +40,12 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FFMA_PROFILE = os.path.join(ROOT, "profiles", "sgemm_ffma_4096.md")
 TF32X3_PROFILE = os.path.join(ROOT, "profiles", "gemm_tf32x3_4096.md")
 BF16_PROFILE = os.path.join(ROOT, "profiles", "gemm_bf16_4096.md")
+F64_PROFILE = os.path.join(ROOT, "profiles", "dgemm_f64_2048.md")
 KERNEL_SOURCES = {
     "ffma": ["sgemm_ffma.cu", "t2s_device.cuh"],
     "tf32x3": ["gemm_tf32x3.cu", "tc_gemm.cuh", "t2s_device.cuh"],
     "bf16": ["gemm_bf16.cu", "tc_gemm.cuh", "t2s_device.cuh"],
+    "f64": ["gemm_f64.cu"],
 }
 
 
@@ -422,7 +424,7 @@ def extra_bf16(lib, M, N, K, stream, flush, args, dev):
     return {"value": flops / t / 1e12, "unit": UNIT, "ms_per_step": t * 1e3,
             "workload": "%dx%dx%d, bfloat16 A and B (uniform values cut to bfloat16), FP32 C"
                         % (M, N, K),
-            "kernel": "t2s_gemm_bf16_f32 (B transpose pre-pass + tcgen05 kind::f16, FP32 acc.)",
+            "kernel": "t2s_gemm_bf16_f32 (B read in place, tcgen05 kind::f16 on SM pairs, FP32 acc.)",
             "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peak,
                          "frac": flops / t / 1e12 / peak, "unit": UNIT,
                          "peak_basis": "measured cuBLAS bf16 burst",
@@ -454,6 +456,7 @@ def extra_f64(lib, stream, flush, args, dev):
         t = sum(times) / len(times) / 1e3
         tf = rl.gemm_flops(n, n, n) / t / 1e12
         out[name] = {"ms": t * 1e3, "tflops": tf, "frac": tf / rl.fp64_peak_tflops()}
+    out["ffma"]["traffic"] = profile_traffic(F64_PROFILE, "f64")
     return out
 
 
