@@ -69,6 +69,8 @@ class Oracle:
         lib.t2s_oracle_vector_add.restype = ip
         lib.t2s_oracle_bf16_to_f32.argtypes = [i64, fp, fp]
         lib.t2s_oracle_bf16_to_f32.restype = ip
+        lib.t2s_oracle_f16_to_f32.argtypes = [i64, fp, fp]
+        lib.t2s_oracle_f16_to_f32.restype = ip
         lib.t2s_oracle_dgemm.argtypes = [i64, i64, i64, fp, fp, fp, ip]
         lib.t2s_oracle_dgemm.restype = ip
         lib.t2s_oracle_dgemm_at.argtypes = [i64, i64, i64, fp, fp, i64, fp, fp, fp, ip]
@@ -135,6 +137,25 @@ class Oracle:
         if self.lib.t2s_oracle_bf16_to_f32(bits.size, bits.ctypes.data, out.ctypes.data) != 0:
             raise ValueError("oracle rejected the arguments")
         return out
+
+    def f16_to_f32(self, bits: np.ndarray) -> np.ndarray:
+        """Widen IEEE binary16 bit patterns (uint16) to the float32 values they encode."""
+        bits = np.ascontiguousarray(bits)
+        if bits.dtype != np.uint16:
+            raise TypeError("binary16 inputs must be uint16 bit patterns, got %s" % bits.dtype)
+        out = np.empty(bits.shape, dtype=np.float32)
+        if self.lib.t2s_oracle_f16_to_f32(bits.size, bits.ctypes.data, out.ctypes.data) != 0:
+            raise ValueError("oracle rejected the arguments")
+        return out
+
+    def gemm_f16(self, A_bits: np.ndarray, B_bits: np.ndarray) -> np.ndarray:
+        """C (float32) = A x B for binary16 A, B: the FP32 definition on the widened values."""
+        return self.sgemm(self.f16_to_f32(A_bits), self.f16_to_f32(B_bits), MUL_ADD)
+
+    def gemm_f16_at(self, A_bits, B_bits, rows, cols) -> np.ndarray:
+        """Elements C[rows[s], cols[s]] of the binary16 product, one by one."""
+        return self.sgemm_at(self.f16_to_f32(A_bits), self.f16_to_f32(B_bits), rows, cols,
+                             MUL_ADD)
 
     def gemm_bf16(self, A_bits: np.ndarray, B_bits: np.ndarray) -> np.ndarray:
         """C (float32) = A x B for bfloat16 A, B: the FP32 definition on the widened values."""
@@ -228,6 +249,18 @@ def gemm_bf16(A_bits, B_bits) -> np.ndarray:
 
 def gemm_bf16_at(A_bits, B_bits, rows, cols) -> np.ndarray:
     return default().gemm_bf16_at(A_bits, B_bits, rows, cols)
+
+
+def f16_to_f32(bits) -> np.ndarray:
+    return default().f16_to_f32(bits)
+
+
+def gemm_f16(A_bits, B_bits) -> np.ndarray:
+    return default().gemm_f16(A_bits, B_bits)
+
+
+def gemm_f16_at(A_bits, B_bits, rows, cols) -> np.ndarray:
+    return default().gemm_f16_at(A_bits, B_bits, rows, cols)
 
 
 def dgemm(A, B, mode: int = MUL_ADD) -> np.ndarray:

@@ -191,6 +191,36 @@ int t2s_oracle_bf16_to_f32(int64_t n, const uint16_t *x, float *y)
     return 0;
 }
 
+/*
+ * IEEE 754 binary16 operands: 1 sign bit, 5 exponent bits (bias 15) and 10 fraction bits.
+ * Exponent field e = 0 encodes zero and the subnormal numbers f * 2^-24; 1 <= e <= 30 the
+ * normal numbers (1 + f / 1024) * 2^(e - 15); e = 31 infinity (f = 0) or NaN (f != 0).
+ * Every binary16 value, subnormals included, is exact in binary32, and so is the product of
+ * two of them (at most 22 significant bits, magnitudes between 2^-48 and 2^32), so the FP16
+ * definition with an FP32 accumulator is again the FP32 definition on the widened inputs.
+ * The value is built here from the fields with ldexp (exact); a NaN keeps its sign.
+ * Returns 0, or -1 if n is negative.
+ */
+int t2s_oracle_f16_to_f32(int64_t n, const uint16_t *x, float *y)
+{
+    if (n < 0) return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const unsigned sign = (x[i] >> 15) & 1u;
+        const int e = (x[i] >> 10) & 0x1f;
+        const unsigned f = x[i] & 0x3ffu;
+        double v;
+        if (e == 0) {
+            v = ldexp((double)f, -24);
+        } else if (e == 31) {
+            v = f == 0 ? INFINITY : NAN;
+        } else {
+            v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+        }
+        y[i] = (float)(sign ? -v : v);
+    }
+    return 0;
+}
+
 /* One FP64 output element: the definition at the top with T = double. */
 static double dot_row_col_f64(int64_t N, int64_t K, const double *A, const double *B,
                               int64_t i, int64_t j, int mode)

@@ -117,6 +117,25 @@ def uniform_bf16(rows: int, cols: int, seed: int) -> np.ndarray:
     return (v >> np.uint32(16)).astype(np.uint16)
 
 
+def uniform_f16(rows: int, cols: int, seed: int) -> np.ndarray:
+    """rows x cols IEEE binary16 bit patterns, i.i.d. on the 2**-11 grid of [-1, 1): output s
+    of the stream gives ``((u >> 52) - 2048) / 2048`` (12 random bits; every such value has
+    at most 11 significant bits and is exact in binary16, so the conversion does not round)."""
+    u = splitmix64(seed, int(rows) * int(cols))
+    j = (u >> np.uint64(52)).astype(np.int64) - 2048
+    return (j.astype(np.float64) / 2048.0).astype(np.float16).view(np.uint16).reshape(rows, cols)
+
+
+def to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """uint16 binary16 bit patterns of float32 values that binary16 holds exactly. Raises
+    ValueError for a value binary16 cannot hold."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    h = x.astype(np.float16)
+    if not np.array_equal(h.astype(np.float32), x, equal_nan=True):
+        raise ValueError("a value is not representable in binary16")
+    return h.view(np.uint16)
+
+
 # The workloads: (name, M, N, K, kind, config number).
 CONFIGS = {
     "c1_int_256": (256, 256, 256, "integer", 1),

@@ -40,10 +40,11 @@ def rounding_cases(fname: str = "rounding_cases.txt", dtype=np.float32) -> list:
     return cases
 
 
-def bf16_values() -> list:
-    """[(bits, value)] from bf16_values.txt; value is a Python float (inf / nan included)."""
+def bf16_values(fname: str = "bf16_values.txt") -> list:
+    """[(bits, value)] from a 16-bit encoding fixture (bf16_values.txt, f16_values.txt); value
+    is a Python float (inf / nan included)."""
     out = []
-    with open(os.path.join(GOLDEN, "bf16_values.txt"), encoding="utf-8") as f:
+    with open(os.path.join(GOLDEN, fname), encoding="utf-8") as f:
         for line in f:
             line = line.strip()
             if not line or line.startswith("#"):

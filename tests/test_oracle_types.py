@@ -1,7 +1,7 @@
-"""Pins for the oracle's other element types: bfloat16 operands and FP64.
+"""Pins for the oracle's other element types: bfloat16 and binary16 operands, and FP64.
 
-As for FP32, nothing here re-types the oracle's loop: the bfloat16 widening is checked
-against hand-derived encodings and the ordering of the format, and the FP64 product against
+As for FP32, nothing here re-types the oracle's loop: the 16-bit widenings are checked
+against hand-derived encodings and the ordering of the formats, and the FP64 product against
 exact integer and dyadic arithmetic, hand-derived binary64 rounding cases, a closed form and
 the standard inner-product error bound. Planted mistakes in copies of the source must fail a
 pin.
@@ -101,6 +101,75 @@ BF16_BATTERY = [check_bf16_encodings, check_bf16_order_and_sign, check_bf16_prod
 
 
 # ----------------------------------------------------------------------------------------
+# IEEE binary16 widening and the binary16 product
+# ----------------------------------------------------------------------------------------
+
+def check_f16_encodings(o):
+    """Hand-derived binary16 encodings decode to their values (subnormals included)."""
+    table = bf16_values("f16_values.txt")
+    got = o.f16_to_f32(np.array([b for b, _ in table], dtype=np.uint16))
+    for (b, want), g in zip(table, got):
+        g = float(g)
+        if math.isnan(want):
+            if not math.isnan(g):
+                return False, "0x%04X: %r is not NaN" % (b, g)
+        elif g != want or math.copysign(1.0, g) != math.copysign(1.0, want):
+            return False, "0x%04X: %r != %r" % (b, g, want)
+    return True, ""
+
+
+def check_f16_order_and_sign(o):
+    """Over all patterns: +0 .. +inf increase strictly with the pattern, the subnormals are
+    evenly spaced by 2^-24, the sign bit negates, exponent 31 with a fraction is NaN."""
+    pos = np.arange(0x0000, 0x7C01, dtype=np.uint16)
+    v = o.f16_to_f32(pos).astype(np.float64)
+    if not np.all(np.diff(v) > 0):
+        return False, "positive patterns are not strictly increasing"
+    if not np.array_equal(v[:0x401], np.arange(0x401) * 2.0 ** -24):
+        return False, "subnormals and the first normal are not multiples of 2^-24"
+    neg = o.f16_to_f32(pos | np.uint16(0x8000)).astype(np.float64)
+    if not np.array_equal(neg, -v) or not np.all(np.signbit(neg)):
+        return False, "the sign bit does not negate"
+    if not np.all(np.isnan(o.f16_to_f32(np.arange(0x7C01, 0x8000, dtype=np.uint16)))):
+        return False, "exponent 31 with a fraction must be NaN"
+    return True, ""
+
+
+def check_f16_product_exact(o):
+    """Integer-pattern and 11-bit dyadic operands in binary16: C equals the exact product."""
+    for (M, N, K) in [(19, 23, 45), (64, 8, 130)]:
+        A, B = inputs.integer_pattern(M, N, K)
+        exact = (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float32)
+        C = o.gemm_f16(inputs.to_f16_bits(A), inputs.to_f16_bits(B))
+        if not np.array_equal(C.view(np.uint32), exact.view(np.uint32)):
+            return False, "f16 integer pattern %s" % ((M, N, K),)
+    A = inputs.dyadic(17, 40, seed=15, denom=256, span=1000)  # |j| <= 1000: exact in binary16
+    B = inputs.dyadic(40, 9, seed=16, denom=16, span=64)
+    exact = A.astype(np.float64) @ B.astype(np.float64)
+    C = o.gemm_f16(inputs.to_f16_bits(A), inputs.to_f16_bits(B))
+    if not np.array_equal(C.astype(np.float64), exact):
+        return False, "f16 dyadic"
+    return True, ""
+
+
+def check_f16_random_bound(o):
+    """Random binary16 operands: within gamma_K (binary32) of the exact sum, elementwise."""
+    for t, (M, N, K) in enumerate([(9, 7, 33), (16, 5, 200)]):
+        Ab = inputs.uniform_f16(M, K, 720 + t)
+        Bb = inputs.uniform_f16(K, N, 820 + t)
+        A, B = o.f16_to_f32(Ab).astype(np.float64), o.f16_to_f32(Bb).astype(np.float64)
+        C = o.gemm_f16(Ab, Bb).astype(np.float64)
+        g = K * 2.0 ** -24 / (1 - K * 2.0 ** -24)
+        if np.any(np.abs(C - A @ B) > g * (np.abs(A) @ np.abs(B))):
+            return False, "f16 error bound %s" % ((M, N, K),)
+    return True, ""
+
+
+F16_BATTERY = [check_f16_encodings, check_f16_order_and_sign, check_f16_product_exact,
+               check_f16_random_bound]
+
+
+# ----------------------------------------------------------------------------------------
 # FP64
 # ----------------------------------------------------------------------------------------
 
@@ -184,8 +253,8 @@ F64_BATTERY = [check_f64_integer_exact, check_f64_rounding_cases, check_f64_cons
                check_f64_random_bound, check_f64_sampled_and_empty]
 
 
-@pytest.mark.parametrize("check", BF16_BATTERY + F64_BATTERY,
-                         ids=[c.__name__ for c in BF16_BATTERY + F64_BATTERY])
+@pytest.mark.parametrize("check", BF16_BATTERY + F16_BATTERY + F64_BATTERY,
+                         ids=[c.__name__ for c in BF16_BATTERY + F16_BATTERY + F64_BATTERY])
 def test_oracle_type_pin(check):
     ok, detail = check(oracle.default())
     assert ok, detail
@@ -201,6 +270,10 @@ def test_type_entries_reject_bad_arguments():
         o.dgemm_at(np.zeros((2, 2)), np.zeros((2, 2)), [2], [0])
     with pytest.raises(ValueError):
         inputs.to_bf16_bits(np.array([1.0 + 2.0 ** -10], np.float32))
+    with pytest.raises(TypeError):
+        o.f16_to_f32(np.zeros(3, np.float16))
+    with pytest.raises(ValueError):
+        inputs.to_f16_bits(np.array([1.0 + 2.0 ** -12], np.float32))
 
 
 # ----------------------------------------------------------------------------------------
@@ -214,6 +287,13 @@ MUTANTS = {
     "bf16_low_half_set": ("(uint32_t)x[i] << 16", "((uint32_t)x[i] << 16) | 0x8000u"),
     "bf16_byte_swapped": ("(uint32_t)x[i] << 16",
                           "(uint32_t)(uint16_t)((x[i] >> 8) | (x[i] << 8)) << 16"),
+    # binary16 widening
+    "f16_wrong_bias": ("ldexp(1.0 + (double)f / 1024.0, e - 15)", "ldexp(1.0 + (double)f / 1024.0, e - 16)"),
+    "f16_subnormal_as_normal": ("v = ldexp((double)f, -24);", "v = ldexp(1.0 + (double)f / 1024.0, -14);"),
+    "f16_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "f16_fraction_bits": ("const unsigned f = x[i] & 0x3ffu;", "const unsigned f = x[i] & 0x1ffu;"),
+    "f16_sign_dropped": ("y[i] = (float)(sign ? -v : v);", "y[i] = (float)v;"),
+    "f16_no_infinity": ("v = f == 0 ? INFINITY : NAN;", "v = ldexp(1.0 + (double)f / 1024.0, 16);"),
     # FP64 product
     "f64_transposed_B": ("const double b = B[k * N + j];", "const double b = B[j * K + k];"),
     "f64_reversed_k_in_A": ("const double a = A[i * K + k];",
@@ -248,6 +328,7 @@ def test_planted_type_mistake_is_caught(name, oracle_source, tmp_path):
     src.write_text(oracle_source.replace(old, new), encoding="utf-8")
     lib = oracle.compile_source(str(src), str(tmp_path / ("libmutant_%s.so" % name)))
     mutant = oracle.Oracle(lib)
-    battery = BF16_BATTERY if name.startswith("bf16") else F64_BATTERY
+    battery = (BF16_BATTERY if name.startswith("bf16") else
+               F16_BATTERY if name.startswith("f16") else F64_BATTERY)
     failed = [c.__name__ for c in battery if not c(mutant)[0]]
     assert failed, "planted mistake %r passed every pin" % name
