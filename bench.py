@@ -44,7 +44,7 @@ F64_PROFILE = os.path.join(ROOT, "profiles", "dgemm_f64_2048.md")
 KERNEL_SOURCES = {
     "ffma": ["sgemm_ffma.cu", "t2s_device.cuh"],
     "tf32x3": ["gemm_tf32x3.cu", "tc_gemm.cuh", "t2s_device.cuh"],
-    "bf16": ["gemm_bf16.cu", "tc_gemm.cuh", "t2s_device.cuh"],
+    "bf16": ["gemm_16bit.cu", "tc_gemm.cuh", "t2s_device.cuh"],
     "f64": ["gemm_f64.cu"],
 }
 
@@ -343,7 +343,8 @@ def run_ours(args):
     # ---- reported separately: 3xTF32 tensor-core kernel and the 1024^3 shape
     if not args.skip_extras:
         line["tf32x3"] = extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws)
-        line["bf16"] = extra_bf16(lib, M, N, K, stream, flush, args, dev)
+        line["bf16"] = extra_half(lib, M, N, K, stream, flush, args, dev, "bf16")
+        line["f16"] = extra_half(lib, M, N, K, stream, flush, args, dev, "f16")
         line["f64"] = extra_f64(lib, stream, flush, args, dev)
         line["also_1024"] = extra_1024(lib, dev, stream, flush, args, ws)
         line["memory_roof"] = extra_vector_add(lib, dev, stream, flush, args)
@@ -393,26 +394,28 @@ def extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws):
                          "traffic": profile_traffic(TF32X3_PROFILE, "tf32x3")}}
 
 
-def extra_bf16(lib, M, N, K, stream, flush, args, dev):
-    """The BF16-operand product (FP32 accumulation) on the same shape, against the measured
-    dense bf16 tensor peak; the call's B transpose pre-pass is inside the timed region."""
+def extra_half(lib, M, N, K, stream, flush, args, dev, fmt="bf16"):
+    """A 16-bit-operand product (FP32 accumulation) on the same shape, against the measured
+    dense bf16 tensor peak (FP16 runs at the same nominal rate); `fmt` is "bf16" or "f16"."""
     import torch
     from roofline_driven_tiling_gb300 import binding, inputs
     from roofline_driven_tiling_gb300 import roofline as rl
-    Ab = inputs.uniform_bf16(M, K, inputs.SEED_A_BASE + WORKLOAD["config_no"])
-    Bb = inputs.uniform_bf16(K, N, inputs.SEED_B_BASE + WORKLOAD["config_no"])
+    make = inputs.uniform_bf16 if fmt == "bf16" else inputs.uniform_f16
+    Ab = make(M, K, inputs.SEED_A_BASE + WORKLOAD["config_no"])
+    Bb = make(K, N, inputs.SEED_B_BASE + WORKLOAD["config_no"])
     dA = torch.from_numpy(Ab.view(np.int16)).to(dev)
     dB = torch.from_numpy(Bb.view(np.int16)).to(dev)
     dC = torch.empty((M, N), dtype=torch.float32, device=dev)
-    need = lib.t2s_gemm_bf16_f32_workspace_size(M, N, K)
+    name = "t2s_gemm_%s_f32" % fmt
+    need = getattr(lib, name + "_workspace_size")(M, N, K)
     wsbuf = torch.empty(need, dtype=torch.uint8, device=dev)
     sp = stream.cuda_stream
+    fn = getattr(lib, name)
 
     def step():
-        rc = lib.t2s_gemm_bf16_f32(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
-                                   wsbuf.data_ptr(), need, sp)
+        rc = fn(M, N, K, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), wsbuf.data_ptr(), need, sp)
         if rc != 0:
-            raise binding.T2SError(rc, "t2s_gemm_bf16_f32")
+            raise binding.T2SError(rc, name)
 
     try:
         times = time_steps(step, args.steps, max(args.warmup, 3), stream, flush)
@@ -421,14 +424,15 @@ def extra_bf16(lib, M, N, K, stream, flush, args, dev):
     flops = rl.gemm_flops(M, N, K)
     t = sum(times) / len(times) / 1e3
     peak = float(measured_peaks().get("bf16_tflops", 1898.5))
+    label = "bfloat16" if fmt == "bf16" else "binary16"
+    cut = "uniform values cut to bfloat16" if fmt == "bf16" else "uniform on the 2^-11 grid"
     return {"value": flops / t / 1e12, "unit": UNIT, "ms_per_step": t * 1e3,
-            "workload": "%dx%dx%d, bfloat16 A and B (uniform values cut to bfloat16), FP32 C"
-                        % (M, N, K),
-            "kernel": "t2s_gemm_bf16_f32 (B read in place, tcgen05 kind::f16 on SM pairs, FP32 acc.)",
+            "workload": "%dx%dx%d, %s A and B (%s), FP32 C" % (M, N, K, label, cut),
+            "kernel": "%s (B read in place, tcgen05 kind::f16 on SM pairs, FP32 acc.)" % name,
             "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peak,
                          "frac": flops / t / 1e12 / peak, "unit": UNIT,
-                         "peak_basis": "measured cuBLAS bf16 burst",
-                         "traffic": profile_traffic(BF16_PROFILE, "bf16")}}
+                         "peak_basis": "measured cuBLAS bf16 burst (FP16 has the same nominal rate)",
+                         "traffic": profile_traffic(BF16_PROFILE, "bf16") if fmt == "bf16" else None}}
 
 
 def extra_f64(lib, stream, flush, args, dev):

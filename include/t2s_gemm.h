@@ -2,8 +2,8 @@
  * t2s_gemm.h -- C ABI of the GB300 (sm_103a) FP32 matrix-multiply library.
  *
  * Operation (all entry points): C = A x B in IEEE binary32, row-major, dense
- * (t2s_gemm_bf16_f32 takes bfloat16 A and B and writes a binary32 C; the t2s_gemm_f64
- * entry points work in binary64 throughout).
+ * (t2s_gemm_bf16_f32 and t2s_gemm_f16_f32 take bfloat16 or binary16 A and B and write a
+ * binary32 C; the t2s_gemm_f64 entry points work in binary64 throughout).
  *
  *   A is M x K, element (row, k)   at A[row * K + k]
  *   B is K x N, element (k, col)   at B[k * N + col]
@@ -228,6 +228,17 @@ int t2s_gemm_f32_tf32x3_noalloc(int64_t M, int64_t N, int64_t K, const float *A,
 size_t t2s_gemm_bf16_f32_workspace_size(int64_t M, int64_t N, int64_t K);
 int t2s_gemm_bf16_f32(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B,
                       float *C, void *workspace, size_t workspace_bytes, t2s_stream_t stream);
+
+/*
+ * The same product for IEEE 754 binary16 (FP16) A and B: uint16_t bit patterns with 1 sign,
+ * 5 exponent (bias 15) and 10 fraction bits, subnormals included. Every product of two FP16
+ * values is exact in FP32, so the same bars hold: exact wherever every partial sum is exact,
+ * otherwise max |C - sum_k a*b| <= 1e-6 * K * max|a| * max|b|. Layout, alignment, workspace
+ * (the same size as for BF16), contract and return codes are those of t2s_gemm_bf16_f32.
+ */
+size_t t2s_gemm_f16_f32_workspace_size(int64_t M, int64_t N, int64_t K);
+int t2s_gemm_f16_f32(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B,
+                     float *C, void *workspace, size_t workspace_bytes, t2s_stream_t stream);
 
 /*
  * FP64 element type on the CUDA cores: C = A x B in IEEE binary64, the same layout and

@@ -43,6 +43,8 @@ SIGNATURES = {
     "t2s_gemm_f64_smem32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_bf16_f32_workspace_size": ([_i64, _i64, _i64], _sz),
     "t2s_gemm_bf16_f32": ([_i64, _i64, _i64, _p, _p, _p, _p, _sz, _p], _i),
+    "t2s_gemm_f16_f32_workspace_size": ([_i64, _i64, _i64], _sz),
+    "t2s_gemm_f16_f32": ([_i64, _i64, _i64, _p, _p, _p, _p, _sz, _p], _i),
     "t2s_vector_add_f32": ([_i64, _p, _p, _p, _p], _i),
     "t2s_status_string": ([_i], ctypes.c_char_p),
     "t2s_device_status": ([_p], _i),
@@ -135,6 +137,14 @@ def t2s_gemm_bf16_f32_workspace_size(M, N, K) -> int:
 
 def t2s_gemm_bf16_f32(M, N, K, A, B, C, workspace, workspace_bytes, stream=0) -> int:
     return lib().t2s_gemm_bf16_f32(M, N, K, A, B, C, workspace, workspace_bytes, stream)
+
+
+def t2s_gemm_f16_f32_workspace_size(M, N, K) -> int:
+    return lib().t2s_gemm_f16_f32_workspace_size(M, N, K)
+
+
+def t2s_gemm_f16_f32(M, N, K, A, B, C, workspace, workspace_bytes, stream=0) -> int:
+    return lib().t2s_gemm_f16_f32(M, N, K, A, B, C, workspace, workspace_bytes, stream)
 
 
 def t2s_vector_add_f32(n, x, y, z, stream=0) -> int:
@@ -247,14 +257,13 @@ def gemm_f64(A, B, out=None, kernel: str = "ffma", stream=None):
     return out
 
 
-def gemm_bf16(A, B, out=None, workspace=None, stream=None):
-    """C (float32) = A @ B for bfloat16 CUDA tensors A (M x K) and B (K x N), row-major."""
+def _gemm_16bit(A, B, out, workspace, stream, dtype, name):
     import torch
-    for t, name in ((A, "A"), (B, "B")):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
-            raise TypeError("%s must be a bfloat16 CUDA tensor" % name)
+    for t, what in ((A, "A"), (B, "B")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != dtype:
+            raise TypeError("%s must be a %s CUDA tensor" % (what, dtype))
         if t.dim() != 2 or not t.is_contiguous():
-            raise ValueError("%s must be a contiguous 2-D (row-major) tensor" % name)
+            raise ValueError("%s must be a contiguous 2-D (row-major) tensor" % what)
     if A.shape[1] != B.shape[0]:
         raise ValueError("shape mismatch: A %s, B %s" % (tuple(A.shape), tuple(B.shape)))
     M, K = A.shape
@@ -266,15 +275,28 @@ def gemm_bf16(A, B, out=None, workspace=None, stream=None):
         raise ValueError("out must be %d x %d" % (M, N))
     if stream is None:
         stream = torch.cuda.current_stream(A.device).cuda_stream
-    need = t2s_gemm_bf16_f32_workspace_size(M, N, K)
+    l = lib()
+    need = getattr(l, name + "_workspace_size")(M, N, K)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
-    rc = t2s_gemm_bf16_f32(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(),
-                           workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                           stream)
+    rc = getattr(l, name)(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(),
+                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                          stream)
     if rc != T2S_OK:
-        raise T2SError(rc, "t2s_gemm_bf16_f32")
+        raise T2SError(rc, name)
     return out
+
+
+def gemm_bf16(A, B, out=None, workspace=None, stream=None):
+    """C (float32) = A @ B for bfloat16 CUDA tensors A (M x K) and B (K x N), row-major."""
+    import torch
+    return _gemm_16bit(A, B, out, workspace, stream, torch.bfloat16, "t2s_gemm_bf16_f32")
+
+
+def gemm_f16(A, B, out=None, workspace=None, stream=None):
+    """C (float32) = A @ B for float16 CUDA tensors A (M x K) and B (K x N), row-major."""
+    import torch
+    return _gemm_16bit(A, B, out, workspace, stream, torch.float16, "t2s_gemm_f16_f32")
 
 
 def device_status(stream=None) -> int:

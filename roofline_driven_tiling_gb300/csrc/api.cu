@@ -194,11 +194,26 @@ int t2s_gemm_f32_tf32x3(int64_t M, int64_t N, int64_t K, const float* A, const f
 
 size_t t2s_gemm_bf16_f32_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return 0;
-  return bf16_workspace_bytes(M, N, K);
+  return half_workspace_bytes(M, N, K);
 }
 
-int t2s_gemm_bf16_f32(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
-                      float* C, void* workspace, size_t workspace_bytes, t2s_stream_t stream) {
+size_t t2s_gemm_f16_f32_workspace_size(int64_t M, int64_t N, int64_t K) {
+  return t2s_gemm_bf16_f32_workspace_size(M, N, K);
+}
+
+}  // extern "C"
+
+namespace t2s {
+namespace {
+
+using LauncherF64 = cudaError_t (*)(int64_t, int64_t, int64_t, const double*, const double*,
+                                    double*, cudaStream_t);
+using LauncherHalf = cudaError_t (*)(int64_t, int64_t, int64_t, const uint16_t*, const uint16_t*,
+                                     float*, void*, cudaStream_t, unsigned*);
+
+int gemm_half_common(LauncherHalf launch, int64_t M, int64_t N, int64_t K, const uint16_t* A,
+                     const uint16_t* B, float* C, void* workspace, size_t workspace_bytes,
+                     t2s_stream_t stream) {
   bool noop = false;
   const int rc = validate(M, N, K, A, B, C, 2, &noop);
   if (rc != T2S_OK || noop) return rc;
@@ -211,20 +226,12 @@ int t2s_gemm_bf16_f32(int64_t M, int64_t N, int64_t K, const uint16_t* A, const 
   cudaError_t e = status_word(&p.status);
   if (e != cudaSuccess) return fail_cuda(e);
   if (K == 0) return zero_fill(p);
-  const size_t need = bf16_workspace_bytes(M, N, K);
+  const size_t need = half_workspace_bytes(M, N, K);
   if (workspace == nullptr || workspace_bytes < need) return T2S_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return T2S_ERR_WORKSPACE;
-  e = launch_bf16(M, N, K, A, B, C, workspace, p.stream, p.status);
+  e = launch(M, N, K, A, B, C, workspace, p.stream, p.status);
   return e == cudaSuccess ? T2S_OK : fail_cuda(e);
 }
-
-}  // extern "C"
-
-namespace t2s {
-namespace {
-
-using LauncherF64 = cudaError_t (*)(int64_t, int64_t, int64_t, const double*, const double*,
-                                    double*, cudaStream_t);
 
 int gemm_f64_common(LauncherF64 launch, int64_t M, int64_t N, int64_t K, const double* A,
                     const double* B, double* C, t2s_stream_t stream) {
@@ -245,6 +252,18 @@ int gemm_f64_common(LauncherF64 launch, int64_t M, int64_t N, int64_t K, const d
 }  // namespace t2s
 
 extern "C" {
+
+int t2s_gemm_bf16_f32(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
+                      float* C, void* workspace, size_t workspace_bytes, t2s_stream_t stream) {
+  return t2s::gemm_half_common(t2s::launch_bf16, M, N, K, A, B, C, workspace, workspace_bytes,
+                               stream);
+}
+
+int t2s_gemm_f16_f32(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
+                     float* C, void* workspace, size_t workspace_bytes, t2s_stream_t stream) {
+  return t2s::gemm_half_common(t2s::launch_f16, M, N, K, A, B, C, workspace, workspace_bytes,
+                               stream);
+}
 
 int t2s_gemm_f64(int64_t M, int64_t N, int64_t K, const double* A, const double* B, double* C,
                  t2s_stream_t stream) {

@@ -35,10 +35,13 @@ int splitk_planes(int64_t K, int splits);
 cudaError_t launch_ffma_splitk(const Problem& p, int splits, float* workspace);
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tf32x3(const Problem& p, void* workspace);
-// BF16 operands (uint16_t bit patterns), FP32 C; workspace for the transposed/padded planes.
-size_t bf16_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// BF16 or FP16 operands (uint16_t bit patterns), FP32 C; workspace for the transposed/padded
+// planes (the same size for both formats).
+size_t half_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
                         float* C, void* workspace, cudaStream_t stream, unsigned* status);
+cudaError_t launch_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
+                       float* C, void* workspace, cudaStream_t stream, unsigned* status);
 // FP64 (binary64) kernels: product, naive and 32 x 32 shared-memory comparison points.
 cudaError_t launch_dgemm(int64_t M, int64_t N, int64_t K, const double* A, const double* B,
                          double* C, cudaStream_t stream);

@@ -59,7 +59,7 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T; `accumulate` = 0 overwrites D.
-// KIND 0: kind::tf32; KIND 1: kind::f16 (the formats in the instruction descriptor say BF16).
+// KIND 0: kind::tf32; otherwise kind::f16 (the instruction descriptor says BF16 or FP16).
 template <int KIND, int G>
 __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {
@@ -70,18 +70,18 @@ __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint6
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
-  } else if constexpr (KIND == 1 && G == 1) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
   } else if constexpr (KIND == 0) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else if constexpr (G == 1) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
   } else {
@@ -170,9 +170,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // ------------------------------------------------------------------ product kernel
-// Operand kinds: 3xTF32 (two TF32 planes per operand, three MMAs per k step) and BF16 (one
-// plane per operand, one MMA per k step); both accumulate in FP32.
-enum TcKind : int { kTf32x3 = 0, kBf16 = 1 };
+// Operand kinds: 3xTF32 (two TF32 planes per operand, three MMAs per k step), BF16 and FP16
+// (one plane per operand, one MMA per k step); all accumulate in FP32.
+enum TcKind : int { kTf32x3 = 0, kBf16 = 1, kF16 = 2 };
 
 // B_MN: B is read in its own row-major K x N layout (MN-major for the tensor core, BF16 only)
 // instead of as an N x K transposed plane.
@@ -197,8 +197,8 @@ struct TcConfig {
   static constexpr int CHUNK_KB = CHUNK_K_ / BK;
   static_assert(CHUNK_K_ % BK == 0 && CHUNK_KB >= 1, "chunk of whole K blocks");
   static constexpr int ROW_BYTES = BK * ELEM;
-  static_assert(!B_MN || (KIND == kBf16 && BN % 64 == 0),
-                "MN-major B: BF16 in whole 64-column (128-byte) swizzle atoms");
+  static_assert(!B_MN || (KIND != kTf32x3 && BN % 64 == 0),
+                "MN-major B: 16-bit operands in whole 64-column (128-byte) swizzle atoms");
   // MN-major B arrives as BN / 64 TMA boxes of BK K-rows x 64 columns (128 bytes), one after
   // another; a box is a column of 128-byte swizzle atoms (8 K-rows x 64 columns each).
   static constexpr int B_BOX_BYTES = BK * 128;
@@ -227,9 +227,10 @@ struct TcConfig {
   static constexpr uint64_t LAYOUT = ROW_BYTES == 128 ? 2 : 4;
   // Stride between 8-row core groups: 8 rows of ROW_BYTES.
   static constexpr uint32_t SBO = 8 * ROW_BYTES;
-  // Instruction descriptor: D = F32 (bits 4..5 = 1), A and B = TF32 (2) or BF16 (1) at bits
-  // 7..9 and 10..12, both K-major (bits 15, 16 = 0), N >> 3 at bits 17..22, M >> 4 at 24..28.
-  static constexpr uint32_t FMT = KIND == kTf32x3 ? 2u : 1u;
+  // Instruction descriptor: D = F32 (bits 4..5 = 1), A and B = TF32 (2), BF16 (1) or FP16 (0)
+  // at bits 7..9 and 10..12, both K-major (bits 15, 16 = 0), N >> 3 at bits 17..22, M >> 4 at
+  // 24..28.
+  static constexpr uint32_t FMT = KIND == kTf32x3 ? 2u : KIND == kBf16 ? 1u : 0u;
   // Bit 16 = 1: B is MN-major.
   // M of one MMA: 128 rows per CTA.
   static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) |
@@ -567,6 +568,7 @@ cudaError_t run_tc(const Problem& p, const void* a0, const void* a1, const void*
   memset(&tBs, 0, sizeof(tBs));
   const CUtensorMapSwizzle sw =
       Cfg::ROW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  // TMA moves 16-bit elements as they are, so one 16-bit map type serves BF16 and FP16.
   auto enc = [&](CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uint32_t box_rows) {
     return Cfg::KIND == kTf32x3 ? encode_tmap_f32_2d(m, base, cols, rows, Cfg::BK, box_rows, sw)
                                 : encode_tmap_bf16_2d(m, base, cols, rows, Cfg::BK, box_rows, sw);

@@ -163,3 +163,15 @@ def test_f64_entries_reject_bad_arguments(lib, fn):
     assert f(4, 4, 4, fake, fake + 256, fake, 0) == binding.T2S_ERR_INVALID  # C == A
     assert f(4, 4, 4, 0, fake + 256, fake + 512, 0) == binding.T2S_ERR_INVALID  # NULL A
     assert f(0, 4, 4, 0, fake + 256, 0, 0) == binding.T2S_OK  # M = 0: nothing to do
+
+
+def test_f16_entry_matches_bf16_contract(lib):
+    for M, N, K in [(4096, 4096, 4096), (128, 64, 997), (3, 5, 7), (0, 0, 0)]:
+        assert binding.t2s_gemm_f16_f32_workspace_size(M, N, K) == \
+            binding.t2s_gemm_bf16_f32_workspace_size(M, N, K)
+    fake = 1 << 20
+    f = binding.t2s_gemm_f16_f32
+    assert f(-1, 4, 4, fake, fake + 64, fake + 4096, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
+    assert f(4, 4, 4, fake + 1, fake + 64, fake + 4096, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
+    assert f(4, 4, 4, fake, fake + 64, fake, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
+    assert f(0, 4, 4, 0, fake + 64, 0, 0, 0, 0) == binding.T2S_OK
