@@ -397,12 +397,14 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
 // block when K is long enough to pay for the larger code.
 using Big = FfmaConfig<128, 128, BIG_BK, BIG_STAGES, 2, 2, BIG_AV, 8, 16, FFMA_KG_UNROLL>;
 using BigShortK = FfmaConfig<128, 128, 32, 3, 2, 2, 2, 8, 16, 1>;
-// 64 x 128 tiles for products too small to give every SM two 128 x 128 tiles.
+// 64 x 128 tiles of 2 warps: about one 128 x 128 tile per SM (1536^3: 52.2 TFLOP/s against
+// 48.9 for 64 x 64 and 51.8 for 128 x 128 tiles).
 using Mid = FfmaConfig<64, 128, 32, 3, 1, 2, 2, 8, 16, 1>;
-// 4 x 8 per thread (64 x 64 CTA tiles of 4 warps): more warps for small products. Measured
-// fastest below ~1.5 tiles of 64 x 128 per SM: 32.4 TFLOP/s at 1024^3 against 22.2 for 64 x 64
-// tiles of 8 x 16 per thread and 31.5 for 8 x 8.
-using Small48 = FfmaConfig<64, 64, 16, 4, 2, 2, 2, 4, 8, 1>;
+// 4 x 8 per thread (64 x 64 CTA tiles of 4 warps, BK = 32, 3 stages): many small CTAs (four
+// per SM) that even out the last wave. Measured fastest up to ~2.4 tiles of 128 x 128 per SM:
+// 1024^3 37.0 TFLOP/s (BK = 16 and 4 stages: 32.4; 128 x 64 tiles of 8 x 8: 35.8), 2048^3 52.3
+// (128 x 128: 51.1), 2304^3 52.1 (45.9).
+using Small48 = FfmaConfig<64, 64, 32, 3, 2, 2, 2, 4, 8, 1>;
 
 bool tma_ok(const Problem& p) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.A), b = reinterpret_cast<uintptr_t>(p.B);
@@ -430,15 +432,15 @@ cudaError_t launch_ffma(const Problem& p) {
     case 3: return run_any<Small48>(p);
     default: break;
   }
-  // Thresholds from measurements on GB300 (152 SMs): the fully unrolled 128 x 128 kernel
-  // pays off once every SM sees two full waves of tile pairs; with fewer tiles the compact
-  // loop is faster, and below ~1.5 tiles per SM 64-row tiles spread the work further.
+  // Thresholds from measurements on GB300 (152 SMs), in 128 x 128 tiles per SM (r): 128 x 128
+  // tiles from r = 2.4 (2560^3: 56.3 TFLOP/s against 53.3 for 64 x 64; 3072^3: 60.3 against
+  // 53.5), the fully unrolled k loop once K >= 256; 64 x 128 tiles around one tile per SM;
+  // 64 x 64 tiles otherwise. The last wave decides between neighbours, so the cut points are
+  // where the measured curves cross, not a smooth model.
   const int64_t big_tiles = ((p.M + 127) / 128) * ((p.N + 127) / 128);
-  const int64_t mid_tiles = ((p.M + 63) / 64) * ((p.N + 127) / 128);
   const int64_t s64 = static_cast<int64_t>(sms);
-  if (big_tiles >= 4 * s64 && p.K >= 256) return run_any<Big>(p);
-  if (2 * big_tiles >= 3 * s64) return run_any<BigShortK>(p);
-  if (mid_tiles >= s64) return run_any<Mid>(p);
+  if (5 * big_tiles >= 12 * s64) return p.K >= 256 ? run_any<Big>(p) : run_any<BigShortK>(p);
+  if (5 * big_tiles >= 4 * s64 && 10 * big_tiles < 11 * s64) return run_any<Mid>(p);
   return run_any<Small48>(p);
 }
 
@@ -486,17 +488,17 @@ int64_t splitk_chunk(int64_t K, int splits) {
 }
 
 // The number of chunks the automatic choice uses (measured on GB300): none once the product
-// alone gives 1.5 tiles of 128 x 128 per SM (splitting 2048^2 x 512 made it slower); below that,
-// enough chunks for about four such tiles per SM, chunks of at least 64 values, at most 16.
-// Measured gains: 1024^3 32.4 -> 38.4 TFLOP/s, 512^3 10.6 -> 15.8, 1024^2 x 4096 35.8 -> 51,
-// 256^2 x 8192 3.4 -> 25.8.
+// alone gives 2.4 tiles of 128 x 128 per SM (the unsplit product is then as fast); below that,
+// about three rounds of chunk tiles on the 2 x SMs CTA slots (2048^3: 4 chunks, 58.0 TFLOP/s
+// against 52.3 unsplit; 1536^3: 6, 52.7; 1024^3: 8, 38.4), chunks of at least 128 values
+// (shorter chunks spend their time filling the pipeline), at most 16.
 int splitk_auto(int64_t M, int64_t N, int64_t K) {
   const int sms = sm_count();
   if (sms <= 0) return 1;
   const int64_t big_tiles = ((M + 127) / 128) * ((N + 127) / 128);
-  if (2 * big_tiles >= 3 * static_cast<int64_t>(sms)) return 1;
-  int64_t s = (4 * static_cast<int64_t>(sms) + big_tiles - 1) / big_tiles;
-  const int64_t by_k = K / 64;
+  if (5 * big_tiles >= 12 * static_cast<int64_t>(sms)) return 1;
+  int64_t s = (6 * static_cast<int64_t>(sms) + big_tiles / 2) / big_tiles;  // round(3 x 2 SMs / tiles)
+  const int64_t by_k = K / 128;
   if (s > by_k) s = by_k;
   if (s > 16) s = 16;
   return s < 1 ? 1 : static_cast<int>(s);
