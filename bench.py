@@ -476,12 +476,18 @@ def extra_1024(lib, dev, stream, flush, args, ws):
     out = {"workload": "sgemm 1024^3 fp32, integer pattern (L2 flushed per step)"}
     need = lib.t2s_gemm_f32_splitk_workspace_size(n, n, n, 0)
     wsk = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    wss = torch.empty(max(lib.t2s_gemm_f32_streamk_workspace_size(n, n, n), 256),
+                      dtype=torch.uint8, device=dev)
 
     def splitk(M, N, K, a, b, c, s):
         return lib.t2s_gemm_f32_splitk(M, N, K, a, b, c, 0, wsk.data_ptr(), wsk.numel(), s)
 
+    def streamk(M, N, K, a, b, c, s):
+        return lib.t2s_gemm_f32_streamk(M, N, K, a, b, c, wss.data_ptr(), wss.numel(), s)
+
     for name, fn in (("ffma", lib.t2s_gemm_f32), ("ffma_splitk_auto", splitk),
-                     ("naive", lib.t2s_gemm_f32_naive), ("smem32", lib.t2s_gemm_f32_smem32)):
+                     ("ffma_streamk", streamk), ("naive", lib.t2s_gemm_f32_naive),
+                     ("smem32", lib.t2s_gemm_f32_smem32)):
         times = time_steps(lambda: fn(n, n, n, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sp),
                            max(args.steps, 10), 3, stream, flush)
         t = sum(times) / len(times) / 1e3

@@ -156,6 +156,29 @@ int t2s_gemm_f32_splitk(int64_t M, int64_t N, int64_t K, const float *A, const f
                         t2s_stream_t stream);
 
 /*
+ * Stream-K product for shapes whose tiles do not divide evenly over the GPU (small and mid
+ * sizes; the last partial wave of large ones). The iterations of the product -- 128 x 128
+ * tiles times 32-deep K blocks, tiles in the product kernel's order, K blocks ascending --
+ * are shared out in equal contiguous ranges over a persistent grid of two CTAs per SM, so
+ * every SM gets the same work whatever the tile count. A tile whose K blocks all fall in one
+ * CTA's range is stored into C by that CTA; the CTAs that share a tile store their partial
+ * sums of it in `workspace`, and a second kernel adds those partial tiles in K order. The
+ * result is deterministic and within max |C - C_fp32| <= 1e-6 * K * max|a| * max|b|, but not
+ * bit-identical to t2s_gemm_f32 (a shared tile's partial sums are added at the end).
+ *  - workspace: a DEVICE buffer, 256-byte aligned, of at least
+ *    t2s_gemm_f32_streamk_workspace_size(M, N, K) bytes (two 128 x 128 float tiles per CTA,
+ *    about 40 MB on a 152-SM GB300), owned by the caller and untouched until the stream has
+ *    run the call; T2S_ERR_WORKSPACE if NULL, too small or misaligned.
+ *  - Needs the TMA path (K % 4 == 0, N % 4 == 0, A and B 16-byte aligned); other shapes run
+ *    the product kernel (bit-identical to t2s_gemm_f32) and leave the workspace unused.
+ *  - Otherwise the common contract and return codes above apply.
+ */
+size_t t2s_gemm_f32_streamk_workspace_size(int64_t M, int64_t N, int64_t K);
+int t2s_gemm_f32_streamk(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
+                         float *C, void *workspace, size_t workspace_bytes,
+                         t2s_stream_t stream);
+
+/*
  * Tensor-core variant: error-compensated 3xTF32 on tcgen05 tensor cores with
  * TMEM accumulators. Each operand x is split into big = tf32(x) and
  * small = tf32(x - big); C accumulates small*big + big*small + big*big in FP32.

@@ -35,6 +35,8 @@ SIGNATURES = {
     "t2s_gemm_f32_smem32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_splitk_workspace_size": ([_i64, _i64, _i64, _i], _sz),
     "t2s_gemm_f32_splitk": ([_i64, _i64, _i64, _p, _p, _p, _i, _p, _sz, _p], _i),
+    "t2s_gemm_f32_streamk_workspace_size": ([_i64, _i64, _i64], _sz),
+    "t2s_gemm_f32_streamk": ([_i64, _i64, _i64, _p, _p, _p, _p, _sz, _p], _i),
     "t2s_gemm_f32_tf32x3_workspace_size": ([_i64, _i64, _i64], _sz),
     "t2s_gemm_f32_tf32x3": ([_i64, _i64, _i64, _p, _p, _p, _p, _sz, _p], _i),
     "t2s_gemm_f32_tf32x3_noalloc": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
@@ -104,6 +106,14 @@ def t2s_gemm_f32_splitk_workspace_size(M, N, K, splits=0) -> int:
 
 def t2s_gemm_f32_splitk(M, N, K, A, B, C, splits, workspace, workspace_bytes, stream=0) -> int:
     return lib().t2s_gemm_f32_splitk(M, N, K, A, B, C, splits, workspace, workspace_bytes, stream)
+
+
+def t2s_gemm_f32_streamk_workspace_size(M, N, K) -> int:
+    return lib().t2s_gemm_f32_streamk_workspace_size(M, N, K)
+
+
+def t2s_gemm_f32_streamk(M, N, K, A, B, C, workspace, workspace_bytes, stream=0) -> int:
+    return lib().t2s_gemm_f32_streamk(M, N, K, A, B, C, workspace, workspace_bytes, stream)
 
 
 def t2s_gemm_f32_tf32x3_workspace_size(M, N, K) -> int:
@@ -179,6 +189,7 @@ KERNELS = {
     "naive": "t2s_gemm_f32_naive",
     "smem32": "t2s_gemm_f32_smem32",
     "tf32x3": "t2s_gemm_f32_tf32x3",
+    "streamk": "t2s_gemm_f32_streamk",
 }
 
 
@@ -193,8 +204,8 @@ def _check(t, name):
 def gemm(A, B, out=None, kernel: str = "ffma", workspace=None, stream=None):
     """C = A @ B through the library (torch tensors in, torch tensor out).
 
-    `kernel` is one of "ffma" (the product), "naive", "smem32", "tf32x3". For
-    "tf32x3" a workspace tensor is allocated here (by torch) unless one is passed.
+    `kernel` is one of "ffma" (the product), "naive", "smem32", "tf32x3", "streamk". For
+    "tf32x3" and "streamk" a workspace tensor is allocated here (by torch) unless one is passed.
     """
     import torch
     _check(A, "A")
@@ -211,8 +222,8 @@ def gemm(A, B, out=None, kernel: str = "ffma", workspace=None, stream=None):
     if stream is None:
         stream = torch.cuda.current_stream(A.device).cuda_stream
     fn = getattr(lib(), KERNELS[kernel])
-    if kernel == "tf32x3":
-        need = t2s_gemm_f32_tf32x3_workspace_size(M, N, K)
+    if kernel in ("tf32x3", "streamk"):
+        need = getattr(lib(), KERNELS[kernel] + "_workspace_size")(M, N, K)
         if workspace is None:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
         rc = fn(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(), workspace.data_ptr(),

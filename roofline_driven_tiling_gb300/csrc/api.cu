@@ -173,6 +173,29 @@ int t2s_gemm_f32_splitk(int64_t M, int64_t N, int64_t K, const float* A, const f
   return e == cudaSuccess ? T2S_OK : fail_cuda(e);
 }
 
+size_t t2s_gemm_f32_streamk_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return 0;
+  return streamk_workspace_bytes(M, N, K);
+}
+
+int t2s_gemm_f32_streamk(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                         float* C, void* workspace, size_t workspace_bytes, t2s_stream_t stream) {
+  Problem p{};
+  bool noop = false;
+  const int rc = prepare(M, N, K, A, B, C, stream, &p, &noop);
+  if (rc != T2S_OK || noop) return rc;
+  if (K == 0) return zero_fill(p);
+  if (!streamk_supported(p)) {
+    const cudaError_t e = launch_ffma(p);
+    return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+  }
+  const size_t need = streamk_workspace_bytes(M, N, K);
+  if (workspace == nullptr || workspace_bytes < need) return T2S_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return T2S_ERR_WORKSPACE;
+  const cudaError_t e = launch_ffma_streamk(p, static_cast<float*>(workspace));
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
 size_t t2s_gemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return 0;
   return tf32x3_workspace_bytes(M, N, K);

@@ -148,6 +148,103 @@ __device__ __forceinline__ void tma_stage(const CUtensorMap* tmA, const CUtensor
   tma_load_2d(b_dst, tmB, n0, k0, full_bar);
 }
 
+// One K block of the register-tile product: groups of 8 k values of A and B fragments from
+// the stage at a_base (this thread's first A row) and b_base (its first B column), fused
+// multiply-adds into acc in ascending k.
+template <class Cfg>
+__device__ __forceinline__ void ffma_kblock(uint64_t (&acc)[Cfg::TM][Cfg::TN / 2], uint32_t a_base,
+                                            uint32_t b_base, uint32_t xr) {
+#pragma unroll Cfg::KG_UNROLL
+  for (int kg = 0; kg < Cfg::BK / 8; ++kg) {
+    // 8 k values = two 16-byte chunks of each A row, swizzled.
+    const uint32_t c0 = ((2u * kg) ^ xr) << 4, c1 = ((2u * kg + 1u) ^ xr) << 4;
+    const uint32_t b_kg = b_base + kg * (8 * Cfg::BN * 4);
+#pragma unroll
+    for (int kv = 0; kv < 8 / Cfg::AV; ++kv) {
+      const uint32_t koff = (kv * Cfg::AV < 4 ? c0 : c1) + (kv * Cfg::AV % 4) * 4;
+      float a[Cfg::TM][Cfg::AV];
+#pragma unroll
+      for (int i = 0; i < Cfg::TM; ++i)
+        lds_vec<Cfg::AV>(a_base + i * Cfg::LM * Cfg::A_ROW_BYTES + koff, a[i]);
+#pragma unroll
+      for (int kk = 0; kk < Cfg::AV; ++kk) {
+        uint64_t b[Cfg::TN / 2];
+        const uint32_t b_row = b_kg + (kv * Cfg::AV + kk) * (Cfg::BN * 4);
+#pragma unroll
+        for (int j = 0; j < Cfg::TN / 4; ++j) lds128_pairs(b_row + j * 64, b[2 * j], b[2 * j + 1]);
+#if FFMA_J_OUTER == 1
+        // Column pairs outer, rows inner: consecutive FMAs share the B pair. Measured 3 %
+        // faster than rows outer at 4096^3 and 8192^3 (hoisting the {a, a} moves alone
+        // changes nothing, so the gain is in operand reuse, not in the moves).
+        uint64_t ap[Cfg::TM];
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[i][kk]);
+#pragma unroll
+        for (int j = 0; j < Cfg::TN / 2; ++j)
+#pragma unroll
+          for (int i = 0; i < Cfg::TM; ++i) ffma2(acc[i][j], ap[i], b[j]);
+#elif FFMA_J_OUTER == 2
+        uint64_t ap[Cfg::TM];
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[i][kk]);
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i)
+#pragma unroll
+          for (int j = 0; j < Cfg::TN / 2; ++j) ffma2(acc[i][j], ap[i], b[j]);
+#elif FFMA_J_OUTER == 3
+        // 2 x 2 blocks of (row, column pair)
+        uint64_t ap[Cfg::TM];
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[i][kk]);
+#pragma unroll
+        for (int j = 0; j < Cfg::TN / 2; j += 2)
+#pragma unroll
+          for (int i = 0; i < Cfg::TM; i += 2) {
+            ffma2(acc[i][j], ap[i], b[j]);
+            ffma2(acc[i + 1][j], ap[i + 1], b[j]);
+            ffma2(acc[i][j + 1], ap[i], b[j + 1]);
+            ffma2(acc[i + 1][j + 1], ap[i + 1], b[j + 1]);
+          }
+#else
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i) {
+          const uint64_t ap = pack_dup(a[i][kk]);
+#pragma unroll
+          for (int j = 0; j < Cfg::TN / 2; ++j) ffma2(acc[i][j], ap, b[j]);
+        }
+#endif
+      }
+    }
+  }
+}
+
+// Stores this thread's C tile (rows row0 + 8i, column chunks col0 + 16j) into the row-major
+// matrix C of M x N (ld = N), skipping what lies outside it.
+template <class Cfg>
+__device__ __forceinline__ void store_tile(const uint64_t (&acc)[Cfg::TM][Cfg::TN / 2], float* C,
+                                           int M, int N, int row0, int col0, int vec_store) {
+#pragma unroll
+  for (int i = 0; i < Cfg::TM; ++i) {
+    const int row = row0 + i * Cfg::LM;
+    if (row >= M) continue;
+    float* crow = C + static_cast<int64_t>(row) * N;
+#pragma unroll
+    for (int j = 0; j < Cfg::TN / 4; ++j) {
+      const int col = col0 + 16 * j;
+      const float2 lo = unpack2(acc[i][2 * j]);
+      const float2 hi = unpack2(acc[i][2 * j + 1]);
+      if (vec_store) {
+        if (col < N) *reinterpret_cast<float4*>(crow + col) = make_float4(lo.x, lo.y, hi.x, hi.y);
+      } else {
+        if (col + 0 < N) crow[col + 0] = lo.x;
+        if (col + 1 < N) crow[col + 1] = lo.y;
+        if (col + 2 < N) crow[col + 2] = hi.x;
+        if (col + 3 < N) crow[col + 3] = hi.y;
+      }
+    }
+  }
+}
+
 template <class Cfg, bool kTma>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -250,70 +347,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
       }
       return;
     }
-    const uint32_t a_base = a_stage(s) + a_row0;
-    const uint32_t b_base = b_stage(s) + b_col0;
-#pragma unroll Cfg::KG_UNROLL
-    for (int kg = 0; kg < Cfg::BK / 8; ++kg) {
-      // 8 k values = two 16-byte chunks of each A row, swizzled.
-      const uint32_t c0 = ((2u * kg) ^ xr) << 4, c1 = ((2u * kg + 1u) ^ xr) << 4;
-      const uint32_t b_kg = b_base + kg * (8 * Cfg::BN * 4);
-#pragma unroll
-      for (int kv = 0; kv < 8 / Cfg::AV; ++kv) {
-        const uint32_t koff = (kv * Cfg::AV < 4 ? c0 : c1) + (kv * Cfg::AV % 4) * 4;
-        float a[Cfg::TM][Cfg::AV];
-#pragma unroll
-        for (int i = 0; i < Cfg::TM; ++i)
-          lds_vec<Cfg::AV>(a_base + i * Cfg::LM * Cfg::A_ROW_BYTES + koff, a[i]);
-#pragma unroll
-        for (int kk = 0; kk < Cfg::AV; ++kk) {
-          uint64_t b[Cfg::TN / 2];
-          const uint32_t b_row = b_kg + (kv * Cfg::AV + kk) * (Cfg::BN * 4);
-#pragma unroll
-          for (int j = 0; j < Cfg::TN / 4; ++j) lds128_pairs(b_row + j * 64, b[2 * j], b[2 * j + 1]);
-#if FFMA_J_OUTER == 1
-          // Column pairs outer, rows inner: consecutive FMAs share the B pair. Measured 3 %
-          // faster than rows outer at 4096^3 and 8192^3 (hoisting the {a, a} moves alone
-          // changes nothing, so the gain is in operand reuse, not in the moves).
-          uint64_t ap[Cfg::TM];
-#pragma unroll
-          for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[i][kk]);
-#pragma unroll
-          for (int j = 0; j < Cfg::TN / 2; ++j)
-#pragma unroll
-            for (int i = 0; i < Cfg::TM; ++i) ffma2(acc[i][j], ap[i], b[j]);
-#elif FFMA_J_OUTER == 2
-          uint64_t ap[Cfg::TM];
-#pragma unroll
-          for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[i][kk]);
-#pragma unroll
-          for (int i = 0; i < Cfg::TM; ++i)
-#pragma unroll
-            for (int j = 0; j < Cfg::TN / 2; ++j) ffma2(acc[i][j], ap[i], b[j]);
-#elif FFMA_J_OUTER == 3
-          // 2 x 2 blocks of (row, column pair)
-          uint64_t ap[Cfg::TM];
-#pragma unroll
-          for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[i][kk]);
-#pragma unroll
-          for (int j = 0; j < Cfg::TN / 2; j += 2)
-#pragma unroll
-            for (int i = 0; i < Cfg::TM; i += 2) {
-              ffma2(acc[i][j], ap[i], b[j]);
-              ffma2(acc[i + 1][j], ap[i + 1], b[j]);
-              ffma2(acc[i][j + 1], ap[i], b[j + 1]);
-              ffma2(acc[i + 1][j + 1], ap[i + 1], b[j + 1]);
-            }
-#else
-#pragma unroll
-          for (int i = 0; i < Cfg::TM; ++i) {
-            const uint64_t ap = pack_dup(a[i][kk]);
-#pragma unroll
-            for (int j = 0; j < Cfg::TN / 2; ++j) ffma2(acc[i][j], ap, b[j]);
-          }
-#endif
-        }
-      }
-    }
+    ffma_kblock<Cfg>(acc, a_stage(s) + a_row0, b_stage(s) + b_col0, xr);
     __syncwarp();
     if (lane == 0) {
       if (kTma) {
@@ -333,28 +367,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
   }
 
   // ---------------------------------------------------------------- epilogue
-  const int row0 = m0 + wm0 + g;
-  const int col0 = n0 + wn0 + 4 * h;
-#pragma unroll
-  for (int i = 0; i < Cfg::TM; ++i) {
-    const int row = row0 + i * Cfg::LM;
-    if (row >= M) continue;
-    float* crow = C + static_cast<int64_t>(row) * N;
-#pragma unroll
-    for (int j = 0; j < Cfg::TN / 4; ++j) {
-      const int col = col0 + 16 * j;
-      const float2 lo = unpack2(acc[i][2 * j]);
-      const float2 hi = unpack2(acc[i][2 * j + 1]);
-      if (vec_store) {
-        if (col < N) *reinterpret_cast<float4*>(crow + col) = make_float4(lo.x, lo.y, hi.x, hi.y);
-      } else {
-        if (col + 0 < N) crow[col + 0] = lo.x;
-        if (col + 1 < N) crow[col + 1] = lo.y;
-        if (col + 2 < N) crow[col + 2] = hi.x;
-        if (col + 3 < N) crow[col + 3] = hi.y;
-      }
-    }
-  }
+  store_tile<Cfg>(acc, C, M, N, m0 + wm0 + g, n0 + wn0 + 4 * h, vec_store);
 }
 
 // Launches the kernel over `splits` K chunks of k_chunk values each (splits == 1: the whole
@@ -533,6 +546,287 @@ cudaError_t launch_ffma_splitk(const Problem& p, int splits, float* workspace) {
   const int64_t blocks = (work + 255) / 256 < cap ? (work + 255) / 256 : cap;
   if (v4) reduce_planes_kernel<4><<<static_cast<unsigned>(blocks), 256, 0, p.stream>>>(workspace, p.C, n, planes);
   else reduce_planes_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, p.stream>>>(workspace, p.C, n, planes);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------- stream K
+namespace {
+
+// First iteration of CTA c when `total` iterations are shared out evenly over `ctas` CTAs.
+__host__ __device__ __forceinline__ int64_t sk_begin(int64_t c, int64_t total, int64_t ctas) {
+  return c * total / ctas;
+}
+
+// The CTA whose share holds iteration g: the largest c with sk_begin(c) <= g.
+__host__ __device__ __forceinline__ int64_t sk_owner(int64_t g, int64_t total, int64_t ctas) {
+  return ((g + 1) * ctas - 1) / total;
+}
+
+// Persistent stream-K product (TMA path), the data-parallel + stream-K hybrid of Osama et al.,
+// "Stream-K: Work-centric Parallel Decomposition for Dense Matrix-Matrix Multiplication on the
+// GPU" (PPoPP 2023), which is not on the source pages:
+//  * tiles 0 .. dp_tiles - 1 (whole waves of G = gridDim.x tiles) run data-parallel: CTA c
+//    takes tiles c, c + G, ..., so the tiles in flight at any time are neighbours in the
+//    grouped order and share their A rows and B columns in L2;
+//  * the iterations of the remaining tiles (tile x k block, tiles in the grouped order, k
+//    blocks ascending) are shared out in equal contiguous ranges, CTA c taking the range
+//    [sk_begin(c), sk_begin(c + 1)) of them after its data-parallel tiles.
+// The TMA ring runs on across tiles. A tile whose k blocks all fall to one CTA is stored into
+// C; otherwise the CTA's partial sums of it go to slot 0 (its first stream-K tile) or slot 1
+// (its last) of its pair of BM x BN workspace tiles, and stream_fixup_kernel adds the partial
+// tiles of every shared tile in k order.
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
+    sgemm_ffma_stream_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, float* __restrict__ C,
+                             float* __restrict__ partials, int M, int N, int tiles_m,
+                             int tiles_n, int nkb, int dp_tiles, int64_t sk_total,
+                             unsigned* status, int vec_store) {
+  constexpr int S = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sA = base;
+  const uint32_t sB = sA + S * Cfg::A_STAGE_BYTES;
+  const uint32_t sBar = sB + S * Cfg::B_STAGE_BYTES;  // full[S] (the empty[S] words are unused)
+  const uint32_t sCnt = sBar + 16u * S;                // refill counters
+  __shared__ int issue_tile, issue_kb;                 // next iteration to load
+  auto full = [&](int s) { return sBar + 8u * s; };
+  auto a_stage = [&](int s) { return sA + static_cast<uint32_t>(s) * Cfg::A_STAGE_BYTES; };
+  auto b_stage = [&](int s) { return sB + static_cast<uint32_t>(s) * Cfg::B_STAGE_BYTES; };
+
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  // Data-parallel tiles of this CTA, then its stream-K range.
+  const int n_dp = c < dp_tiles ? (dp_tiles - c + G - 1) / G : 0;
+  const int64_t sk0 = sk_begin(c, sk_total, G), sk1 = sk_begin(c + 1, sk_total, G);
+  const int sk_first_tile = dp_tiles + static_cast<int>(sk0 / nkb);
+  const int sk_first_kb = static_cast<int>(sk0 % nkb);
+  const int count = n_dp * nkb + static_cast<int>(sk1 - sk0);  // the host keeps it < 2^31
+
+  // Origin of tile t in the grouped order (8 tile-rows sweep the columns together).
+  auto origin = [&](int tile, int& m0, int& n0) {
+    constexpr int kGroup = 8;
+    const int per_group = kGroup * tiles_n;
+    const int first_m = (tile / per_group) * kGroup;
+    const int gsz = min(tiles_m - first_m, kGroup);
+    m0 = (first_m + (tile % per_group) % gsz) * Cfg::BM;
+    n0 = ((tile % per_group) / gsz) * Cfg::BN;
+  };
+  // Loads the next iteration into ring slot s and advances the cursor. Loads are issued in
+  // iteration order (the prologue, then the refill of each slot once every warp is done
+  // with it, which happens in slot order), so one cursor serves all issuing threads.
+  auto issue_next = [&](int s) {
+    const int tile = issue_tile, kb = issue_kb;
+    int m0, n0;
+    origin(tile, m0, n0);
+    tma_stage<Cfg>(&tmA, &tmB, m0, n0, kb * Cfg::BK, a_stage(s), b_stage(s), full(s));
+    if (kb + 1 < nkb) {
+      issue_kb = kb + 1;
+    } else if (tile < dp_tiles && tile + G < dp_tiles) {
+      issue_tile = tile + G;  // next data-parallel tile
+      issue_kb = 0;
+    } else if (tile < dp_tiles) {
+      issue_tile = sk_first_tile;  // data-parallel part done: the stream-K range
+      issue_kb = sk_first_kb;
+    } else {
+      issue_tile = tile + 1;
+      issue_kb = 0;
+    }
+  };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1u);
+      asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
+    }
+    mbar_fence_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    issue_tile = n_dp > 0 ? c : sk_first_tile;
+    issue_kb = n_dp > 0 ? 0 : sk_first_kb;
+    for (int j = 0; j < S && j < count; ++j) issue_next(j);
+  }
+  __syncthreads();
+
+  const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
+  const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
+  const int g = lane >> 2, h = lane & 3;
+  const uint32_t a_row0 = static_cast<uint32_t>((wm0 + g) * Cfg::A_ROW_BYTES);
+  const uint32_t xr = (a_row0 >> 7) & Cfg::SWZ_MASK;
+  const uint32_t b_col0 = static_cast<uint32_t>((wn0 + 4 * h) * 4);
+
+  uint64_t acc[Cfg::TM][Cfg::TN / 2];
+  int j = 0;  // local iteration
+  int tile = n_dp > 0 ? c : sk_first_tile;
+  int kb0 = n_dp > 0 ? 0 : sk_first_kb;
+  while (j < count) {
+    // This CTA's part of `tile`: k blocks kb0 .. kb0 + len - 1.
+    const int len = min(nkb - kb0, count - j);
+#pragma unroll
+    for (int i = 0; i < Cfg::TM; ++i)
+#pragma unroll
+      for (int q = 0; q < Cfg::TN / 2; ++q) acc[i][q] = 0ull;
+    for (int jend = j + len; j < jend; ++j) {
+      const int s = j % S;
+      const bool landed = mbar_wait_bounded(full(s), static_cast<uint32_t>(j / S) & 1u, status);
+      if (!__all_sync(0xffffffffu, landed)) {
+        if (lane == 0) {
+          for (int q = j; q < j + S && q < count; ++q)
+            mbar_wait_bounded(full(q % S), static_cast<uint32_t>(q / S) & 1u, status, 10000000ull);
+        }
+        return;
+      }
+      ffma_kblock<Cfg>(acc, a_stage(s) + a_row0, b_stage(s) + b_col0, xr);
+      __syncwarp();
+      if (lane == 0) {
+        // The last warp to finish with this slot refills it with iteration j + S.
+        uint32_t old;
+        asm volatile("atom.shared.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(sCnt + 4u * s) : "memory");
+        if (old == Cfg::WARPS - 1) {
+          asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
+          if (j + S < count) issue_next(s);
+        }
+      }
+    }
+    if (kb0 == 0 && len == nkb) {
+      int m0, n0;
+      origin(tile, m0, n0);
+      store_tile<Cfg>(acc, C, M, N, m0 + wm0 + g, n0 + wn0 + 4 * h, vec_store);
+    } else {
+      float* slot = partials + (2 * static_cast<int64_t>(c) + (tile == sk_first_tile ? 0 : 1)) *
+                                   (Cfg::BM * Cfg::BN);
+      store_tile<Cfg>(acc, slot, Cfg::BM, Cfg::BN, wm0 + g, wn0 + 4 * h, 1);
+    }
+    if (tile < dp_tiles) {
+      tile += G;
+      kb0 = 0;
+      if (tile >= dp_tiles) {
+        tile = sk_first_tile;
+        kb0 = sk_first_kb;
+      }
+    } else {
+      ++tile;
+      kb0 = 0;
+    }
+  }
+}
+
+// Tiles shared by several CTAs: C = P_c0 + P_c0+1 + ... + P_c1, the partial tiles of the CTAs
+// that ran the tile's k blocks, added in that (ascending k) order. kFixupSplit CTAs per tile,
+// each over a contiguous part of the tile in float4 groups (BN % 4 == 0); tiles run whole by
+// one CTA return at once. The slots of the contributors are found once per CTA.
+constexpr int kFixupSplit = 8;
+constexpr int kMaxStreamCtas = 1024;
+
+template <int BM, int BN>
+__global__ void __launch_bounds__(256) stream_fixup_kernel(const float* __restrict__ partials,
+                                                           float* __restrict__ C, int M, int N,
+                                                           int tiles_m, int tiles_n, int nkb,
+                                                           int dp_tiles, int64_t sk_total,
+                                                           int64_t ctas) {
+  __shared__ int slot_of[kMaxStreamCtas];
+  // Stream-K tile t (tile dp_tiles + t of the grouped order).
+  const int64_t t = blockIdx.x / kFixupSplit;
+  const int part = static_cast<int>(blockIdx.x % kFixupSplit);
+  const int64_t c0 = sk_owner(t * nkb, sk_total, ctas);
+  const int64_t c1 = sk_owner((t + 1) * nkb - 1, sk_total, ctas);
+  if (c0 == c1) return;
+  const int n = static_cast<int>(c1 - c0 + 1);
+  for (int q = threadIdx.x; q < n; q += blockDim.x) {
+    const int64_t c = c0 + q;
+    slot_of[q] = static_cast<int>(2 * c + (t == sk_begin(c, sk_total, ctas) / nkb ? 0 : 1));
+  }
+  __syncthreads();
+  constexpr int kGroup = 8;
+  const int tile = dp_tiles + static_cast<int>(t);
+  const int per_group = kGroup * tiles_n;
+  const int first_m = (tile / per_group) * kGroup;
+  const int gsz = min(tiles_m - first_m, kGroup);
+  const int m0 = (first_m + (tile % per_group) % gsz) * BM;
+  const int n0 = ((tile % per_group) / gsz) * BN;
+  constexpr int kVecs = BM * BN / 4;
+  constexpr int kPer = kVecs / kFixupSplit;
+  const float4* P = reinterpret_cast<const float4*>(partials);
+  for (int v = part * kPer + threadIdx.x; v < (part + 1) * kPer; v += blockDim.x) {
+    float4 sum = P[static_cast<int64_t>(slot_of[0]) * kVecs + v];
+    for (int q = 1; q < n; ++q) {
+      const float4 x = P[static_cast<int64_t>(slot_of[q]) * kVecs + v];
+      sum = make_float4(__fadd_rn(sum.x, x.x), __fadd_rn(sum.y, x.y), __fadd_rn(sum.z, x.z),
+                        __fadd_rn(sum.w, x.w));
+    }
+    const int r = (4 * v) / BN, c = (4 * v) % BN;
+    const int row = m0 + r, col = n0 + c;
+    if (row >= M) continue;
+    float* dst = C + static_cast<int64_t>(row) * N + col;
+    if (col + 0 < N) dst[0] = sum.x;
+    if (col + 1 < N) dst[1] = sum.y;
+    if (col + 2 < N) dst[2] = sum.z;
+    if (col + 3 < N) dst[3] = sum.w;
+  }
+}
+
+}  // namespace
+
+// Partial-tile workspace of the stream-K product: two 128 x 128 tiles per CTA.
+size_t streamk_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)M;
+  (void)N;
+  (void)K;
+  const int sms = sm_count();
+  return static_cast<size_t>(2 * (sms > 0 ? sms : 1)) * 2 * 128 * 128 * sizeof(float);
+}
+
+bool streamk_supported(const Problem& p) { return tma_ok(p); }
+
+cudaError_t launch_ffma_streamk(const Problem& p, float* workspace) {
+#ifdef T2S_STREAMK_UNROLLED
+  using Cfg = Big;
+#else
+  using Cfg = BigShortK;
+#endif
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  CUtensorMap ta, tb;
+  cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BK, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  e = encode_tmap_f32_2d(&tb, p.B, p.N, p.K, Cfg::BN, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  auto kern = sgemm_ffma_stream_kernel<Cfg>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES)) !=
+      cudaSuccess)
+    return e;
+  const int64_t tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
+  const int64_t tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
+  const int64_t tiles = tiles_m * tiles_n;
+  const int64_t nkb = (p.K + Cfg::BK - 1) / Cfg::BK;
+  if (tiles * kFixupSplit > 0x7fffffffLL || nkb > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // Two CTAs per SM (the product kernel's occupancy), each with at least 4 k blocks so that
+  // small products do not split into many partial tiles.
+  const int64_t slots = 2 * static_cast<int64_t>(sms);
+  const int64_t by_work = (tiles * nkb + 3) / 4;
+  int64_t ctas = by_work < slots ? by_work : slots;
+  if (ctas > kMaxStreamCtas) ctas = kMaxStreamCtas;
+  // All whole waves but the last run data-parallel; the rest (one to two waves of tiles) is
+  // shared out. A tile count that is a whole number of waves runs all data-parallel.
+  const int64_t waves = tiles / ctas;
+  const int64_t dp_tiles = tiles % ctas == 0 ? tiles : (waves > 0 ? (waves - 1) * ctas : 0);
+  const int64_t sk_tiles = tiles - dp_tiles;
+  const int64_t sk_total = sk_tiles * nkb;
+  const int64_t per_cta = (dp_tiles / ctas + 1) * nkb + sk_total / ctas + 1;
+  if (per_cta > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int vec_store = (p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) ? 1 : 0;
+  kern<<<static_cast<unsigned>(ctas), Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(
+      ta, tb, p.C, workspace, static_cast<int>(p.M), static_cast<int>(p.N),
+      static_cast<int>(tiles_m), static_cast<int>(tiles_n), static_cast<int>(nkb),
+      static_cast<int>(dp_tiles), sk_total, p.status, vec_store);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (sk_tiles > 0) {
+    stream_fixup_kernel<Cfg::BM, Cfg::BN><<<static_cast<unsigned>(sk_tiles * kFixupSplit), 256, 0,
+                                            p.stream>>>(
+        workspace, p.C, static_cast<int>(p.M), static_cast<int>(p.N), static_cast<int>(tiles_m),
+        static_cast<int>(tiles_n), static_cast<int>(nkb), static_cast<int>(dp_tiles), sk_total,
+        ctas);
+  }
   return cudaGetLastError();
 }
 

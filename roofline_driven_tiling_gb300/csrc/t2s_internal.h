@@ -33,6 +33,12 @@ cudaError_t launch_ffma(const Problem& p);
 int splitk_auto(int64_t M, int64_t N, int64_t K);
 int splitk_planes(int64_t K, int splits);
 cudaError_t launch_ffma_splitk(const Problem& p, int splits, float* workspace);
+// Stream K: the flattened tile x k-block space shared evenly over two CTAs per SM, partial
+// tiles of shared tiles in `workspace` (streamk_workspace_bytes), added by a fixup kernel.
+// Needs the TMA path (streamk_supported).
+size_t streamk_workspace_bytes(int64_t M, int64_t N, int64_t K);
+bool streamk_supported(const Problem& p);
+cudaError_t launch_ffma_streamk(const Problem& p, float* workspace);
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tf32x3(const Problem& p, void* workspace);
 // BF16 or FP16 operands (uint16_t bit patterns), FP32 C; workspace for the transposed/padded

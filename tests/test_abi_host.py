@@ -175,3 +175,12 @@ def test_f16_entry_matches_bf16_contract(lib):
     assert f(4, 4, 4, fake + 1, fake + 64, fake + 4096, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
     assert f(4, 4, 4, fake, fake + 64, fake, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
     assert f(0, 4, 4, 0, fake + 64, 0, 0, 0, 0) == binding.T2S_OK
+
+
+def test_streamk_arguments(lib):
+    assert binding.t2s_gemm_f32_streamk_workspace_size(-1, 4, 4) == 0
+    fake = 1 << 20
+    f = binding.t2s_gemm_f32_streamk
+    assert f(-1, 4, 4, fake, fake + 64, fake + 128, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
+    assert f(4, 4, 4, fake, fake + 64, fake, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
+    assert f(0, 4, 4, 0, fake + 64, 0, 0, 0, 0) == binding.T2S_OK

@@ -501,3 +501,89 @@ def test_splitk_workspace_checks():
         binding.T2S_ERR_INVALID
     assert f(*args, ws.data_ptr(), need, s) == binding.T2S_OK
     assert binding.t2s_device_status(s) == binding.T2S_OK
+
+
+# ------------------------------------------------------------------ stream K
+def run_streamk(A, B, shift=0):
+    M, K = A.shape
+    N = B.shape[1]
+    dA = Guarded(A, np.nan, shift)
+    dB = Guarded(B, np.nan, shift)
+    dC = Guarded(np.full((M, N), C_SENTINEL, np.float32), C_SENTINEL, shift)
+    need = binding.t2s_gemm_f32_streamk_workspace_size(M, N, K)
+    ws = torch.full((max(need, 256) // 4,), float("nan"), device="cuda")  # stale partials show
+    s = torch.cuda.current_stream().cuda_stream
+    rc = binding.t2s_gemm_f32_streamk(M, N, K, dA.ptr, dB.ptr, dC.ptr, ws.data_ptr(),
+                                      ws.numel() * 4, s)
+    assert rc == binding.T2S_OK, binding.status_string(rc)
+    assert binding.t2s_device_status(s) == binding.T2S_OK
+    assert dA.guards_intact(np.nan) and dB.guards_intact(np.nan)
+    assert dC.guards_intact(C_SENTINEL), "write outside C"
+    return dC.data()
+
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (2048, 2048, 2048), (1000, 1004, 996),
+                                   (128, 128, 32), (256, 256, 8192), (1536, 1536, 1536),
+                                   (130, 4100, 260), (2304, 640, 1024), (64, 64, 4),
+                                   (5120, 2048, 128), (2048, 2432, 64), (5000, 2044, 100)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_streamk_within_tolerance(shape):
+    """Equal shares of the tile x k-block space: tiles run whole by one CTA, shared by two or
+    by many (long K, few tiles), a single iteration in all (128^3 / 32); with a data-parallel
+    wave before the shared tiles (5120 x 2048: 640 tiles on 304 CTAs) and with a whole number
+    of waves, all data-parallel (2048 x 2432: 304 tiles)."""
+    M, N, K = shape
+    A, B = inputs.uniform_pair(M, N, K, 8)
+    C = run_streamk(A, B)
+    assert np.all(np.isfinite(C))
+    for mode in (oracle.FMA, oracle.MUL_ADD):
+        ref = oracle.sgemm(A, B, mode)
+        assert float(np.max(np.abs(C - ref))) <= tolerance(A, B)
+
+
+def test_streamk_integer_exact_and_deterministic():
+    A, B = inputs.integer_pattern(1536, 1024, 1024)
+    C1 = run_streamk(A, B)
+    C2 = run_streamk(A, B)
+    assert bits_equal(C1, C2)
+    want = oracle.sgemm(A, B, oracle.FMA)
+    assert bits_equal(C1, want), mismatch(C1, want)
+
+
+def test_streamk_headline_sampled():
+    A, B = inputs.uniform_pair(4096, 4096, 4096, 4)
+    C = binding.gemm(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), kernel="streamk")
+    assert binding.device_status() == binding.T2S_OK
+    C = C.cpu().numpy()
+    rows, cols = sample_positions(4096, 4096, np.random.default_rng(44))
+    for mode in (oracle.FMA, oracle.MUL_ADD):
+        ref = oracle.sgemm_at(A, B, rows, cols, mode)
+        assert float(np.max(np.abs(C[rows, cols] - ref))) <= tolerance(A, B)
+
+
+def test_streamk_general_path_is_the_product():
+    """K or N not a multiple of 4 (no TMA): the call runs the product kernel, bit-exact."""
+    A, B = inputs.uniform_pair(300, 257, 131, 9)
+    C = run_streamk(A, B)
+    assert bits_equal(C, oracle.sgemm(A, B, oracle.FMA))
+    A, B = inputs.uniform_pair(300, 256, 128, 9)
+    C = run_streamk(A, B, shift=1)  # misaligned pointers: no TMA either
+    assert bits_equal(C, oracle.sgemm(A, B, oracle.FMA))
+
+
+def test_streamk_workspace_checks():
+    M, N, K = 256, 256, 256
+    dA = torch.zeros((M, K), device="cuda")
+    dB = torch.zeros((K, N), device="cuda")
+    dC = torch.zeros((M, N), device="cuda")
+    need = binding.t2s_gemm_f32_streamk_workspace_size(M, N, K)
+    assert need >= 2 * 128 * 128 * 4
+    ws = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    f = binding.t2s_gemm_f32_streamk
+    a, b, c, w = dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), ws.data_ptr()
+    assert f(M, N, K, a, b, c, 0, need, s) == binding.T2S_ERR_WORKSPACE
+    assert f(M, N, K, a, b, c, w, need - 1, s) == binding.T2S_ERR_WORKSPACE
+    assert f(M, N, K, a, b, c, w + 4, need, s) == binding.T2S_ERR_WORKSPACE
+    assert f(M, N, K, a, b, c, w, need, s) == binding.T2S_OK
+    assert binding.t2s_device_status(s) == binding.T2S_OK
