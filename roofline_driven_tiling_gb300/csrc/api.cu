@@ -119,6 +119,17 @@ __global__ void wait_selftest_kernel(unsigned* status, uint64_t limit_ns) {
 
 void set_last_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
 
+int gemm_f32_block(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+                   t2s_stream_t stream, int concurrent) {
+  Problem p{};
+  bool noop = false;
+  const int rc = prepare(M, N, K, A, B, C, stream, &p, &noop);
+  if (rc != T2S_OK || noop) return rc;
+  if (K == 0) return zero_fill(p);
+  const cudaError_t e = launch_ffma_concurrent(p, concurrent);
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
   return cudaGetLastError();

@@ -121,8 +121,9 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
       if ((e = cudaEventRecord(r->a_ready[i], r->copy_in)) != cudaSuccess) return fail(e);
       if ((e = cudaStreamWaitEvent(cs, r->a_ready[i], 0)) != cudaSuccess) return fail(e);
     }
-    const int rc = t2s_gemm_f32(rows, N, K, has_ab ? dA + r0 * K : nullptr, has_ab ? dB : nullptr,
-                                dC + r0 * N, reinterpret_cast<t2s_stream_t>(cs));
+    // Blocks alternate between two compute streams, so two of them share the GPU.
+    const int rc = gemm_f32_block(rows, N, K, has_ab ? dA + r0 * K : nullptr, has_ab ? dB : nullptr,
+                                  dC + r0 * N, reinterpret_cast<t2s_stream_t>(cs), nb > 1 ? 2 : 1);
     if (rc != T2S_OK) return rc;
     if ((e = cudaEventRecord(r->c_ready[i], cs)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamWaitEvent(r->copy_out, r->c_ready[i], 0)) != cudaSuccess) return fail(e);

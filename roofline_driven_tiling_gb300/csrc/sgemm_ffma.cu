@@ -432,7 +432,9 @@ cudaError_t run_any(const Problem& p, int splits = 1, int k_chunk = 0, float* ou
 
 }  // namespace
 
-cudaError_t launch_ffma(const Problem& p) {
+cudaError_t launch_ffma(const Problem& p) { return launch_ffma_concurrent(p, 1); }
+
+cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -450,7 +452,10 @@ cudaError_t launch_ffma(const Problem& p) {
   // 53.5), the fully unrolled k loop once K >= 256; 64 x 128 tiles around one tile per SM;
   // 64 x 64 tiles otherwise. The last wave decides between neighbours, so the cut points are
   // where the measured curves cross, not a smooth model.
-  const int64_t big_tiles = ((p.M + 127) / 128) * ((p.N + 127) / 128);
+  // `concurrent` products of this size share the GPU (host pipeline blocks on two streams):
+  // the choice follows the tiles in flight together.
+  const int64_t big_tiles =
+      ((p.M + 127) / 128) * ((p.N + 127) / 128) * (concurrent > 1 ? concurrent : 1);
   const int64_t s64 = static_cast<int64_t>(sms);
   if (5 * big_tiles >= 12 * s64) return p.K >= 256 ? run_any<Big>(p) : run_any<BigShortK>(p);
   if (5 * big_tiles >= 4 * s64 && 10 * big_tiles < 11 * s64) return run_any<Mid>(p);

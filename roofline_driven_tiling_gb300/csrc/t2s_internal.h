@@ -28,6 +28,12 @@ struct Problem {
 cudaError_t launch_naive(const Problem& p);
 cudaError_t launch_smem32(const Problem& p);
 cudaError_t launch_ffma(const Problem& p);
+// The product when `concurrent` products of the same size run on the GPU at once (the
+// configuration is chosen for all their tiles together); the same bits as launch_ffma.
+cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent);
+// t2s_gemm_f32 for a block of a larger computation that runs beside `concurrent - 1` others.
+int gemm_f32_block(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+                   t2s_stream_t stream, int concurrent);
 // Split K: `splits` requested chunks (>= 1); partial products in `workspace`
 // (splitk_planes(K, splits) planes of M x N floats), summed into p.C in plane order.
 int splitk_auto(int64_t M, int64_t N, int64_t K);
