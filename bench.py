@@ -485,8 +485,15 @@ def extra_1024(lib, dev, stream, flush, args, ws):
     def streamk(M, N, K, a, b, c, s):
         return lib.t2s_gemm_f32_streamk(M, N, K, a, b, c, wss.data_ptr(), wss.numel(), s)
 
+    wst = torch.empty(max(lib.t2s_gemm_f32_tf32x3_workspace_size(n, n, n), 256),
+                      dtype=torch.uint8, device=dev)
+
+    def tf32x3(M, N, K, a, b, c, s):
+        return lib.t2s_gemm_f32_tf32x3(M, N, K, a, b, c, wst.data_ptr(), wst.numel(), s)
+
     for name, fn in (("ffma", lib.t2s_gemm_f32), ("ffma_splitk_auto", splitk),
-                     ("ffma_streamk", streamk), ("naive", lib.t2s_gemm_f32_naive),
+                     ("ffma_streamk", streamk), ("tf32x3", tf32x3),
+                     ("naive", lib.t2s_gemm_f32_naive),
                      ("smem32", lib.t2s_gemm_f32_smem32)):
         times = time_steps(lambda: fn(n, n, n, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sp),
                            max(args.steps, 10), 3, stream, flush)

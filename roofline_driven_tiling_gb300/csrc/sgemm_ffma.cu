@@ -152,8 +152,9 @@ __device__ __forceinline__ void tma_stage(const CUtensorMap* tmA, const CUtensor
 // the stage at a_base (this thread's first A row) and b_base (its first B column), fused
 // multiply-adds into acc in ascending k.
 template <class Cfg>
-__device__ __forceinline__ void ffma_kblock(uint64_t (&acc)[Cfg::TM][Cfg::TN / 2], uint32_t a_base,
-                                            uint32_t b_base, uint32_t xr) {
+__device__ __forceinline__ void ffma_kblock_direct(uint64_t (&acc)[Cfg::TM][Cfg::TN / 2],
+                                                   uint32_t a_base, uint32_t b_base,
+                                                   uint32_t xr) {
 #pragma unroll Cfg::KG_UNROLL
   for (int kg = 0; kg < Cfg::BK / 8; ++kg) {
     // 8 k values = two 16-byte chunks of each A row, swizzled.
@@ -215,6 +216,54 @@ __device__ __forceinline__ void ffma_kblock(uint64_t (&acc)[Cfg::TM][Cfg::TN / 2
 #endif
       }
     }
+  }
+}
+
+// The same K block with the fragments of k step k + 1 loaded while step k is multiplied (two
+// register sets). It pays where few warps share a sub-partition and latency shows: tiles of at
+// most 64 accumulators per thread (1024^3 with 128 x 64 tiles: 37.0 -> 39.9 TFLOP/s). It made
+// the 128-accumulator tile slower (4096^3: 62.9 -> 61.2), which keeps the direct form.
+template <class Cfg>
+__device__ __forceinline__ void ffma_kblock_pipelined(uint64_t (&acc)[Cfg::TM][Cfg::TN / 2],
+                                                      uint32_t a_base, uint32_t b_base,
+                                                      uint32_t xr) {
+  float a[2][Cfg::TM];
+  uint64_t b[2][Cfg::TN / 2];
+  auto load = [&](int k, int buf) {
+    const uint32_t koff = ((static_cast<uint32_t>(k >> 2) ^ xr) << 4) + (k & 3) * 4;
+#pragma unroll
+    for (int i = 0; i < Cfg::TM; ++i) {
+      float v[1];
+      lds_vec<1>(a_base + i * Cfg::LM * Cfg::A_ROW_BYTES + koff, v);
+      a[buf][i] = v[0];
+    }
+    const uint32_t b_row = b_base + k * (Cfg::BN * 4);
+#pragma unroll
+    for (int j = 0; j < Cfg::TN / 4; ++j)
+      lds128_pairs(b_row + j * 64, b[buf][2 * j], b[buf][2 * j + 1]);
+  };
+  load(0, 0);
+#pragma unroll
+  for (int k = 0; k < Cfg::BK; ++k) {
+    const int cur = k & 1;
+    if (k + 1 < Cfg::BK) load(k + 1, cur ^ 1);
+    uint64_t ap[Cfg::TM];
+#pragma unroll
+    for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[cur][i]);
+#pragma unroll
+    for (int j = 0; j < Cfg::TN / 2; ++j)
+#pragma unroll
+      for (int i = 0; i < Cfg::TM; ++i) ffma2(acc[i][j], ap[i], b[cur][j]);
+  }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void ffma_kblock(uint64_t (&acc)[Cfg::TM][Cfg::TN / 2], uint32_t a_base,
+                                            uint32_t b_base, uint32_t xr) {
+  if constexpr (Cfg::TM * Cfg::TN <= 64) {
+    ffma_kblock_pipelined<Cfg>(acc, a_base, b_base, xr);
+  } else {
+    ffma_kblock_direct<Cfg>(acc, a_base, b_base, xr);
   }
 }
 
@@ -410,14 +459,13 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
 // block when K is long enough to pay for the larger code.
 using Big = FfmaConfig<128, 128, BIG_BK, BIG_STAGES, 2, 2, BIG_AV, 8, 16, FFMA_KG_UNROLL>;
 using BigShortK = FfmaConfig<128, 128, 32, 3, 2, 2, 2, 8, 16, 1>;
-// 64 x 128 tiles of 2 warps: about one 128 x 128 tile per SM (1536^3: 52.2 TFLOP/s against
-// 48.9 for 64 x 64 and 51.8 for 128 x 128 tiles).
-using Mid = FfmaConfig<64, 128, 32, 3, 1, 2, 2, 8, 16, 1>;
 // 4 x 8 per thread (64 x 64 CTA tiles of 4 warps, BK = 32, 3 stages): many small CTAs (four
 // per SM) that even out the last wave. Measured fastest up to ~2.4 tiles of 128 x 128 per SM:
 // 1024^3 37.0 TFLOP/s (BK = 16 and 4 stages: 32.4; 128 x 64 tiles of 8 x 8: 35.8), 2048^3 52.3
 // (128 x 128: 51.1), 2304^3 52.1 (45.9).
 using Small48 = FfmaConfig<64, 64, 32, 3, 2, 2, 2, 4, 8, 1>;
+// 128 x 64 tiles of 4 warps, 8 x 8 per thread (pipelined fragments): about one tile per SM.
+using Tall88 = FfmaConfig<128, 64, 32, 3, 2, 2, 2, 8, 8, 1>;
 
 bool tma_ok(const Problem& p) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.A), b = reinterpret_cast<uintptr_t>(p.B);
@@ -434,6 +482,63 @@ cudaError_t run_any(const Problem& p, int splits = 1, int k_chunk = 0, float* ou
 
 cudaError_t launch_ffma(const Problem& p) { return launch_ffma_concurrent(p, 1); }
 
+namespace {
+
+enum class FfmaPick { kBig, kBigShortK, kTall88, kSmall48 };
+
+// Picks the configuration whose busiest SM has the least work: ceil(tiles / SMs) tiles of the
+// configuration's area, divided by its relative efficiency per FLOP, fitted to a sweep of square
+// and rectangular shapes from 768 to 4096 on GB300: 64 x 64 tiles 1.0, 128 x 64 1.05, 64 x 128
+// 1.04 (never ahead of 128 x 64, so not built); 128 x 128 tiles 1.15 from three tiles per SM on, 1.05 at two and 1.03 at one (with the
+// compact k loop; the fully unrolled one pays only from three). Every measured winner of the
+// sweep is the model's pick, including the non-monotone ones (1280^3 and 2816^3 go to 64 x 64
+// tiles, 1536^3 and 1792^3 to 128 x 64, 2560^3 to 128 x 128). `copies` products of this size
+// share the GPU.
+FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
+  struct Cand {
+    FfmaPick pick;
+    int bm, bn;
+    double eff;
+  };
+  const Cand cands[3] = {{FfmaPick::kBig, 128, 128, 1.15},  // efficiency set per tiles per SM
+                         {FfmaPick::kTall88, 128, 64, 1.05},
+                         {FfmaPick::kSmall48, 64, 64, 1.0}};
+  FfmaPick best = FfmaPick::kSmall48;
+  double best_cost = 0.0;
+  int64_t big_per_sm = 0;
+  for (int i = 0; i < 3; ++i) {
+    const int64_t tiles = ((M + cands[i].bm - 1) / cands[i].bm) * ((N + cands[i].bn - 1) / cands[i].bn) *
+                          (copies > 1 ? copies : 1);
+    const int64_t per_sm = (tiles + sms - 1) / sms;
+    double eff = cands[i].eff;
+    if (cands[i].pick == FfmaPick::kBig) {
+      big_per_sm = per_sm;
+      eff = per_sm >= 3 ? 1.15 : per_sm == 2 ? 1.05 : 1.03;
+    }
+    const double cost = static_cast<double>(per_sm) * cands[i].bm * cands[i].bn / eff;
+    if (i == 0 || cost < best_cost) {
+      best = cands[i].pick;
+      best_cost = cost;
+    }
+  }
+  // The 128 x 128 tile fully unrolls its k loop once K is long enough and every SM runs at
+  // least three tiles.
+  if (best == FfmaPick::kBig && (K < 256 || big_per_sm < 3)) best = FfmaPick::kBigShortK;
+  return best;
+}
+
+template <class... Ts>
+cudaError_t run_pick(FfmaPick pick, const Problem& p, Ts... args) {
+  switch (pick) {
+    case FfmaPick::kBig: return run_any<Big>(p, args...);
+    case FfmaPick::kBigShortK: return run_any<BigShortK>(p, args...);
+    case FfmaPick::kTall88: return run_any<Tall88>(p, args...);
+    default: return run_any<Small48>(p, args...);
+  }
+}
+
+}  // namespace
+
 cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -443,23 +548,17 @@ cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent) {
   switch (FFMA_FORCE_CFG) {
     case 0: return run_any<Big>(p);
     case 1: return run_any<BigShortK>(p);
-    case 2: return run_any<Mid>(p);
     case 3: return run_any<Small48>(p);
+    case 4: return run_any<Tall88>(p);
     default: break;
   }
-  // Thresholds from measurements on GB300 (152 SMs), in 128 x 128 tiles per SM (r): 128 x 128
-  // tiles from r = 2.4 (2560^3: 56.3 TFLOP/s against 53.3 for 64 x 64; 3072^3: 60.3 against
-  // 53.5), the fully unrolled k loop once K >= 256; 64 x 128 tiles around one tile per SM;
-  // 64 x 64 tiles otherwise. The last wave decides between neighbours, so the cut points are
-  // where the measured curves cross, not a smooth model.
-  // `concurrent` products of this size share the GPU (host pipeline blocks on two streams):
-  // the choice follows the tiles in flight together.
-  const int64_t big_tiles =
-      ((p.M + 127) / 128) * ((p.N + 127) / 128) * (concurrent > 1 ? concurrent : 1);
-  const int64_t s64 = static_cast<int64_t>(sms);
-  if (5 * big_tiles >= 12 * s64) return p.K >= 256 ? run_any<Big>(p) : run_any<BigShortK>(p);
-  if (5 * big_tiles >= 4 * s64 && 10 * big_tiles < 11 * s64) return run_any<Mid>(p);
-  return run_any<Small48>(p);
+  // Blocks of a larger product that overlap on two streams (the host pipeline) run 128 x 128
+  // tiles: their copies stagger them, so they share the GPU only in part, and the end-to-end
+  // leg at 4096^3 measured 50.8 TFLOP/s with these tiles against 49.2 with the single-product
+  // choice for two copies (128 x 64).
+  if (concurrent > 1)
+    return run_pick(p.K >= 256 ? FfmaPick::kBig : FfmaPick::kBigShortK, p);
+  return run_pick(pick_ffma(p.M, p.N, p.K, sms, 1), p);
 }
 
 // ---------------------------------------------------------------------------- split K
@@ -534,15 +633,8 @@ cudaError_t launch_ffma_splitk(const Problem& p, int splits, float* workspace) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   // Configuration by the tiles of all chunks together, as for the unsplit product.
-  const int64_t big_tiles = ((p.M + 127) / 128) * ((p.N + 127) / 128) * planes;
-  const int64_t mid_tiles = ((p.M + 63) / 64) * ((p.N + 127) / 128) * planes;
-  const int64_t s64 = static_cast<int64_t>(sms);
   const int chunk = static_cast<int>(kc);
-  cudaError_t e;
-  if (big_tiles >= 4 * s64 && kc >= 256) e = run_any<Big>(p, planes, chunk, workspace);
-  else if (2 * big_tiles >= 3 * s64) e = run_any<BigShortK>(p, planes, chunk, workspace);
-  else if (mid_tiles >= s64) e = run_any<Mid>(p, planes, chunk, workspace);
-  else e = run_any<Small48>(p, planes, chunk, workspace);
+  cudaError_t e = run_pick(pick_ffma(p.M, p.N, kc, sms, planes), p, planes, chunk, workspace);
   if (e != cudaSuccess) return e;
   const int64_t n = p.M * p.N;
   const bool v4 = n % 4 == 0 && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0;

@@ -413,11 +413,11 @@ def test_vector_add_matches_oracle(n, shift):
 # One shape per configuration the dispatcher picks on a 152-SM GB300 (tile counts in the
 # comments), each on the TMA path (aligned) and the cp.async path (K and N not multiples of 4).
 DISPATCH_SHAPES = {
-    "big_4096": (4096, 4096, 1024),        # 1024 tiles of 128^2 >= 2.4 x 152, K >= 256
-    "big_short_k": (3072, 3072, 128),      # 576 tiles of 128^2 >= 2.4 x 152, K < 256
-    "mid_1536": (1536, 1536, 512),         # 144 tiles of 128^2: 0.8 .. 1.1 per SM
-    "small48_2048": (2048, 2048, 128),     # 256 tiles of 128^2: 64 x 64 tiles, 4 x 8 per thread
-    "small48_640": (640, 700, 300),        # 30 tiles of 128^2
+    "big_4096": (4096, 4096, 1024),        # 1024 tiles of 128^2 (7 per SM), K >= 256
+    "big_short_k": (3072, 3072, 128),      # 576 tiles of 128^2, K < 256
+    "tall88_1536": (1536, 1536, 512),      # 288 tiles of 128 x 64: 8 x 8 per thread, pipelined
+    "small48_2048": (2048, 2048, 128),     # 1024 tiles of 64 x 64: 4 x 8 per thread, pipelined
+    "small48_640": (640, 700, 300),        # 110 tiles of 64 x 64
 }
 
 
