@@ -221,35 +221,39 @@ __device__ __forceinline__ void ffma_kblock_direct(uint64_t (&acc)[Cfg::TM][Cfg:
 
 // The same K block with the fragments of k step k + 1 loaded while step k is multiplied (two
 // register sets). It pays where few warps share a sub-partition and latency shows: tiles of at
-// most 64 accumulators per thread (1024^3 with 128 x 64 tiles: 37.0 -> 39.9 TFLOP/s). It made
-// the 128-accumulator tile slower (4096^3: 62.9 -> 61.2), which keeps the direct form.
+// most 64 accumulators per thread (1024^3 with 128 x 64 tiles: 37.0 -> 39.9 TFLOP/s; 2048^3
+// with 64 x 64 tiles: 52.3 -> 54.0). It made the 128-accumulator tile slower (4096^3: 62.9 ->
+// 61.2; B alone one step ahead: 60.8), which keeps the direct form.
 template <class Cfg>
 __device__ __forceinline__ void ffma_kblock_pipelined(uint64_t (&acc)[Cfg::TM][Cfg::TN / 2],
                                                       uint32_t a_base, uint32_t b_base,
                                                       uint32_t xr) {
-  float a[2][Cfg::TM];
+  // A in pairs of k values (one 8-byte load per row every two steps), B per step; each loaded
+  // one step (A: one pair) ahead into the other register set.
+  float a[2][Cfg::TM][2];
   uint64_t b[2][Cfg::TN / 2];
-  auto load = [&](int k, int buf) {
-    const uint32_t koff = ((static_cast<uint32_t>(k >> 2) ^ xr) << 4) + (k & 3) * 4;
+  auto load_a = [&](int k2, int buf) {
+    const uint32_t koff = ((static_cast<uint32_t>(k2 >> 2) ^ xr) << 4) + (k2 & 3) * 4;
 #pragma unroll
-    for (int i = 0; i < Cfg::TM; ++i) {
-      float v[1];
-      lds_vec<1>(a_base + i * Cfg::LM * Cfg::A_ROW_BYTES + koff, v);
-      a[buf][i] = v[0];
-    }
+    for (int i = 0; i < Cfg::TM; ++i)
+      lds_vec<2>(a_base + i * Cfg::LM * Cfg::A_ROW_BYTES + koff, a[buf][i]);
+  };
+  auto load_b = [&](int k, int buf) {
     const uint32_t b_row = b_base + k * (Cfg::BN * 4);
 #pragma unroll
     for (int j = 0; j < Cfg::TN / 4; ++j)
       lds128_pairs(b_row + j * 64, b[buf][2 * j], b[buf][2 * j + 1]);
   };
-  load(0, 0);
+  load_a(0, 0);
+  load_b(0, 0);
 #pragma unroll
   for (int k = 0; k < Cfg::BK; ++k) {
-    const int cur = k & 1;
-    if (k + 1 < Cfg::BK) load(k + 1, cur ^ 1);
+    const int cur = k & 1, abuf = (k >> 1) & 1;
+    if (k + 1 < Cfg::BK) load_b(k + 1, cur ^ 1);
+    if ((k & 1) == 0 && k + 2 < Cfg::BK) load_a(k + 2, abuf ^ 1);
     uint64_t ap[Cfg::TM];
 #pragma unroll
-    for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[cur][i]);
+    for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[abuf][i][k & 1]);
 #pragma unroll
     for (int j = 0; j < Cfg::TN / 2; ++j)
 #pragma unroll
