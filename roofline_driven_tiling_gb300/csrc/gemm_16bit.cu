@@ -13,10 +13,10 @@
 //    K). B (K x N, row-major) is MN-major for the tensor core; when N % 8 == 0 and B is
 //    16-byte aligned it too is read in place (128-byte-swizzled MN-major atoms), otherwise it
 //    is first transposed into an N x Kp K-major plane.
-// 2. The persistent tcgen05 kernel of tc_gemm.cuh: 64-deep k blocks of MMAs with K = 16, K
-//    chunks of 2048 accumulated in TMEM and added into FP32 registers with round-to-nearest by
-//    the epilogue warps. With B in place and more than one 128-row tile row, pairs of CTAs on
-//    two SMs run 256-row tiles with .cta_group::2 MMAs.
+// 2. The persistent tcgen05 kernel of tc_gemm.cuh: 64- or 128-deep k blocks of MMAs with
+//    K = 16, K chunks of 2048 accumulated in TMEM and added into FP32 registers with
+//    round-to-nearest by the epilogue warps. With B in place and more than one 128-row tile
+//    row, pairs of CTAs on two SMs run 256-row tiles with .cta_group::2 MMAs.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(256) pad_rows_16bit_kernel(const uint16_t* __r
 #endif
 
 // The configurations of one 16-bit format (tc::kBf16 or tc::kF16). Tile widths BN (M is 128
-// per CTA), BK = 64 (128-byte rows): wider tiles read A less per FLOP.
+// per CTA), BK = 64 (128-byte rows) unless stated: wider tiles read A less per FLOP.
 template <int KIND>
 struct HalfConfigs {
   static constexpr int C = T2S_HALF_CHUNK_K;
@@ -92,10 +92,12 @@ struct HalfConfigs {
   using M128 = tc::TcConfig<KIND, 128, 64, 6, C, true>;
   using M192 = tc::TcConfig<KIND, 192, 64, 4, C, true>;
   using M256 = tc::TcConfig<KIND, 256, 64, 4, C, true>;
-  // Pairs of CTAs on two SMs, 256-row tiles; each CTA stages 128 rows of A and half of B
-  // (stages of 24 KB and 32 KB).
-  using P128 = tc::TcConfig<KIND, 128, 64, 8, C, true, true>;
-  using P256 = tc::TcConfig<KIND, 256, 64, 6, C, true, true>;
+  // Pairs of CTAs on two SMs, 256-row tiles; each CTA stages 128 rows of A and half of B.
+  // The 256-wide pair stages 128-deep K blocks (3 stages of 64 KB): each stage costs a barrier
+  // round trip between the producer, the MMA issuer and the peer, and 64-deep blocks in 6
+  // stages of 32 KB ran 9 % slower at 4096^3 (1171 against 1283 TFLOP/s).
+  using P128 = tc::TcConfig<KIND, 128, 64, 8, C, true, true>;  // 8 stages of 24 KB
+  using P256 = tc::TcConfig<KIND, 256, 128, 3, C, true, true>;
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -191,12 +191,18 @@ struct TcConfig {
   static constexpr int MMA_K = KIND == kTf32x3 ? 8 : 16;  // K of one instruction (32 bytes)
   static constexpr int PLANES = KIND == kTf32x3 ? 2 : 1;  // smem boxes per operand per stage
   static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "UMMA N for M = 128");
-  static_assert(BK * ELEM == 64 || BK * ELEM == 128, "64- or 128-byte swizzled K-major rows");
+  // K-major A rows are staged in swizzle atoms of up to 128 bytes: a deeper K block is several
+  // atom-wide TMA boxes side by side (16-bit operands with B read in place only).
+  static_assert(BK * ELEM == 64 || BK * ELEM == 128 || (BK * ELEM == 256 && B_MN_),
+                "64- or 128-byte swizzled K-major rows, or two 128-byte atoms");
   // K values accumulated inside the tensor core before the partial sum is added, with
   // round-to-nearest, into the FP32 sums the epilogue warps keep in registers.
   static constexpr int CHUNK_KB = CHUNK_K_ / BK;
   static_assert(CHUNK_K_ % BK == 0 && CHUNK_KB >= 1, "chunk of whole K blocks");
   static constexpr int ROW_BYTES = BK * ELEM;
+  static constexpr int ATOM_BYTES = ROW_BYTES > 128 ? 128 : ROW_BYTES;  // swizzle row width
+  static constexpr int ATOM_COLS = ATOM_BYTES / ELEM;                   // K values per atom row
+  static constexpr int A_SUBS = ROW_BYTES / ATOM_BYTES;                 // A boxes per plane
   static_assert(!B_MN || (KIND != kTf32x3 && BN % 64 == 0),
                 "MN-major B: 16-bit operands in whole 64-column (128-byte) swizzle atoms");
   // MN-major B arrives as BN / 64 TMA boxes of BK K-rows x 64 columns (128 bytes), one after
@@ -206,7 +212,8 @@ struct TcConfig {
   static_assert(!PAIR || (B_MN && B_BOXES % 2 == 0), "pairs split an even number of B boxes");
   static constexpr int G = PAIR ? 2 : 1;                  // CTAs per MMA
   static constexpr int B_BOXES_CTA = B_BOXES / G;          // B boxes this CTA stages
-  static constexpr int A_BYTES = BM * ROW_BYTES;
+  static constexpr int A_BOX_BYTES = BM * ATOM_BYTES;
+  static constexpr int A_BYTES = A_SUBS * A_BOX_BYTES;
   static constexpr int B_BYTES = BN / G * ROW_BYTES;  // this CTA's share of the B tile
   static constexpr int STAGE_BYTES = PLANES * (A_BYTES + B_BYTES);
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atom alignment");
@@ -224,9 +231,9 @@ struct TcConfig {
   static constexpr uint32_t ACC_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
   // Matrix-descriptor swizzle code (bits 61..63): 2 = 128-byte, 4 = 64-byte.
-  static constexpr uint64_t LAYOUT = ROW_BYTES == 128 ? 2 : 4;
-  // Stride between 8-row core groups: 8 rows of ROW_BYTES.
-  static constexpr uint32_t SBO = 8 * ROW_BYTES;
+  static constexpr uint64_t LAYOUT = ATOM_BYTES == 128 ? 2 : 4;
+  // Stride between 8-row core groups: 8 rows of one atom.
+  static constexpr uint32_t SBO = 8 * ATOM_BYTES;
   // Instruction descriptor: D = F32 (bits 4..5 = 1), A and B = TF32 (2), BF16 (1) or FP16 (0)
   // at bits 7..9 and 10..12, both K-major (bits 15, 16 = 0), N >> 3 at bits 17..22, M >> 4 at
   // 24..28.
@@ -379,7 +386,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
             // Both CTAs' copies complete on rank 0's barrier, where the MMAs wait.
             const uint32_t bar0 = map_to_rank(full(s), 0);
             if (rank == 0) mbar_arrive_expect_tx(full(s), 2 * Cfg::STAGE_BYTES);
-            tma_load_2d_pair(st, &tmAb, k0, m0, bar0);
+#pragma unroll
+            for (int q = 0; q < Cfg::A_SUBS; ++q)
+              tma_load_2d_pair(st + q * Cfg::A_BOX_BYTES, &tmAb, k0 + q * Cfg::ATOM_COLS, m0, bar0);
 #pragma unroll
             for (int j = 0; j < Cfg::B_BOXES_CTA; ++j)
               tma_load_2d_pair(st + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &tmBb,
@@ -387,7 +396,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
             continue;
           }
           mbar_arrive_expect_tx(full(s), Cfg::STAGE_BYTES);
-          tma_load_2d(st, &tmAb, k0, m0, full(s));
+#pragma unroll
+          for (int q = 0; q < Cfg::A_SUBS; ++q)
+            tma_load_2d(st + q * Cfg::A_BOX_BYTES, &tmAb, k0 + q * Cfg::ATOM_COLS, m0, full(s));
           if constexpr (Cfg::B_MN) {
 #pragma unroll
             for (int j = 0; j < Cfg::B_BOXES; ++j)
@@ -442,7 +453,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
 #pragma unroll
             for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k) {
               const uint32_t off = k * Cfg::MMA_K * Cfg::ELEM;  // 32 bytes per k step
-              const uint64_t a_big = smem_desc<Cfg>(st + off);
+              // A: the atom box holding this k step, 32-byte offset inside its rows.
+              const uint64_t a_big = smem_desc<Cfg>(st + (off / Cfg::ATOM_BYTES) * Cfg::A_BOX_BYTES +
+                                                    off % Cfg::ATOM_BYTES);
               // MN-major B: a k step is MMA_K whole 128-byte K-rows further on.
               const uint64_t b_big =
                   Cfg::B_MN ? smem_desc_mn<Cfg>(st + Cfg::A_BYTES + k * Cfg::MMA_K * 128)
@@ -567,11 +580,12 @@ cudaError_t run_tc(const Problem& p, const void* a0, const void* a1, const void*
   memset(&tAs, 0, sizeof(tAs));
   memset(&tBs, 0, sizeof(tBs));
   const CUtensorMapSwizzle sw =
-      Cfg::ROW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+      Cfg::ATOM_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   // TMA moves 16-bit elements as they are, so one 16-bit map type serves BF16 and FP16.
   auto enc = [&](CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uint32_t box_rows) {
-    return Cfg::KIND == kTf32x3 ? encode_tmap_f32_2d(m, base, cols, rows, Cfg::BK, box_rows, sw)
-                                : encode_tmap_bf16_2d(m, base, cols, rows, Cfg::BK, box_rows, sw);
+    return Cfg::KIND == kTf32x3
+               ? encode_tmap_f32_2d(m, base, cols, rows, Cfg::ATOM_COLS, box_rows, sw)
+               : encode_tmap_bf16_2d(m, base, cols, rows, Cfg::ATOM_COLS, box_rows, sw);
   };
   cudaError_t e;
   if ((e = enc(&tAb, a0, lda, p.M, Cfg::BM)) != cudaSuccess) return e;
@@ -599,7 +613,8 @@ cudaError_t run_tc(const Problem& p, const void* a0, const void* a1, const void*
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const int vec_store = (p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) ? 1 : 0;
   const int M32 = static_cast<int>(p.M), N32 = static_cast<int>(p.N);
-  const int nkb = static_cast<int>(Kp / Cfg::BK), tm = static_cast<int>(tiles_m),
+  // K blocks over the padded K (TMA fills zeros beyond the matrices' K).
+  const int nkb = static_cast<int>((Kp + Cfg::BK - 1) / Cfg::BK), tm = static_cast<int>(tiles_m),
             tn = static_cast<int>(tiles_n);
   if constexpr (Cfg::PAIR) {
     // One cluster of two CTAs per 256-row tile, at most as many clusters as can be resident

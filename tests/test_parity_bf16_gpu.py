@@ -221,3 +221,17 @@ def test_bf16_paired_tiles(shape):
     A, B = inputs.integer_pattern(M, N, K)
     Ab, Bb = inputs.to_bf16_bits(A), inputs.to_bf16_bits(B)
     assert bits_equal(run_bf16(Ab, Bb), oracle.gemm_bf16(Ab, Bb))
+
+
+@pytest.mark.parametrize("shape", [(512, 512, 192), (300, 256, 72), (640, 512, 4160), (256, 768, 8)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bf16_paired_deep_k_blocks(shape):
+    """256-wide pair tiles stage 128-deep K blocks: K not a multiple of 128 ends in a half-empty
+    block (zeros from TMA), and K < 64 in a single partly filled one."""
+    M, N, K = shape
+    Ab, Bb = inputs.uniform_bf16(M, K, 91 + M), inputs.uniform_bf16(K, N, 93 + N)
+    C = run_bf16(Ab, Bb)
+    assert float(np.max(np.abs(C - oracle.gemm_bf16(Ab, Bb)))) <= tolerance(Ab, Bb)
+    A, B = inputs.integer_pattern(M, N, K)
+    Ab, Bb = inputs.to_bf16_bits(A), inputs.to_bf16_bits(B)
+    assert bits_equal(run_bf16(Ab, Bb), oracle.gemm_bf16(Ab, Bb))
