@@ -92,11 +92,11 @@ struct HalfConfigs {
   using M128 = tc::TcConfig<KIND, 128, 64, 6, C, true>;
   using M192 = tc::TcConfig<KIND, 192, 64, 4, C, true>;
   using M256 = tc::TcConfig<KIND, 256, 64, 4, C, true>;
-  // Pairs of CTAs on two SMs, 256-row tiles; each CTA stages 128 rows of A and half of B.
-  // The 256-wide pair stages 128-deep K blocks (3 stages of 64 KB): each stage costs a barrier
-  // round trip between the producer, the MMA issuer and the peer, and 64-deep blocks in 6
-  // stages of 32 KB ran 9 % slower at 4096^3 (1171 against 1283 TFLOP/s).
-  using P128 = tc::TcConfig<KIND, 128, 64, 8, C, true, true>;  // 8 stages of 24 KB
+  // Pairs of CTAs on two SMs, 256-row tiles; each CTA stages 128 rows of A and half of B, in
+  // 128-deep K blocks: each stage costs a barrier round trip between the producer, the MMA
+  // issuer and the peer, and 64-deep blocks with the same bytes in flight ran slower (4096^3:
+  // 1171 against 1283 TFLOP/s for the 256-wide pair, 825 against 1060 for the 128-wide one).
+  using P128 = tc::TcConfig<KIND, 128, 128, 4, C, true, true>;  // 4 stages of 48 KB
   using P256 = tc::TcConfig<KIND, 256, 128, 3, C, true, true>;
 };
 
@@ -145,10 +145,11 @@ cudaError_t launch_half(int64_t M, int64_t N, int64_t K, const uint16_t* A, cons
   }
   Problem p{M, N, K, nullptr, nullptr, C, stream, status};
   if (N % 8 == 0 && aligned16(B)) {
-    // Weights: measured time of one persistent round per unit of width, relative to 256
-    // (4096^3: 24.7, 26.8 and 29.9 us per round at widths 128, 192, 256).
+    // Weights: measured time of one persistent round per unit of tile area, relative to the
+    // 256-wide pair (4096^3: 18.5 us per round of 256 x 128 pair tiles, 26.8 of 128 x 192
+    // single-SM tiles, 26.8 of 256 x 256 pair tiles).
     const int widths[3] = {128, 192, 256};
-    const double weight[3] = {1.65, 1.19, 1.0};
+    const double weight[3] = {1.38, 1.33, 1.0};
     int best = pick_width(M, N, sms, widths, weight, 3);
 #ifdef T2S_HALF_FORCE_WIDTH
     best = T2S_HALF_FORCE_WIDTH;
