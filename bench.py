@@ -41,6 +41,13 @@ FFMA_PROFILE = os.path.join(ROOT, "profiles", "sgemm_ffma_4096.md")
 TF32X3_PROFILE = os.path.join(ROOT, "profiles", "gemm_tf32x3_4096.md")
 BF16_PROFILE = os.path.join(ROOT, "profiles", "gemm_bf16_4096.md")
 F64_PROFILE = os.path.join(ROOT, "profiles", "dgemm_f64_2048.md")
+# Codes of t2s_gemm_f32_plan.
+PLAN_HUGE_TAIL = 5
+PLAN_NAMES = {0: "128x128x32 tiles", 1: "128x128x32 tiles, compact k loop", 2: "128x64x32 tiles",
+              3: "64x64x32 tiles", 4: "256x128x32 tiles",
+              5: "256x128x32 tiles in whole rounds over the SMs, the rest as 64x64x32 tiles "
+                 "in a second launch"}
+
 KERNEL_SOURCES = {
     "ffma": ["sgemm_ffma.cu", "t2s_device.cuh"],
     "tf32x3": ["gemm_tf32x3.cu", "tc_gemm.cuh", "t2s_device.cuh"],
@@ -282,6 +289,9 @@ def run_ours(args):
             raise binding.T2SError(rc, "t2s_gemm_f32")
 
     flops = rl.gemm_flops(M, N, K)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    plan = binding.t2s_gemm_f32_plan(M, N, K, sms)
+    launches_per_call = 2 if plan == PLAN_HUGE_TAIL else 1
     with ClockSampler(torch.cuda.current_device()) as clk:
         times = time_steps(step, args.steps, max(args.warmup, 3), stream, flush)
     clocks = clk.summary()
@@ -297,7 +307,7 @@ def run_ours(args):
     fp32_peak = rl.fp32_peak_tflops()
     achieved = flops / avg_launch_s / 1e12
     roof = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": UNIT,
-            "frac": achieved / fp32_peak,
+            "frac": achieved / fp32_peak, "launches_per_call": launches_per_call,
             "traffic": profile_traffic(FFMA_PROFILE, "ffma"),
             "peak_basis": "152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz (unit counts and max clock)",
             "algorithmic_flops_per_launch": flops,
@@ -331,12 +341,12 @@ def run_ours(args):
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_block(),
-        "kernel": "t2s_gemm_f32 (packed FP32 FMA, TMA + mbarrier ring, 128x128x32 tiles)",
+        "kernel": "t2s_gemm_f32 (packed FP32 FMA, TMA + mbarrier ring; %s)" % PLAN_NAMES.get(plan, plan),
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * (M * K + K * N),
                 "d2h_bytes_per_step": 4 * M * N,
                 "call": "t2s_gemm_f32_host (pinned host A, B, C; copies overlapped in the call)"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_call,
         "clocks": clocks,
     }
 

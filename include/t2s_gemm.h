@@ -93,6 +93,18 @@ int t2s_gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B
                  float *C, t2s_stream_t stream);
 
 /*
+ * The CTA tiling t2s_gemm_f32 takes for an M x N x K product on a GPU with `sms`
+ * multiprocessors (page "4주차: Roofline과 Tiling", item 8 of "이번 주차 핵심": the tile is
+ * chosen per problem, large tiles for reuse, small ones to fill the machine). A host-only
+ * query: it touches no device, and every choice gives the same bits.
+ *  - Returns 0: 128 x 128 tiles, k loop unrolled over a K block; 1: 128 x 128 tiles, compact
+ *    k loop; 2: 128 x 64 tiles; 3: 64 x 64 tiles; 4: 256 x 128 tiles; 5: 256 x 128 tiles in
+ *    whole rounds of `sms` tiles, then the remaining 256 x 128 tiles as 64 x 64 tiles in a
+ *    second launch. -1 if a dimension is negative or above T2S_MAX_DIM, or sms < 1.
+ */
+int t2s_gemm_f32_plan(int64_t M, int64_t N, int64_t K, int sms);
+
+/*
  * The product of t2s_gemm_f32 for matrices in HOST memory (row-major, same layout),
  * staged through device buffers the caller owns: dA (M*K floats), dB (K*N), dC (M*N).
  * The library copies B, then streams A in row blocks and runs the product of each block
@@ -141,9 +153,9 @@ int t2s_gemm_f32_smem32(int64_t M, int64_t N, int64_t K, const float *A,
  * deterministic and within max |C - C_fp32| <= 1e-6 * K * max|a| * max|b|, but not
  * bit-identical.
  *  - splits: 1..64 chunks requested, or <= 0 for the library's choice (no split when the
- *    product already gives every SM 1.5 tiles of 128 x 128; otherwise about four such tiles
- *    per SM, chunks of at least 64 values, at most 16 chunks). With a single chunk the call
- *    is t2s_gemm_f32.
+ *    product already gives every SM 2.4 tiles of 128 x 128; otherwise about three rounds of
+ *    chunk tiles on two CTAs per SM, chunks of at least 128 values, at most 16 chunks). With
+ *    a single chunk the call is t2s_gemm_f32.
  *  - workspace: a DEVICE buffer, 256-byte aligned, of at least
  *    t2s_gemm_f32_splitk_workspace_size(M, N, K, splits) bytes (0 if no split is made), owned
  *    by the caller and untouched until the stream has run the call.

@@ -31,6 +31,7 @@ _i64, _p, _i, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size
 SIGNATURES = {
     "t2s_gemm_f32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_host": ([_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p], _i),
+    "t2s_gemm_f32_plan": ([_i64, _i64, _i64, _i], _i),
     "t2s_gemm_f32_naive": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_smem32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_splitk_workspace_size": ([_i64, _i64, _i64, _i], _sz),
@@ -90,6 +91,10 @@ def t2s_gemm_f32(M, N, K, A, B, C, stream=0) -> int:
 
 def t2s_gemm_f32_host(M, N, K, hA, hB, hC, dA, dB, dC, stream=0) -> int:
     return lib().t2s_gemm_f32_host(M, N, K, hA, hB, hC, dA, dB, dC, stream)
+
+
+def t2s_gemm_f32_plan(M, N, K, sms) -> int:
+    return lib().t2s_gemm_f32_plan(M, N, K, sms)
 
 
 def t2s_gemm_f32_naive(M, N, K, A, B, C, stream=0) -> int:

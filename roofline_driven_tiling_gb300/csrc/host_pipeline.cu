@@ -20,6 +20,9 @@ namespace {
 #ifndef T2S_PIPE_MIN_ROWS
 #define T2S_PIPE_MIN_ROWS 1024
 #endif
+#ifndef T2S_PIPE_CONCURRENT
+#define T2S_PIPE_CONCURRENT 2
+#endif
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxBlocks = 8;
@@ -123,7 +126,7 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
     }
     // Blocks alternate between two compute streams, so two of them share the GPU.
     const int rc = gemm_f32_block(rows, N, K, has_ab ? dA + r0 * K : nullptr, has_ab ? dB : nullptr,
-                                  dC + r0 * N, reinterpret_cast<t2s_stream_t>(cs), nb > 1 ? 2 : 1);
+                                  dC + r0 * N, reinterpret_cast<t2s_stream_t>(cs), nb > 1 ? T2S_PIPE_CONCURRENT : 1);
     if (rc != T2S_OK) return rc;
     if ((e = cudaEventRecord(r->c_ready[i], cs)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamWaitEvent(r->copy_out, r->c_ready[i], 0)) != cudaSuccess) return fail(e);

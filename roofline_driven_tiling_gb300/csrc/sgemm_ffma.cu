@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
                       const __grid_constant__ CUtensorMap tmB, const float* __restrict__ A,
                       const float* __restrict__ B, float* __restrict__ C, int M, int N, int K,
                       int tiles_m, int tiles_n, unsigned* status, int vec_store, int k_chunk,
-                      int64_t c_plane) {
+                      int64_t c_plane, int wbm, int wbn, int tile_off, int dm, int dn) {
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -317,15 +317,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
   auto a_stage = [&](int s) { return sA + static_cast<uint32_t>(s) * Cfg::A_STAGE_BYTES; };
   auto b_stage = [&](int s) { return sB + static_cast<uint32_t>(s) * Cfg::B_STAGE_BYTES; };
 
-  // Grouped tile order: 8 tile-rows at a time sweep the columns, so that the A rows
-  // and B columns in flight stay resident in L2.
+  // Grouped tile order over the tiles_m x tiles_n grid of wbm x wbn tiles: 8 tile-rows at a
+  // time sweep the columns, so that the A rows and B columns in flight stay resident in L2.
+  // This launch covers tiles tile_off, tile_off + 1, ... of that order, each as dm x dn CTA
+  // tiles of BM x BN (wbm = dm BM, wbn = dn BN); CTA tiles wholly outside C have no work.
   constexpr int kGroup = 8;
-  const int tile = blockIdx.x;
+  const int tile = tile_off + static_cast<int>(blockIdx.x) / (dm * dn);
+  const int sub = static_cast<int>(blockIdx.x) % (dm * dn);
   const int per_group = kGroup * tiles_n;
   const int first_m = (tile / per_group) * kGroup;
   const int gsz = min(tiles_m - first_m, kGroup);
-  const int m0 = (first_m + (tile % per_group) % gsz) * Cfg::BM;
-  const int n0 = ((tile % per_group) / gsz) * Cfg::BN;
+  const int m0 = (first_m + (tile % per_group) % gsz) * wbm + (sub / dn) * Cfg::BM;
+  const int n0 = ((tile % per_group) / gsz) * wbn + (sub % dn) * Cfg::BN;
+  if (m0 >= M || n0 >= N) return;
   // K range of this CTA: chunk blockIdx.y of k_chunk values (the whole of K when the grid
   // has one row), written to plane blockIdx.y of C. k_chunk is a multiple of BK.
   const int kbeg = static_cast<int>(blockIdx.y) * k_chunk;
@@ -423,10 +427,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
   store_tile<Cfg>(acc, C, M, N, m0 + wm0 + g, n0 + wn0 + 4 * h, vec_store);
 }
 
+// A run of the grouped tile order: tiles [off, off + count) of C cut into wbm x wbn tiles
+// (count < 0: to the end). Zero sizes stand for the configuration's own tile.
+struct TilePart {
+  int wbm = 0, wbn = 0;
+  int64_t off = 0, count = -1;
+};
+
 // Launches the kernel over `splits` K chunks of k_chunk values each (splits == 1: the whole
-// product into p.C). Chunk z writes plane z of `out`, planes M x N apart.
+// product into p.C). Chunk z writes plane z of `out`, planes M x N apart. `part` limits the
+// launch to a run of tiles, each computed as CTA tiles of the configuration.
 template <class Cfg, bool kTma>
-cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = nullptr) {
+cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = nullptr,
+                TilePart part = TilePart()) {
   CUtensorMap ta, tb;
   memset(&ta, 0, sizeof(ta));
   memset(&tb, 0, sizeof(tb));
@@ -443,18 +456,25 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int64_t tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
-  const int64_t tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
+  const int wbm = part.wbm > 0 ? part.wbm : Cfg::BM, wbn = part.wbn > 0 ? part.wbn : Cfg::BN;
+  if (wbm % Cfg::BM != 0 || wbn % Cfg::BN != 0) return cudaErrorInvalidConfiguration;
+  const int dm = wbm / Cfg::BM, dn = wbn / Cfg::BN;
+  const int64_t tiles_m = (p.M + wbm - 1) / wbm;
+  const int64_t tiles_n = (p.N + wbn - 1) / wbn;
   const int64_t tiles = tiles_m * tiles_n;
-  if (tiles > 0x7fffffffLL || splits < 1 || splits > 65535) return cudaErrorInvalidConfiguration;
+  const int64_t count = part.count < 0 ? tiles - part.off : part.count;
+  if (part.off < 0 || count < 0 || part.off + count > tiles) return cudaErrorInvalidConfiguration;
+  if (count == 0) return cudaSuccess;
+  if (count * dm * dn > 0x7fffffffLL || splits < 1 || splits > 65535)
+    return cudaErrorInvalidConfiguration;
   float* c = out != nullptr ? out : p.C;
   const int vec_store = (p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(c) & 15u) == 0) ? 1 : 0;
   const int chunk = splits == 1 ? static_cast<int>(p.K) : k_chunk;
-  const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(splits));
+  const dim3 grid(static_cast<unsigned>(count * dm * dn), static_cast<unsigned>(splits));
   kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(
       ta, tb, p.A, p.B, c, static_cast<int>(p.M), static_cast<int>(p.N), static_cast<int>(p.K),
       static_cast<int>(tiles_m), static_cast<int>(tiles_n), p.status, vec_store, chunk,
-      p.M * p.N);
+      p.M * p.N, wbm, wbn, static_cast<int>(part.off), dm, dn);
   return cudaGetLastError();
 }
 
@@ -463,6 +483,11 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
 // block when K is long enough to pay for the larger code.
 using Big = FfmaConfig<128, 128, BIG_BK, BIG_STAGES, 2, 2, BIG_AV, 8, 16, FFMA_KG_UNROLL>;
 using BigShortK = FfmaConfig<128, 128, 32, 3, 2, 2, 2, 8, 16, 1>;
+// 256 x 128 CTA tile, 8 warps (4 x 2 of 64 x 64), 8 x 16 per thread, BK = 32, 3 stages: 144 KB
+// of ring, one CTA (8 warps) per SM. The same warps per SM as two 128 x 128 CTAs but half the
+// staged bytes and barrier rounds per FLOP: in whole rounds 4-5 % faster (3072^3: 63.4 against
+// 60.5 TFLOP/s), while its coarser rounds leave longer tails.
+using Huge = FfmaConfig<256, 128, 32, 3, 4, 2, 2, 8, 16, FFMA_KG_UNROLL>;
 // 4 x 8 per thread (64 x 64 CTA tiles of 4 warps, BK = 32, 3 stages): many small CTAs (four
 // per SM) that even out the last wave. Measured fastest up to ~2.4 tiles of 128 x 128 per SM:
 // 1024^3 37.0 TFLOP/s (BK = 16 and 4 stages: 32.4; 128 x 64 tiles of 8 x 8: 35.8), 2048^3 52.3
@@ -477,9 +502,10 @@ bool tma_ok(const Problem& p) {
 }
 
 template <class Cfg>
-cudaError_t run_any(const Problem& p, int splits = 1, int k_chunk = 0, float* out = nullptr) {
-  return tma_ok(p) ? run<Cfg, true>(p, splits, k_chunk, out)
-                   : run<Cfg, false>(p, splits, k_chunk, out);
+cudaError_t run_any(const Problem& p, int splits = 1, int k_chunk = 0, float* out = nullptr,
+                    TilePart part = TilePart()) {
+  return tma_ok(p) ? run<Cfg, true>(p, splits, k_chunk, out, part)
+                   : run<Cfg, false>(p, splits, k_chunk, out, part);
 }
 
 }  // namespace
@@ -488,16 +514,21 @@ cudaError_t launch_ffma(const Problem& p) { return launch_ffma_concurrent(p, 1);
 
 namespace {
 
-enum class FfmaPick { kBig, kBigShortK, kTall88, kSmall48 };
+// The values are those of t2s_gemm_f32_plan.
+enum class FfmaPick { kBig = 0, kBigShortK = 1, kTall88 = 2, kSmall48 = 3, kHuge = 4, kHugeTail = 5 };
 
 // Picks the configuration whose busiest SM has the least work: ceil(tiles / SMs) tiles of the
 // configuration's area, divided by its relative efficiency per FLOP, fitted to a sweep of square
-// and rectangular shapes from 768 to 4096 on GB300: 64 x 64 tiles 1.0, 128 x 64 1.05, 64 x 128
-// 1.04 (never ahead of 128 x 64, so not built); 128 x 128 tiles 1.15 from three tiles per SM on, 1.05 at two and 1.03 at one (with the
-// compact k loop; the fully unrolled one pays only from three). Every measured winner of the
-// sweep is the model's pick, including the non-monotone ones (1280^3 and 2816^3 go to 64 x 64
-// tiles, 1536^3 and 1792^3 to 128 x 64, 2560^3 to 128 x 128). `copies` products of this size
-// share the GPU.
+// and rectangular shapes from 768 to 8192 on GB300: 64 x 64 tiles 1.0, 128 x 64 1.05, 64 x 128
+// 1.04 (never ahead of 128 x 64, so not built); 128 x 128 tiles 1.15 from three tiles per SM on,
+// 1.05 at two and 1.03 at one (with the compact k loop; the fully unrolled one pays only from
+// three); 256 x 128 tiles 1.17 (K >= 256). The 256 x 128 tiles also run as whole rounds
+// followed by the rest of their tiles cut into 64 x 64 ones, which the tail spreads over all
+// SMs: floor(tiles / SMs) rounds plus ceil(8 x rest / SMs) small tiles. Every measured winner
+// of the sweep is the model's pick, up to 1 %, including the non-monotone ones (1280^3 goes to
+// 64 x 64 tiles, 1536^3 and 1792^3 to 128 x 64, 2048^3 and 3072^3 to 256 x 128, 2560^3,
+// 4096^3 and 6144^3 to 256 x 128 with the 64 x 64 tail). `copies` products of this size share
+// the GPU; they (and K < 256) keep to the one-launch configurations of at most 128 x 128.
 FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
   struct Cand {
     FfmaPick pick;
@@ -507,12 +538,13 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
   const Cand cands[3] = {{FfmaPick::kBig, 128, 128, 1.15},  // efficiency set per tiles per SM
                          {FfmaPick::kTall88, 128, 64, 1.05},
                          {FfmaPick::kSmall48, 64, 64, 1.0}};
+  const int64_t n_copies = copies > 1 ? copies : 1;
   FfmaPick best = FfmaPick::kSmall48;
   double best_cost = 0.0;
   int64_t big_per_sm = 0;
   for (int i = 0; i < 3; ++i) {
     const int64_t tiles = ((M + cands[i].bm - 1) / cands[i].bm) * ((N + cands[i].bn - 1) / cands[i].bn) *
-                          (copies > 1 ? copies : 1);
+                          n_copies;
     const int64_t per_sm = (tiles + sms - 1) / sms;
     double eff = cands[i].eff;
     if (cands[i].pick == FfmaPick::kBig) {
@@ -523,6 +555,25 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
     if (i == 0 || cost < best_cost) {
       best = cands[i].pick;
       best_cost = cost;
+    }
+  }
+  if (n_copies == 1 && K >= 256) {
+    constexpr double kHugeEff = 1.17;
+    const int64_t tiles = ((M + 255) / 256) * ((N + 127) / 128);
+    const double per_tile = 256.0 * 128.0 / kHugeEff;
+    const double whole = static_cast<double>((tiles + sms - 1) / sms) * per_tile;
+    if (whole < best_cost) {
+      best = FfmaPick::kHuge;
+      best_cost = whole;
+    }
+    const int64_t rounds = tiles / sms, rest = tiles % sms;
+    if (rounds >= 1 && rest > 0) {
+      const double split = static_cast<double>(rounds) * per_tile +
+                           static_cast<double>((8 * rest + sms - 1) / sms) * 64.0 * 64.0;
+      if (split < best_cost) {
+        best = FfmaPick::kHugeTail;
+        best_cost = split;
+      }
     }
   }
   // The 128 x 128 tile fully unrolls its k loop once K is long enough and every SM runs at
@@ -541,7 +592,26 @@ cudaError_t run_pick(FfmaPick pick, const Problem& p, Ts... args) {
   }
 }
 
+// 256 x 128 tiles in whole rounds over the SMs, then the rest of them as 64 x 64 tiles in a
+// second launch (disjoint parts of C, so the order of the two launches changes no bit).
+cudaError_t run_huge_tail(const Problem& p, int sms) {
+  const int64_t tiles = ((p.M + 255) / 256) * ((p.N + 127) / 128);
+  const int64_t main = tiles / sms * sms;
+  TilePart head, tail;
+  head.wbm = tail.wbm = Huge::BM;
+  head.wbn = tail.wbn = Huge::BN;
+  head.count = main;
+  tail.off = main;
+  cudaError_t e = run_any<Huge>(p, 1, 0, nullptr, head);
+  if (e != cudaSuccess) return e;
+  return run_any<Small48>(p, 1, 0, nullptr, tail);
+}
+
 }  // namespace
+
+int ffma_plan(int64_t M, int64_t N, int64_t K, int sms) {
+  return static_cast<int>(pick_ffma(M, N, K, sms, 1));
+}
 
 cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent) {
   int dev = 0, sms = 0;
@@ -554,6 +624,8 @@ cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent) {
     case 1: return run_any<BigShortK>(p);
     case 3: return run_any<Small48>(p);
     case 4: return run_any<Tall88>(p);
+    case 5: return run_any<Huge>(p);
+    case 6: return run_huge_tail(p, sms);
     default: break;
   }
   // Blocks of a larger product that overlap on two streams (the host pipeline) run 128 x 128
@@ -562,7 +634,10 @@ cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent) {
   // choice for two copies (128 x 64).
   if (concurrent > 1)
     return run_pick(p.K >= 256 ? FfmaPick::kBig : FfmaPick::kBigShortK, p);
-  return run_pick(pick_ffma(p.M, p.N, p.K, sms, 1), p);
+  const FfmaPick pick = pick_ffma(p.M, p.N, p.K, sms, 1);
+  if (pick == FfmaPick::kHuge) return run_any<Huge>(p);
+  if (pick == FfmaPick::kHugeTail) return run_huge_tail(p, sms);
+  return run_pick(pick, p);
 }
 
 // ---------------------------------------------------------------------------- split K

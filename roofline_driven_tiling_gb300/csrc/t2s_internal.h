@@ -31,6 +31,8 @@ cudaError_t launch_ffma(const Problem& p);
 // The product when `concurrent` products of the same size run on the GPU at once (the
 // configuration is chosen for all their tiles together); the same bits as launch_ffma.
 cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent);
+// The configuration the product takes (the codes of t2s_gemm_f32_plan).
+int ffma_plan(int64_t M, int64_t N, int64_t K, int sms);
 // t2s_gemm_f32 for a block of a larger computation that runs beside `concurrent - 1` others.
 int gemm_f32_block(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
                    t2s_stream_t stream, int concurrent);

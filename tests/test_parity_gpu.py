@@ -413,7 +413,10 @@ def test_vector_add_matches_oracle(n, shift):
 # One shape per configuration the dispatcher picks on a 152-SM GB300 (tile counts in the
 # comments), each on the TMA path (aligned) and the cp.async path (K and N not multiples of 4).
 DISPATCH_SHAPES = {
-    "big_4096": (4096, 4096, 1024),        # 1024 tiles of 128^2 (7 per SM), K >= 256
+    "big_flat": (128, 131072, 288),        # 1024 tiles of 128^2 (7 per SM), K >= 256
+    "huge_2048": (2048, 2048, 512),        # 128 tiles of 256 x 128: one round
+    "huge_tail_2500": (2500, 2000, 512),   # 160 tiles of 256 x 128: 152, then 8 as 64 x 64
+    "huge_tail_4096": (4096, 4096, 1024),  # 512 tiles of 256 x 128: 456, then 56 as 64 x 64
     "big_short_k": (3072, 3072, 128),      # 576 tiles of 128^2, K < 256
     "tall88_1536": (1536, 1536, 512),      # 288 tiles of 128 x 64: 8 x 8 per thread, pipelined
     "small48_2048": (2048, 2048, 128),     # 1024 tiles of 64 x 64: 4 x 8 per thread, pipelined
@@ -433,6 +436,22 @@ def test_every_configuration(name, ragged):
     rows, cols = sample_positions(M, N, np.random.default_rng(K))
     want = oracle.sgemm_at(A, B, rows, cols, oracle.FMA)
     assert bits_equal(C[rows, cols], want), mismatch(C[rows, cols], want)
+
+
+@pytest.mark.parametrize("ragged", [False, True], ids=["tma", "cpasync"])
+def test_huge_tail_every_element(ragged):
+    """256 x 128 tiles in one whole round, the 8 tiles left over as 64 x 64 tiles in a second
+    launch: every element, the ragged last tile row and column included, is the definition's."""
+    M, N, K = 2500, 2000, 512
+    if ragged:
+        N, K = N - 1, K - 3
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert binding.t2s_gemm_f32_plan(M, N, K, 152) == 5
+    A = inputs.uniform(M, K, 71)
+    B = inputs.uniform(K, N, 73)
+    C = run("ffma", A, B)
+    want = oracle.sgemm(A, B, oracle.FMA)
+    assert bits_equal(C, want), mismatch(C, want)
 
 
 # ------------------------------------------------------------------ split K

@@ -1,0 +1,67 @@
+"""The product's choice of CTA tiling (t2s_gemm_f32_plan, a host-only query; no GPU needed).
+
+The plan is pinned to the winners of the measured sweep on a 152-SM GB300 (bit-exact product,
+L2 flushed, TFLOP/s of each forced configuration), and the query's argument checks are tested.
+"""
+from __future__ import annotations
+
+import pytest
+
+from roofline_driven_tiling_gb300 import binding
+
+BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL = range(6)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+# (M, N, K) -> the configuration measured fastest (or within 1 % of it) on GB300.
+MEASURED = {
+    (768, 768, 768): SMALL48,
+    (1024, 1024, 1024): TALL88,
+    (1280, 1280, 1280): SMALL48,
+    (1536, 1536, 1536): TALL88,
+    (1792, 1792, 1792): TALL88,
+    (2048, 2048, 2048): HUGE,         # 55.4 TFLOP/s; 64 x 64 tiles 54.0
+    (2560, 2560, 2560): HUGE_TAIL,    # 59.7; 128 x 128 tiles 56.4
+    (3072, 3072, 3072): HUGE,         # 63.4; 128 x 128 60.5, with the tail 58.2
+    (4096, 4096, 4096): HUGE_TAIL,    # 65.3; 128 x 128 62.8, 256 x 128 alone 57.0
+    (5120, 5120, 5120): HUGE_TAIL,    # 64.8; 128 x 128 63.6
+    (6144, 6144, 6144): HUGE_TAIL,    # 65.6; 128 x 128 63.6
+    (8192, 8192, 8192): HUGE_TAIL,    # 66.3; 128 x 128 66.5
+}
+
+
+@pytest.mark.parametrize("shape", sorted(MEASURED), ids=lambda s: "x".join(map(str, s)))
+def test_plan_matches_measured_winner(shape):
+    assert binding.t2s_gemm_f32_plan(*shape, 152) == MEASURED[shape]
+
+
+def test_plan_short_k_and_copies():
+    # K < 256 keeps to tiles of at most 128 x 128 with the compact k loop.
+    assert binding.t2s_gemm_f32_plan(3072, 3072, 128, 152) == BIG_SHORT_K
+    assert binding.t2s_gemm_f32_plan(16384, 16384, 32, 152) == BIG_SHORT_K
+    # One tile row of 128: the 256-row tile would be half empty.
+    assert binding.t2s_gemm_f32_plan(128, 131072, 288, 152) == BIG
+
+
+def test_plan_tail_only_with_a_whole_round():
+    # Fewer 256 x 128 tiles than SMs: no whole round, so no split launch.
+    assert binding.t2s_gemm_f32_plan(2048, 2048, 512, 152) == HUGE  # 128 tiles
+    # A whole number of rounds: nothing left for a tail.
+    assert binding.t2s_gemm_f32_plan(256 * 19, 128 * 16, 1024, 152) != HUGE_TAIL  # 304 tiles
+    assert binding.t2s_gemm_f32_plan(2500, 2000, 512, 152) == HUGE_TAIL  # 160 = 152 + 8
+
+
+def test_plan_depends_on_sm_count():
+    # The same 4096^3 product on a GPU with 128 SMs: 512 tiles are exactly 4 rounds.
+    assert binding.t2s_gemm_f32_plan(4096, 4096, 4096, 128) == HUGE
+
+
+@pytest.mark.parametrize("args", [(-1, 4, 4, 152), (4, -1, 4, 152), (4, 4, -1, 152),
+                                  ((1 << 30) + 1, 4, 4, 152), (4, 4, 4, 0), (4, 4, 4, -3)])
+def test_plan_rejects_bad_arguments(args):
+    assert binding.t2s_gemm_f32_plan(*args) == -1
