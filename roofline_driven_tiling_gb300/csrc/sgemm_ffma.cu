@@ -484,9 +484,9 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
 using Big = FfmaConfig<128, 128, BIG_BK, BIG_STAGES, 2, 2, BIG_AV, 8, 16, FFMA_KG_UNROLL>;
 using BigShortK = FfmaConfig<128, 128, 32, 3, 2, 2, 2, 8, 16, 1>;
 // 256 x 128 CTA tile, 8 warps (4 x 2 of 64 x 64), 8 x 16 per thread, BK = 32, 3 stages: 144 KB
-// of ring, one CTA (8 warps) per SM. The same warps per SM as two 128 x 128 CTAs but half the
-// staged bytes and barrier rounds per FLOP: in whole rounds 4-5 % faster (3072^3: 63.4 against
-// 60.5 TFLOP/s), while its coarser rounds leave longer tails.
+// of ring, one CTA (8 warps) per SM. The same warps per SM as two 128 x 128 CTAs, with three
+// quarters of the staged bytes and half the barrier rounds per FLOP: in whole rounds 4-5 %
+// faster (3072^3: 63.4 against 60.5 TFLOP/s), while its coarser rounds leave longer tails.
 using Huge = FfmaConfig<256, 128, 32, 3, 4, 2, 2, 8, 16, FFMA_KG_UNROLL>;
 // 4 x 8 per thread (64 x 64 CTA tiles of 4 warps, BK = 32, 3 stages): many small CTAs (four
 // per SM) that even out the last wave. Measured fastest up to ~2.4 tiles of 128 x 128 per SM:

@@ -454,6 +454,26 @@ def test_huge_tail_every_element(ragged):
     assert bits_equal(C, want), mismatch(C, want)
 
 
+def test_huge_tail_result_complete_for_next_launch():
+    """The call is two launches on the caller's stream; work queued after it must see all of
+    C. Here a second product reads the first one's C right away, twice in a row."""
+    M, N, K, N2 = 2500, 2000, 512, 640
+    A = inputs.uniform(M, K, 81)
+    B = inputs.uniform(K, N, 83)
+    B2 = inputs.uniform(N, N2, 85)
+    dA, dB, dB2 = (torch.from_numpy(x).cuda() for x in (A, B, B2))
+    s = torch.cuda.current_stream()
+    for _ in range(2):
+        C1 = binding.gemm(dA, dB, stream=s.cuda_stream)
+        C2 = binding.gemm(C1, dB2, stream=s.cuda_stream)
+    assert binding.device_status() == binding.T2S_OK
+    want1 = oracle.sgemm(A, B, oracle.FMA)
+    want2 = oracle.sgemm(want1, B2, oracle.FMA)
+    assert bits_equal(C1.cpu().numpy(), want1)
+    got2 = C2.cpu().numpy()
+    assert bits_equal(got2, want2), mismatch(got2, want2)
+
+
 # ------------------------------------------------------------------ split K
 def run_splitk(A, B, splits, shift=0):
     M, K = A.shape
