@@ -107,16 +107,22 @@ int t2s_gemm_f32_plan(int64_t M, int64_t N, int64_t K, int sms);
 /*
  * The product of t2s_gemm_f32 for matrices in HOST memory (row-major, same layout),
  * staged through device buffers the caller owns: dA (M*K floats), dB (K*N), dC (M*N).
- * The library copies B, then streams A in row blocks and runs the product of each block
- * as soon as it has arrived, copying every finished block of C back while later blocks
- * compute (host-to-device and device-to-host copies on their own streams). The result is
- * bit-identical to t2s_gemm_f32.
+ * Copies run on their own streams under the products, in one of two schedules, whichever
+ * leaves fewer bytes to copy before the first product starts:
+ *  - row blocks: copy B, then stream A in row blocks, multiplying each block as soon as it
+ *    has arrived and copying its block of C back while later blocks compute;
+ *  - K chunks (K of at least two chunks of about 1024): stream A and B in chunks of K
+ *    (columns of A, rows of B); the product over each chunk resumes from the partial sums
+ *    the previous chunk stored in dC, and the last chunk runs in row blocks whose blocks of
+ *    C are copied back as they finish.
+ * Either way every element is the same chain of fused multiply-adds in ascending k, so the
+ * result is bit-identical to t2s_gemm_f32.
  *  - hA, hB, hC should be page-locked (cudaHostAlloc, cudaHostRegister) for the copies to
  *    run asynchronously and overlap; pageable memory gives the same result, serialised.
  *  - Asynchronous: returns once everything is enqueued; hC is complete, and hA, hB, dA,
  *    dB, dC may be reused, after `stream` has been synchronised.
  *  - Allocates no device memory. The first call on a device creates three streams and
- *    twenty events that the library keeps for later calls; calls from several host
+ *    twenty-one events that the library keeps for later calls; calls from several host
  *    threads are serialised while they enqueue.
  *  - Errors: T2S_ERR_INVALID as for t2s_gemm_f32 (a NULL buffer for a non-empty matrix,
  *    dC equal to dA or dB); T2S_ERR_CUDA if a copy, event or launch fails.

@@ -130,6 +130,18 @@ int gemm_f32_block(int64_t M, int64_t N, int64_t K, const float* A, const float*
   return e == cudaSuccess ? T2S_OK : fail_cuda(e);
 }
 
+int gemm_f32_kchunk(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+                    t2s_stream_t stream, int concurrent, int64_t k0, int64_t kc, bool accumulate) {
+  Problem p{};
+  bool noop = false;
+  const int rc = prepare(M, N, K, A, B, C, stream, &p, &noop);
+  if (rc != T2S_OK || noop) return rc;
+  if (K == 0) return zero_fill(p);
+  if (kc <= 0 || k0 < 0 || k0 >= K || k0 % 32 != 0 || kc % 32 != 0) return T2S_ERR_INVALID;
+  const cudaError_t e = launch_ffma_range(p, concurrent, k0, kc, accumulate);
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
   return cudaGetLastError();

@@ -1,12 +1,23 @@
 // host_pipeline.cu -- C = A x B for matrices in host memory, with the host<->device copies
 // overlapped with the product.
 //
-// The product needs all of B but only a row block of A for a row block of C, so the
-// pipeline is: copy B; then for each row block i of A, copy it, multiply it (on one of two
-// compute streams, so consecutive blocks can share the GPU), and copy the block of C back
-// as soon as it is done. Host->device and device->host copies use separate copy streams,
-// so both directions run under the products. Only the copy of B, the first block of A and
-// the last block of C remain exposed.
+// Two schedules, whichever leaves fewer bytes to copy before the first product can start:
+//
+// Row blocks. The product needs all of B but only a row block of A for a row block of C:
+// copy B; then for each row block i of A, copy it, multiply it (on one of two compute
+// streams, so consecutive blocks can share the GPU), and copy the block of C back as soon
+// as it is done. The copy of B and of the first block of A are exposed.
+//
+// K chunks. The product over K chunk j needs only the columns of A and the rows of B in that
+// chunk: copy chunk j of A (a strided copy of M rows) and of B while chunk j - 1 is being
+// multiplied. Each chunk's product resumes from the accumulators the previous one stored in C
+// (an FP32 value stored and reloaded is the same value, so the chain of fused multiply-adds
+// and the result are those of one pass over K). The last chunk runs as row blocks on two
+// streams, each copied back as soon as it is done. Only the first chunk of A and B is exposed
+// before the products start.
+//
+// Host->device and device->host copies use separate copy streams, so both directions run
+// under the products; the last block of C is copied back after the products in both.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -23,6 +34,18 @@ namespace {
 #ifndef T2S_PIPE_CONCURRENT
 #define T2S_PIPE_CONCURRENT 2
 #endif
+// K values per chunk of the K-chunk schedule (a multiple of 32); the first and the last
+// chunk take 1 / T2S_PIPE_EDGE_DIV of that, so that the products start sooner and the
+// last chunk, which runs in row blocks of T2S_PIPE_TAIL_ROWS, ends sooner.
+#ifndef T2S_PIPE_KCHUNK
+#define T2S_PIPE_KCHUNK 1024
+#endif
+#ifndef T2S_PIPE_EDGE_DIV
+#define T2S_PIPE_EDGE_DIV 2
+#endif
+#ifndef T2S_PIPE_TAIL_ROWS
+#define T2S_PIPE_TAIL_ROWS 512
+#endif
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxBlocks = 8;
@@ -35,6 +58,7 @@ struct PipelineResources {
   bool ready = false;
   cudaStream_t copy_in = nullptr, copy_out = nullptr, compute2 = nullptr;
   cudaEvent_t start = nullptr, b_ready = nullptr, done_out = nullptr, done_compute2 = nullptr;
+  cudaEvent_t chunks_done = nullptr;
   cudaEvent_t a_ready[kMaxBlocks] = {}, c_ready[kMaxBlocks] = {};
 };
 
@@ -59,6 +83,7 @@ cudaError_t resources(PipelineResources** out) {
     if ((e = make_event(&r.b_ready)) != cudaSuccess) return e;
     if ((e = make_event(&r.done_out)) != cudaSuccess) return e;
     if ((e = make_event(&r.done_compute2)) != cudaSuccess) return e;
+    if ((e = make_event(&r.chunks_done)) != cudaSuccess) return e;
     for (int i = 0; i < kMaxBlocks; ++i) {
       if ((e = make_event(&r.a_ready[i])) != cudaSuccess) return e;
       if ((e = make_event(&r.c_ready[i])) != cudaSuccess) return e;
@@ -101,23 +126,77 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
   nb = nb < 1 ? 1 : nb > kMaxBlocks ? kMaxBlocks : nb;
   const int64_t rows_per = (M + nb - 1) / nb;
 
+  // K chunk boundaries: an edge chunk, whole chunks of about T2S_PIPE_KCHUNK values, an
+  // edge chunk; at most kMaxBlocks chunks, every boundary but K a multiple of 32.
+  const int64_t kt = T2S_PIPE_KCHUNK / 32 * 32;
+  const int64_t edge = (kt / T2S_PIPE_EDGE_DIV + 31) / 32 * 32;
+  int64_t kb[kMaxBlocks + 1] = {0};
+  int nk = 0;
+  if (has_ab && K > 2 * edge) {
+    const int64_t mid = K - 2 * edge;
+    int64_t m = (mid + kt - 1) / kt;
+    m = m > kMaxBlocks - 2 ? kMaxBlocks - 2 : m;
+    const int64_t step = m > 0 ? ((mid + m - 1) / m + 31) / 32 * 32 : 0;
+    kb[++nk] = edge;
+    for (int64_t i = 0; i < m && kb[nk] + step < K; ++i, ++nk) kb[nk + 1] = kb[nk] + step;
+    kb[++nk] = K;
+  }
+  // The K-chunk schedule when it has at least two chunks and exposes fewer bytes.
+  const bool by_k = nk >= 2 && kb[1] * (M + N) < K * (N + rows_per);
+  // Its last chunk runs in row blocks of T2S_PIPE_TAIL_ROWS.
+  if (by_k) {
+    nb = static_cast<int>(M / T2S_PIPE_TAIL_ROWS);
+    nb = nb < 1 ? 1 : nb > kMaxBlocks ? kMaxBlocks : nb;
+  }
+  const int64_t rows_blk = (M + nb - 1) / nb;
+
   // Everything starts after the work already enqueued on the caller's stream.
   if ((e = cudaEventRecord(r->start, s)) != cudaSuccess) return fail(e);
   if ((e = cudaStreamWaitEvent(r->copy_in, r->start, 0)) != cudaSuccess) return fail(e);
   if ((e = cudaStreamWaitEvent(r->copy_out, r->start, 0)) != cudaSuccess) return fail(e);
   if ((e = cudaStreamWaitEvent(r->compute2, r->start, 0)) != cudaSuccess) return fail(e);
-  if (has_ab) {
+  int64_t last_k0 = 0;
+  if (by_k) {
+    // Chunk j of A (columns k0 .. k0 + kj - 1 of every row) and of B (rows k0 .. k0 + kj - 1);
+    // the products of all chunks but the last, each resuming from C, on the caller's stream.
+    for (int j = 0; j < nk; ++j) {
+      const int64_t k0 = kb[j], kj = kb[j + 1] - kb[j];
+      if ((e = cudaMemcpy2DAsync(dA + k0, static_cast<size_t>(K) * sizeof(float), hA + k0,
+                                 static_cast<size_t>(K) * sizeof(float),
+                                 static_cast<size_t>(kj) * sizeof(float), static_cast<size_t>(M),
+                                 cudaMemcpyHostToDevice, r->copy_in)) != cudaSuccess)
+        return fail(e);
+      if ((e = cudaMemcpyAsync(dB + k0 * N, hB + k0 * N, static_cast<size_t>(kj) * N * sizeof(float),
+                               cudaMemcpyHostToDevice, r->copy_in)) != cudaSuccess)
+        return fail(e);
+      if ((e = cudaEventRecord(r->a_ready[j], r->copy_in)) != cudaSuccess) return fail(e);
+    }
+    for (int j = 0; j + 1 < nk; ++j) {
+      if ((e = cudaStreamWaitEvent(s, r->a_ready[j], 0)) != cudaSuccess) return fail(e);
+      const int rc = gemm_f32_kchunk(M, N, K, dA, dB, dC, stream, 1, kb[j], kb[j + 1] - kb[j],
+                                     j > 0);
+      if (rc != T2S_OK) return rc;
+    }
+    if ((e = cudaEventRecord(r->chunks_done, s)) != cudaSuccess) return fail(e);
+    if ((e = cudaStreamWaitEvent(r->compute2, r->chunks_done, 0)) != cudaSuccess) return fail(e);
+    if ((e = cudaStreamWaitEvent(s, r->a_ready[nk - 1], 0)) != cudaSuccess) return fail(e);
+    if ((e = cudaStreamWaitEvent(r->compute2, r->a_ready[nk - 1], 0)) != cudaSuccess) return fail(e);
+    last_k0 = kb[nk - 1];
+  } else if (has_ab) {
     if ((e = cudaMemcpyAsync(dB, hB, static_cast<size_t>(K) * N * sizeof(float),
                              cudaMemcpyHostToDevice, r->copy_in)) != cudaSuccess)
       return fail(e);
     if ((e = cudaEventRecord(r->b_ready, r->copy_in)) != cudaSuccess) return fail(e);
   }
+  // Row blocks: the whole product of each block (row-block schedule) or its last K chunk.
+  // Chunk sizes passed on are rounded up to 32; the kernels stop at K.
+  const int64_t last_kc = (K - last_k0 + 31) / 32 * 32;
   for (int i = 0; i < nb; ++i) {
-    const int64_t r0 = i * rows_per;
+    const int64_t r0 = i * rows_blk;
     if (r0 >= M) break;
-    const int64_t rows = (r0 + rows_per <= M) ? rows_per : M - r0;
+    const int64_t rows = (r0 + rows_blk <= M) ? rows_blk : M - r0;
     const cudaStream_t cs = (i & 1) ? r->compute2 : s;
-    if (has_ab) {
+    if (has_ab && !by_k) {
       if ((e = cudaMemcpyAsync(dA + r0 * K, hA + r0 * K, static_cast<size_t>(rows) * K * sizeof(float),
                                cudaMemcpyHostToDevice, r->copy_in)) != cudaSuccess)
         return fail(e);
@@ -125,8 +204,13 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
       if ((e = cudaStreamWaitEvent(cs, r->a_ready[i], 0)) != cudaSuccess) return fail(e);
     }
     // Blocks alternate between two compute streams, so two of them share the GPU.
-    const int rc = gemm_f32_block(rows, N, K, has_ab ? dA + r0 * K : nullptr, has_ab ? dB : nullptr,
-                                  dC + r0 * N, reinterpret_cast<t2s_stream_t>(cs), nb > 1 ? T2S_PIPE_CONCURRENT : 1);
+    const int conc = nb > 1 ? T2S_PIPE_CONCURRENT : 1;
+    const float* a_blk = has_ab ? dA + r0 * K : nullptr;
+    const float* b_all = has_ab ? dB : nullptr;
+    const t2s_stream_t ts = reinterpret_cast<t2s_stream_t>(cs);
+    const int rc = by_k ? gemm_f32_kchunk(rows, N, K, a_blk, b_all, dC + r0 * N, ts, conc, last_k0,
+                                          last_kc, true)
+                        : gemm_f32_block(rows, N, K, a_blk, b_all, dC + r0 * N, ts, conc);
     if (rc != T2S_OK) return rc;
     if ((e = cudaEventRecord(r->c_ready[i], cs)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamWaitEvent(r->copy_out, r->c_ready[i], 0)) != cudaSuccess) return fail(e);

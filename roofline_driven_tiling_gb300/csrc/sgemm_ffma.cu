@@ -298,13 +298,49 @@ __device__ __forceinline__ void store_tile(const uint64_t (&acc)[Cfg::TM][Cfg::T
   }
 }
 
+__device__ __forceinline__ uint64_t pack_pair(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// Loads this thread's C tile (the positions store_tile writes) into the accumulators; +0.0f
+// outside C.
+template <class Cfg>
+__device__ __forceinline__ void load_tile(uint64_t (&acc)[Cfg::TM][Cfg::TN / 2], const float* C,
+                                          int M, int N, int row0, int col0, int vec_load) {
+#pragma unroll
+  for (int i = 0; i < Cfg::TM; ++i) {
+    const int row = row0 + i * Cfg::LM;
+    const float* crow = C + static_cast<int64_t>(row < M ? row : 0) * N;
+#pragma unroll
+    for (int j = 0; j < Cfg::TN / 4; ++j) {
+      const int col = col0 + 16 * j;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row < M) {
+        if (vec_load) {
+          if (col < N) v = *reinterpret_cast<const float4*>(crow + col);
+        } else {
+          if (col + 0 < N) v.x = crow[col + 0];
+          if (col + 1 < N) v.y = crow[col + 1];
+          if (col + 2 < N) v.z = crow[col + 2];
+          if (col + 3 < N) v.w = crow[col + 3];
+        }
+      }
+      acc[i][2 * j] = pack_pair(v.x, v.y);
+      acc[i][2 * j + 1] = pack_pair(v.z, v.w);
+    }
+  }
+}
+
 template <class Cfg, bool kTma>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const float* __restrict__ A,
                       const float* __restrict__ B, float* __restrict__ C, int M, int N, int K,
                       int tiles_m, int tiles_n, unsigned* status, int vec_store, int k_chunk,
-                      int64_t c_plane, int wbm, int wbn, int tile_off, int dm, int dn) {
+                      int64_t c_plane, int wbm, int wbn, int tile_off, int dm, int dn,
+                      int k_base, int accumulate) {
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -330,9 +366,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
   const int m0 = (first_m + (tile % per_group) % gsz) * wbm + (sub / dn) * Cfg::BM;
   const int n0 = ((tile % per_group) / gsz) * wbn + (sub % dn) * Cfg::BN;
   if (m0 >= M || n0 >= N) return;
-  // K range of this CTA: chunk blockIdx.y of k_chunk values (the whole of K when the grid
-  // has one row), written to plane blockIdx.y of C. k_chunk is a multiple of BK.
-  const int kbeg = static_cast<int>(blockIdx.y) * k_chunk;
+  // K range of this CTA: chunk blockIdx.y of k_chunk values from k_base on (the whole of K
+  // when the grid has one row and k_base is 0), written to plane blockIdx.y of C. k_chunk and
+  // k_base are multiples of BK.
+  const int kbeg = k_base + static_cast<int>(blockIdx.y) * k_chunk;
   const int kend = min(K, kbeg + k_chunk);
   C += static_cast<int64_t>(blockIdx.y) * c_plane;
   const int nkb = (kend - kbeg + Cfg::BK - 1) / Cfg::BK;
@@ -365,10 +402,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
   const int g = lane >> 2, h = lane & 3;
 
   uint64_t acc[Cfg::TM][Cfg::TN / 2];
+  if (accumulate) {
+    // Continue the sums already in C (the product over the K values before kbeg): each
+    // accumulator resumes from the FP32 value it was stored as, so the chain of fused
+    // multiply-adds is the same as in one pass over all of K.
+    load_tile<Cfg>(acc, C, M, N, m0 + wm0 + g, n0 + wn0 + 4 * h, vec_store);
+  } else {
 #pragma unroll
-  for (int i = 0; i < Cfg::TM; ++i)
+    for (int i = 0; i < Cfg::TM; ++i)
 #pragma unroll
-    for (int j = 0; j < Cfg::TN / 2; ++j) acc[i][j] = 0ull;  // two +0.0f
+      for (int j = 0; j < Cfg::TN / 2; ++j) acc[i][j] = 0ull;  // two +0.0f
+  }
 
   // This thread's A rows are wm0 + g + 8i: every one has the same swizzle XOR (the row
   // index mod 8 is g), so the swizzle reduces to XORing the chunk index with `xr`.
@@ -432,6 +476,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
 struct TilePart {
   int wbm = 0, wbn = 0;
   int64_t off = 0, count = -1;
+  // K values [k0, k0 + kc) only (kc > 0, multiples of 32), added onto the values in C when
+  // `accumulate` is set.
+  int64_t k0 = 0, kc = 0;
+  int accumulate = 0;
 };
 
 // Launches the kernel over `splits` K chunks of k_chunk values each (splits == 1: the whole
@@ -469,12 +517,17 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
     return cudaErrorInvalidConfiguration;
   float* c = out != nullptr ? out : p.C;
   const int vec_store = (p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(c) & 15u) == 0) ? 1 : 0;
-  const int chunk = splits == 1 ? static_cast<int>(p.K) : k_chunk;
+  if (part.kc > 0 && (splits != 1 || part.k0 % 32 != 0 || part.kc % 32 != 0 || part.k0 < 0 ||
+                      part.k0 >= p.K))
+    return cudaErrorInvalidConfiguration;
+  const int chunk = part.kc > 0 ? static_cast<int>(part.kc)
+                    : splits == 1 ? static_cast<int>(p.K) : k_chunk;
   const dim3 grid(static_cast<unsigned>(count * dm * dn), static_cast<unsigned>(splits));
   kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(
       ta, tb, p.A, p.B, c, static_cast<int>(p.M), static_cast<int>(p.N), static_cast<int>(p.K),
       static_cast<int>(tiles_m), static_cast<int>(tiles_n), p.status, vec_store, chunk,
-      p.M * p.N, wbm, wbn, static_cast<int>(part.off), dm, dn);
+      p.M * p.N, wbm, wbn, static_cast<int>(part.off), dm, dn, static_cast<int>(part.k0),
+      part.accumulate);
   return cudaGetLastError();
 }
 
@@ -594,10 +647,10 @@ cudaError_t run_pick(FfmaPick pick, const Problem& p, Ts... args) {
 
 // 256 x 128 tiles in whole rounds over the SMs, then the rest of them as 64 x 64 tiles in a
 // second launch (disjoint parts of C, so the order of the two launches changes no bit).
-cudaError_t run_huge_tail(const Problem& p, int sms) {
+cudaError_t run_huge_tail(const Problem& p, int sms, const TilePart& range) {
   const int64_t tiles = ((p.M + 255) / 256) * ((p.N + 127) / 128);
   const int64_t main = tiles / sms * sms;
-  TilePart head, tail;
+  TilePart head = range, tail = range;
   head.wbm = tail.wbm = Huge::BM;
   head.wbn = tail.wbn = Huge::BN;
   head.count = main;
@@ -613,19 +666,26 @@ int ffma_plan(int64_t M, int64_t N, int64_t K, int sms) {
   return static_cast<int>(pick_ffma(M, N, K, sms, 1));
 }
 
-cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent) {
+cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int64_t kc,
+                              bool accumulate) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  TilePart range;
+  range.k0 = k0;
+  range.kc = kc;
+  range.accumulate = accumulate ? 1 : 0;
+  // The configuration is chosen by the K values this launch covers.
+  const int64_t span = kc > 0 ? (p.K - k0 < kc ? p.K - k0 : kc) : p.K;
   switch (FFMA_FORCE_CFG) {
-    case 0: return run_any<Big>(p);
-    case 1: return run_any<BigShortK>(p);
-    case 3: return run_any<Small48>(p);
-    case 4: return run_any<Tall88>(p);
-    case 5: return run_any<Huge>(p);
-    case 6: return run_huge_tail(p, sms);
+    case 0: return run_any<Big>(p, 1, 0, nullptr, range);
+    case 1: return run_any<BigShortK>(p, 1, 0, nullptr, range);
+    case 3: return run_any<Small48>(p, 1, 0, nullptr, range);
+    case 4: return run_any<Tall88>(p, 1, 0, nullptr, range);
+    case 5: return run_any<Huge>(p, 1, 0, nullptr, range);
+    case 6: return run_huge_tail(p, sms, range);
     default: break;
   }
   // Blocks of a larger product that overlap on two streams (the host pipeline) run 128 x 128
@@ -633,11 +693,15 @@ cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent) {
   // leg at 4096^3 measured 50.8 TFLOP/s with these tiles against 49.2 with the single-product
   // choice for two copies (128 x 64).
   if (concurrent > 1)
-    return run_pick(p.K >= 256 ? FfmaPick::kBig : FfmaPick::kBigShortK, p);
-  const FfmaPick pick = pick_ffma(p.M, p.N, p.K, sms, 1);
-  if (pick == FfmaPick::kHuge) return run_any<Huge>(p);
-  if (pick == FfmaPick::kHugeTail) return run_huge_tail(p, sms);
-  return run_pick(pick, p);
+    return run_pick(span >= 256 ? FfmaPick::kBig : FfmaPick::kBigShortK, p, 1, 0, nullptr, range);
+  const FfmaPick pick = pick_ffma(p.M, p.N, span, sms, 1);
+  if (pick == FfmaPick::kHuge) return run_any<Huge>(p, 1, 0, nullptr, range);
+  if (pick == FfmaPick::kHugeTail) return run_huge_tail(p, sms, range);
+  return run_pick(pick, p, 1, 0, nullptr, range);
+}
+
+cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent) {
+  return launch_ffma_range(p, concurrent, 0, 0, false);
 }
 
 // ---------------------------------------------------------------------------- split K

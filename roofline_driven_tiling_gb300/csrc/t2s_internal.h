@@ -31,11 +31,20 @@ cudaError_t launch_ffma(const Problem& p);
 // The product when `concurrent` products of the same size run on the GPU at once (the
 // configuration is chosen for all their tiles together); the same bits as launch_ffma.
 cudaError_t launch_ffma_concurrent(const Problem& p, int concurrent);
+// The product over the K values [k0, k0 + kc) only (kc > 0; k0 and kc multiples of 32,
+// k0 < K), added onto the values already in p.C when `accumulate` is set: the accumulators
+// resume from C, so consecutive chunks give the same bits as one pass over K.
+cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int64_t kc,
+                              bool accumulate);
 // The configuration the product takes (the codes of t2s_gemm_f32_plan).
 int ffma_plan(int64_t M, int64_t N, int64_t K, int sms);
 // t2s_gemm_f32 for a block of a larger computation that runs beside `concurrent - 1` others.
 int gemm_f32_block(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
                    t2s_stream_t stream, int concurrent);
+// The same for the K values [k0, k0 + kc) of the product, added onto C when `accumulate`
+// is set (see launch_ffma_range).
+int gemm_f32_kchunk(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+                    t2s_stream_t stream, int concurrent, int64_t k0, int64_t kc, bool accumulate);
 // Split K: `splits` requested chunks (>= 1); partial products in `workspace`
 // (splitk_planes(K, splits) planes of M x N floats), summed into p.C in plane order.
 int splitk_auto(int64_t M, int64_t N, int64_t K);
