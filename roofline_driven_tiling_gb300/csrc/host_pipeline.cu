@@ -12,9 +12,10 @@
 // chunk: copy chunk j of A (a strided copy of M rows) and of B while chunk j - 1 is being
 // multiplied. Each chunk's product resumes from the accumulators the previous one stored in C
 // (an FP32 value stored and reloaded is the same value, so the chain of fused multiply-adds
-// and the result are those of one pass over K). The last chunk runs as row blocks on two
-// streams, each copied back as soon as it is done. Only the first chunk of A and B is exposed
-// before the products start.
+// and the result are those of one pass over K). Once the operands have arrived (estimated
+// from the copy and FLOP rates), the rest of K runs as row blocks on two streams, each block
+// of C copied back as soon as it is done, so that the copy back overlaps the products. Only
+// the first chunk of A and B is exposed before the products start.
 //
 // Host->device and device->host copies use separate copy streams, so both directions run
 // under the products; the last block of C is copied back after the products in both.
@@ -35,8 +36,8 @@ namespace {
 #define T2S_PIPE_CONCURRENT 2
 #endif
 // K values per chunk of the K-chunk schedule (a multiple of 32); the first and the last
-// chunk take 1 / T2S_PIPE_EDGE_DIV of that, so that the products start sooner and the
-// last chunk, which runs in row blocks of T2S_PIPE_TAIL_ROWS, ends sooner.
+// chunk take 1 / T2S_PIPE_EDGE_DIV of that, so that the products start sooner. The rest of
+// K after the switch runs in row blocks of T2S_PIPE_TAIL_ROWS.
 #ifndef T2S_PIPE_KCHUNK
 #define T2S_PIPE_KCHUNK 1024
 #endif
@@ -44,7 +45,18 @@ namespace {
 #define T2S_PIPE_EDGE_DIV 2
 #endif
 #ifndef T2S_PIPE_TAIL_ROWS
-#define T2S_PIPE_TAIL_ROWS 512
+#define T2S_PIPE_TAIL_ROWS 1024
+#endif
+// The K-chunk schedule switches to row blocks over the rest of K once the operands have
+// arrived, estimated from these rates (percent scale on the estimate for tuning).
+#ifndef T2S_PIPE_COPY_GBS
+#define T2S_PIPE_COPY_GBS 200.0
+#endif
+#ifndef T2S_PIPE_TFLOPS
+#define T2S_PIPE_TFLOPS 60.0
+#endif
+#ifndef T2S_PIPE_SWITCH_PCT
+#define T2S_PIPE_SWITCH_PCT 100
 #endif
 
 constexpr int kMaxDevices = 64;
@@ -143,7 +155,7 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
   }
   // The K-chunk schedule when it has at least two chunks and exposes fewer bytes.
   const bool by_k = nk >= 2 && kb[1] * (M + N) < K * (N + rows_per);
-  // Its last chunk runs in row blocks of T2S_PIPE_TAIL_ROWS.
+  // The rest of K after the switch runs in row blocks of T2S_PIPE_TAIL_ROWS.
   if (by_k) {
     nb = static_cast<int>(M / T2S_PIPE_TAIL_ROWS);
     nb = nb < 1 ? 1 : nb > kMaxBlocks ? kMaxBlocks : nb;
@@ -158,7 +170,7 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
   int64_t last_k0 = 0;
   if (by_k) {
     // Chunk j of A (columns k0 .. k0 + kj - 1 of every row) and of B (rows k0 .. k0 + kj - 1);
-    // the products of all chunks but the last, each resuming from C, on the caller's stream.
+    // the products of the first chunks, each resuming from C, on the caller's stream.
     for (int j = 0; j < nk; ++j) {
       const int64_t k0 = kb[j], kj = kb[j + 1] - kb[j];
       if ((e = cudaMemcpy2DAsync(dA + k0, static_cast<size_t>(K) * sizeof(float), hA + k0,
@@ -171,7 +183,16 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
         return fail(e);
       if ((e = cudaEventRecord(r->a_ready[j], r->copy_in)) != cudaSuccess) return fail(e);
     }
-    for (int j = 0; j + 1 < nk; ++j) {
+    // The chunks multiplied over all rows: enough of them to cover the copies, after which
+    // the row blocks take the rest of K (their C blocks then go back while later blocks
+    // compute). The copy of the operands takes about (M + N) K 4 bytes / copy rate, the
+    // product 2 M N K / FLOP rate.
+    const double copy_s = 4.0 * static_cast<double>(M + N) * K / (T2S_PIPE_COPY_GBS * 1e9);
+    const double per_k_s = 2.0 * static_cast<double>(M) * N / (T2S_PIPE_TFLOPS * 1e12);
+    const double k_cover = copy_s / per_k_s * (T2S_PIPE_SWITCH_PCT / 100.0);
+    int p = 1;
+    while (p < nk - 1 && static_cast<double>(kb[p]) < k_cover) ++p;
+    for (int j = 0; j < p; ++j) {
       if ((e = cudaStreamWaitEvent(s, r->a_ready[j], 0)) != cudaSuccess) return fail(e);
       const int rc = gemm_f32_kchunk(M, N, K, dA, dB, dC, stream, 1, kb[j], kb[j + 1] - kb[j],
                                      j > 0);
@@ -181,14 +202,14 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
     if ((e = cudaStreamWaitEvent(r->compute2, r->chunks_done, 0)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamWaitEvent(s, r->a_ready[nk - 1], 0)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamWaitEvent(r->compute2, r->a_ready[nk - 1], 0)) != cudaSuccess) return fail(e);
-    last_k0 = kb[nk - 1];
+    last_k0 = kb[p];
   } else if (has_ab) {
     if ((e = cudaMemcpyAsync(dB, hB, static_cast<size_t>(K) * N * sizeof(float),
                              cudaMemcpyHostToDevice, r->copy_in)) != cudaSuccess)
       return fail(e);
     if ((e = cudaEventRecord(r->b_ready, r->copy_in)) != cudaSuccess) return fail(e);
   }
-  // Row blocks: the whole product of each block (row-block schedule) or its last K chunk.
+  // Row blocks: the whole product of each block (row-block schedule) or the rest of its K.
   // Chunk sizes passed on are rounded up to 32; the kernels stop at K.
   const int64_t last_kc = (K - last_k0 + 31) / 32 * 32;
   for (int i = 0; i < nb; ++i) {
