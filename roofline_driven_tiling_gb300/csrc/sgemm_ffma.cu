@@ -548,6 +548,12 @@ using Huge = FfmaConfig<256, 128, 32, 3, 4, 2, 2, 8, 16, FFMA_KG_UNROLL>;
 using Small48 = FfmaConfig<64, 64, 32, 3, 2, 2, 2, 4, 8, 1>;
 // 128 x 64 tiles of 4 warps, 8 x 8 per thread (pipelined fragments): about one tile per SM.
 using Tall88 = FfmaConfig<128, 64, 32, 3, 2, 2, 2, 8, 8, 1>;
+// Tiles of 8 warps for problems of at most one tile per SM, where a CTA runs alone on its SM
+// and its latency shows: 128 x 128 of 8 x 8 per thread (1536^3: 55.9 TFLOP/s against 52.6
+// with two 128 x 64 tiles per SM) and 128 x 64 of 8 x 4 per thread (1024^3: 41.4 against
+// 39.9 with 4 warps of 8 x 8).
+using Big88 = FfmaConfig<128, 128, 32, 3, 2, 4, 2, 8, 8, 1>;
+using Tall84 = FfmaConfig<128, 64, 32, 3, 2, 4, 2, 8, 4, 1>;
 
 bool tma_ok(const Problem& p) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.A), b = reinterpret_cast<uintptr_t>(p.B);
@@ -568,19 +574,30 @@ cudaError_t launch_ffma(const Problem& p) { return launch_ffma_concurrent(p, 1);
 namespace {
 
 // The values are those of t2s_gemm_f32_plan.
-enum class FfmaPick { kBig = 0, kBigShortK = 1, kTall88 = 2, kSmall48 = 3, kHuge = 4, kHugeTail = 5 };
+enum class FfmaPick {
+  kBig = 0,
+  kBigShortK = 1,
+  kTall88 = 2,
+  kSmall48 = 3,
+  kHuge = 4,
+  kHugeTail = 5,
+  kBig88 = 6,
+  kTall84 = 7
+};
 
 // Picks the configuration whose busiest SM has the least work: ceil(tiles / SMs) tiles of the
 // configuration's area, divided by its relative efficiency per FLOP, fitted to a sweep of square
 // and rectangular shapes from 768 to 8192 on GB300: 64 x 64 tiles 1.0, 128 x 64 1.05, 64 x 128
 // 1.04 (never ahead of 128 x 64, so not built); 128 x 128 tiles 1.15 from three tiles per SM on,
 // 1.05 at two and 1.03 at one (with the compact k loop; the fully unrolled one pays only from
-// three); 256 x 128 tiles 1.17 (K >= 256). The 256 x 128 tiles also run as whole rounds
+// three); 256 x 128 tiles 1.17 (K >= 256); the 8-warp tiles only where they come to at most
+// one per SM: 128 x 128 1.116, 128 x 64 1.091. The 256 x 128 tiles also run as whole rounds
 // followed by the rest of their tiles cut into 64 x 64 ones, which the tail spreads over all
 // SMs: floor(tiles / SMs) rounds plus ceil(8 x rest / SMs) small tiles. Every measured winner
-// of the sweep is the model's pick, up to 1 %, including the non-monotone ones (1280^3 goes to
-// 64 x 64 tiles, 1536^3 and 1792^3 to 128 x 64, 2048^3 and 3072^3 to 256 x 128, 2560^3,
-// 4096^3 and 6144^3 to 256 x 128 with the 64 x 64 tail). `copies` products of this size share
+// of the sweep is the model's pick, up to 1 %, including the non-monotone ones (1024^3 goes to
+// 128 x 64 tiles of 8 warps, 1280^3 to 64 x 64, 1536^3 to 128 x 128 of 8 warps, 1792^3 to
+// 128 x 64, 2048^3 and 3072^3 to 256 x 128, 2560^3, 4096^3 and 6144^3 to 256 x 128 with the
+// 64 x 64 tail). `copies` products of this size share
 // the GPU; they (and K < 256) keep to the one-launch configurations of at most 128 x 128.
 FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
   struct Cand {
@@ -608,6 +625,19 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
     if (i == 0 || cost < best_cost) {
       best = cands[i].pick;
       best_cost = cost;
+    }
+  }
+  {
+    const Cand one[2] = {{FfmaPick::kBig88, 128, 128, 1.116}, {FfmaPick::kTall84, 128, 64, 1.091}};
+    for (int i = 0; i < 2; ++i) {
+      const int64_t tiles = ((M + one[i].bm - 1) / one[i].bm) * ((N + one[i].bn - 1) / one[i].bn) *
+                            n_copies;
+      if (tiles > sms) continue;
+      const double cost = static_cast<double>(one[i].bm) * one[i].bn / one[i].eff;
+      if (cost < best_cost) {
+        best = one[i].pick;
+        best_cost = cost;
+      }
     }
   }
   if (n_copies == 1 && K >= 256) {
@@ -641,6 +671,8 @@ cudaError_t run_pick(FfmaPick pick, const Problem& p, Ts... args) {
     case FfmaPick::kBig: return run_any<Big>(p, args...);
     case FfmaPick::kBigShortK: return run_any<BigShortK>(p, args...);
     case FfmaPick::kTall88: return run_any<Tall88>(p, args...);
+    case FfmaPick::kBig88: return run_any<Big88>(p, args...);
+    case FfmaPick::kTall84: return run_any<Tall84>(p, args...);
     default: return run_any<Small48>(p, args...);
   }
 }

@@ -9,7 +9,7 @@ import pytest
 
 from roofline_driven_tiling_gb300 import binding
 
-BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL = range(6)
+BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL, BIG88, TALL84 = range(8)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -21,9 +21,9 @@ def built():
 # (M, N, K) -> the configuration measured fastest (or within 1 % of it) on GB300.
 MEASURED = {
     (768, 768, 768): SMALL48,
-    (1024, 1024, 1024): TALL88,
+    (1024, 1024, 1024): TALL84,       # 41.4; 4 warps of 8 x 8 39.9
     (1280, 1280, 1280): SMALL48,
-    (1536, 1536, 1536): TALL88,
+    (1536, 1536, 1536): BIG88,        # 55.9; 128 x 64 tiles 52.6
     (1792, 1792, 1792): TALL88,
     (2048, 2048, 2048): HUGE,         # 55.4 TFLOP/s; 64 x 64 tiles 54.0
     (2560, 2560, 2560): HUGE_TAIL,    # 59.7; 128 x 128 tiles 56.4
@@ -54,6 +54,15 @@ def test_plan_tail_only_with_a_whole_round():
     # A whole number of rounds: nothing left for a tail.
     assert binding.t2s_gemm_f32_plan(256 * 19, 128 * 16, 1024, 152) != HUGE_TAIL  # 304 tiles
     assert binding.t2s_gemm_f32_plan(2500, 2000, 512, 152) == HUGE_TAIL  # 160 = 152 + 8
+
+
+def test_plan_eight_warp_tiles_only_for_one_round():
+    # 128 tiles of 128 x 64 on 152 SMs: one each, 8 warps.
+    assert binding.t2s_gemm_f32_plan(1024, 1024, 512, 152) == TALL84
+    # 162 tiles of 128 x 64 would need a second round on some SMs: not the 8-warp tile.
+    assert binding.t2s_gemm_f32_plan(1152, 1152, 1152, 152) != TALL84
+    assert binding.t2s_gemm_f32_plan(1408, 1408, 1408, 152) == BIG88   # 121 tiles of 128^2
+    assert binding.t2s_gemm_f32_plan(1792, 1792, 512, 152) == TALL88  # 196 tiles of 128^2
 
 
 def test_plan_depends_on_sm_count():
