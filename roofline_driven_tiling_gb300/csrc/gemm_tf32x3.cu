@@ -67,25 +67,39 @@ __device__ __forceinline__ void split(float x, float& big, float& small) {
   small = isfinite(x) ? tf32_round(__fsub_rn(x, big)) : 0.0f;
 }
 
-// A (M x K, row-major) -> big, small (M x Kp), zeros for k >= K. Four k per thread.
+// A (M x K, row-major) -> big, small (M x Kp), zeros for k >= K. Four k per thread, rows
+// along the grid's y (no 64-bit division per element); 16-byte loads when every row starts
+// on a 16-byte boundary (kVec: K % 4 == 0 and A 16-byte aligned).
+template <bool kVec>
 __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict__ A,
                                                          float* __restrict__ big,
                                                          float* __restrict__ small, int64_t M,
                                                          int64_t K, int64_t Kp) {
   const int64_t q = Kp / 4;
-  const int64_t total = M * q;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row = idx / q;
-    const int64_t k = (idx % q) * 4;
-    float b[4], s[4];
+  for (int64_t row = blockIdx.y; row < M; row += gridDim.y) {
+    const float* arow = A + row * K;
+    float* brow = big + row * Kp;
+    float* srow = small + row * Kp;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < q;
+         c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t k = 4 * c;
+      float x[4];
+      if (kVec && k + 3 < K) {
+        const float4 v = *reinterpret_cast<const float4*>(arow + k);
+        x[0] = v.x;
+        x[1] = v.y;
+        x[2] = v.z;
+        x[3] = v.w;
+      } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float x = (k + e < K) ? A[row * K + k + e] : 0.0f;
-      split(x, b[e], s[e]);
+        for (int e = 0; e < 4; ++e) x[e] = (k + e < K) ? arow[k + e] : 0.0f;
+      }
+      float b[4], s[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split(x[e], b[e], s[e]);
+      *reinterpret_cast<float4*>(brow + k) = make_float4(b[0], b[1], b[2], b[3]);
+      *reinterpret_cast<float4*>(srow + k) = make_float4(s[0], s[1], s[2], s[3]);
     }
-    *reinterpret_cast<float4*>(big + row * Kp + k) = make_float4(b[0], b[1], b[2], b[3]);
-    *reinterpret_cast<float4*>(small + row * Kp + k) = make_float4(s[0], s[1], s[2], s[3]);
   }
 }
 
@@ -151,10 +165,12 @@ cudaError_t launch_tf32x3(const Problem& p, void* workspace) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   {
-    const int64_t work = p.M * (Kp / 4);
-    const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(sms) * 16);
-    split_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, p.stream>>>(p.A, a_big, a_small,
-                                                                           p.M, p.K, Kp);
+    const int64_t gx = std::min<int64_t>((Kp / 4 + 255) / 256, 64);
+    const int64_t gy = std::min<int64_t>(p.M, 65535);
+    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+    const bool vec = p.K % 4 == 0 && (reinterpret_cast<uintptr_t>(p.A) & 15u) == 0;
+    if (vec) split_rows_kernel<true><<<grid, 256, 0, p.stream>>>(p.A, a_big, a_small, p.M, p.K, Kp);
+    else split_rows_kernel<false><<<grid, 256, 0, p.stream>>>(p.A, a_big, a_small, p.M, p.K, Kp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
