@@ -78,3 +78,13 @@ def test_place_point():
     assert math.isclose(p["frac_of_roof"], p["tflops"] / 80.0)
     low = rl.place(flops=1e9, seconds=1e-3, nbytes=1e9, peak_tflops=80.0, bw_gbs=8000.0)
     assert low["region"] == "memory" and low["roof_tflops"] == pytest.approx(8.0)
+
+
+def test_sweep_covers_the_sweep_configuration():
+    """The roofline sweep tool measures the square shapes 128^3 .. 8192^3, the two low-AI
+    shapes and the ragged one, for every FP32 entry point (no GPU needed to check this)."""
+    from roofline_driven_tiling_gb300 import sweep
+    squares = {(n, n, n) for n in (128, 256, 512, 1024, 2048, 4096, 8192)}
+    assert squares <= set(sweep.SHAPES)
+    assert {(16384, 16384, 32), (8192, 8192, 64), (1000, 1003, 997)} <= set(sweep.SHAPES)
+    assert set(sweep.KERNELS) == {"ffma", "tf32x3", "splitk", "streamk", "smem32", "naive"}
