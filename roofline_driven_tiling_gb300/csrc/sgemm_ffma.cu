@@ -582,7 +582,8 @@ enum class FfmaPick {
   kHuge = 4,
   kHugeTail = 5,
   kBig88 = 6,
-  kTall84 = 7
+  kTall84 = 7,
+  kPersistent = 8
 };
 
 // Picks the configuration whose busiest SM has the least work: ceil(tiles / SMs) tiles of the
@@ -662,6 +663,12 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
   // The 128 x 128 tile fully unrolls its k loop once K is long enough and every SM runs at
   // least three tiles.
   if (best == FfmaPick::kBig && (K < 256 || big_per_sm < 3)) best = FfmaPick::kBigShortK;
+  // With a single K block per tile nothing in a CTA overlaps the load of its operands; a
+  // persistent grid loads the next tile's while this one computes and stores (16384^2 x 32:
+  // 47.6 against 42.3 TFLOP/s). From two K blocks on it measured slower (8192^2 x 64: 50.3
+  // against 53.6).
+  if (best == FfmaPick::kBigShortK && n_copies == 1 && K <= 32 && big_per_sm > 2)
+    best = FfmaPick::kPersistent;
   return best;
 }
 
@@ -727,6 +734,11 @@ cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int6
   if (concurrent > 1)
     return run_pick(span >= 256 ? FfmaPick::kBig : FfmaPick::kBigShortK, p, 1, 0, nullptr, range);
   const FfmaPick pick = pick_ffma(p.M, p.N, span, sms, 1);
+  if (pick == FfmaPick::kPersistent) {
+    // The persistent loop covers whole products on the TMA path only.
+    if (kc == 0 && tma_ok(p)) return launch_ffma_persistent(p);
+    return run_pick(FfmaPick::kBigShortK, p, 1, 0, nullptr, range);
+  }
   if (pick == FfmaPick::kHuge) return run_any<Huge>(p, 1, 0, nullptr, range);
   if (pick == FfmaPick::kHugeTail) return run_huge_tail(p, sms, range);
   return run_pick(pick, p, 1, 0, nullptr, range);
@@ -1049,6 +1061,39 @@ size_t streamk_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 }
 
 bool streamk_supported(const Problem& p) { return tma_ok(p); }
+
+// The persistent loop of the stream-K kernel with every tile data-parallel: 2 CTAs per SM walk
+// tiles c, c + G, ... of the grouped order with one TMA ring across tiles, so the next tile's
+// operands load while this tile computes and stores. Each tile is summed by one CTA in
+// ascending k: the bits of the product.
+cudaError_t launch_ffma_persistent(const Problem& p) {
+  using Cfg = BigShortK;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  CUtensorMap ta, tb;
+  cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BK, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  e = encode_tmap_f32_2d(&tb, p.B, p.N, p.K, Cfg::BN, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  auto kern = sgemm_ffma_stream_kernel<Cfg>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES)) !=
+      cudaSuccess)
+    return e;
+  const int64_t tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
+  const int64_t tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
+  const int64_t tiles = tiles_m * tiles_n;
+  const int64_t nkb = (p.K + Cfg::BK - 1) / Cfg::BK;
+  const int64_t slots = 2 * static_cast<int64_t>(sms);
+  const int64_t ctas = tiles < slots ? tiles : slots;
+  if (tiles > 0x7fffffffLL || (tiles / ctas + 1) * nkb > 0x7fffffffLL)
+    return cudaErrorInvalidConfiguration;
+  const int vec_store = (p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) ? 1 : 0;
+  kern<<<static_cast<unsigned>(ctas), Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(
+      ta, tb, p.C, nullptr, static_cast<int>(p.M), static_cast<int>(p.N),
+      static_cast<int>(tiles_m), static_cast<int>(tiles_n), static_cast<int>(nkb),
+      static_cast<int>(tiles), 0, p.status, vec_store);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_ffma_streamk(const Problem& p, float* workspace) {
 #ifdef T2S_STREAMK_UNROLLED

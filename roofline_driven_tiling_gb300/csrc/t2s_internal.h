@@ -56,6 +56,9 @@ cudaError_t launch_ffma_splitk(const Problem& p, int splits, float* workspace);
 size_t streamk_workspace_bytes(int64_t M, int64_t N, int64_t K);
 bool streamk_supported(const Problem& p);
 cudaError_t launch_ffma_streamk(const Problem& p, float* workspace);
+// The product on a persistent grid (2 CTAs per SM, one TMA ring across tiles); TMA path
+// only (K % 4 == 0, N % 4 == 0, 16-byte aligned A and B). The bits of launch_ffma.
+cudaError_t launch_ffma_persistent(const Problem& p);
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tf32x3(const Problem& p, void* workspace);
 // BF16 or FP16 operands (uint16_t bit patterns), FP32 C; workspace for the transposed/padded

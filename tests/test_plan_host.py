@@ -9,7 +9,7 @@ import pytest
 
 from roofline_driven_tiling_gb300 import binding
 
-BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL, BIG88, TALL84 = range(8)
+BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL, BIG88, TALL84, PERSISTENT = range(9)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -43,7 +43,10 @@ def test_plan_matches_measured_winner(shape):
 def test_plan_short_k_and_copies():
     # K < 256 keeps to tiles of at most 128 x 128 with the compact k loop.
     assert binding.t2s_gemm_f32_plan(3072, 3072, 128, 152) == BIG_SHORT_K
-    assert binding.t2s_gemm_f32_plan(16384, 16384, 32, 152) == BIG_SHORT_K
+    assert binding.t2s_gemm_f32_plan(8192, 8192, 64, 152) == BIG_SHORT_K
+    # One K block per tile: the persistent grid (47.6 against 42.3 TFLOP/s at 16384^2 x 32).
+    assert binding.t2s_gemm_f32_plan(16384, 16384, 32, 152) == PERSISTENT
+    assert binding.t2s_gemm_f32_plan(16384, 16384, 33, 152) == BIG_SHORT_K
     # One tile row of 128: the 256-row tile would be half empty.
     assert binding.t2s_gemm_f32_plan(128, 131072, 288, 152) == BIG
 
