@@ -93,6 +93,34 @@ def sample_positions(M, N, rng, n_random=4096):
     return np.concatenate(r), np.concatenate(c)
 
 
+def split_round_positions(M, N, rng):
+    """The bottom-right 512 x 512 corner (the tiles of the last, partial round when 256 x 256
+    pair tiles do not fill whole rounds, as in 2560 x 2048 on 76 SM pairs), the last row and
+    column, and random positions."""
+    r0, c0 = M - 512, N - 512
+    rr, cc = np.meshgrid(np.arange(r0, M), np.arange(c0, N), indexing="ij")
+    rows = [rr.ravel(), np.full(N, M - 1), np.arange(M), rng.integers(0, M, 4096)]
+    cols = [cc.ravel(), np.arange(N), np.full(M, N - 1), rng.integers(0, N, 4096)]
+    return np.concatenate(rows), np.concatenate(cols)
+
+
+def test_bf16_split_last_round_exact():
+    """2560 x 2048 x 4096: 80 pair tiles on 76 pairs, so the last 4 run as one unit per K
+    chunk and a fix-up adds the partial tiles. Integer-valued operands make every sum exact:
+    the split tiles must equal the definition bit for bit, like the others."""
+    M, N, K = 2560, 2048, 4096
+    A, B = inputs.integer_pattern(M, N, K)
+    Ab, Bb = inputs.to_bf16_bits(A), inputs.to_bf16_bits(B)
+    dA = torch.from_numpy(Ab.view(np.int16)).cuda().view(torch.bfloat16)
+    dB = torch.from_numpy(Bb.view(np.int16)).cuda().view(torch.bfloat16)
+    C = binding.gemm_bf16(dA, dB)
+    assert binding.device_status() == binding.T2S_OK
+    C = C.cpu().numpy()
+    rows, cols = split_round_positions(M, N, np.random.default_rng(5))
+    want = oracle.gemm_bf16_at(Ab, Bb, rows, cols)
+    assert bits_equal(C[rows, cols], want)
+
+
 @pytest.mark.parametrize("shape", [(256, 256, 256), (1024, 1024, 1024), (1000, 1003, 997),
                                    (129, 65, 24)], ids=lambda s: "x".join(map(str, s)))
 def test_bf16_integer_pattern_exact(shape):

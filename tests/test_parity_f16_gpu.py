@@ -65,6 +65,20 @@ def test_f16_integer_pattern_exact(shape):
     assert h.bits_equal(run_f16(Ab, Bb), oracle.gemm_f16(Ab, Bb))
 
 
+def test_f16_split_last_round_exact():
+    """The BF16 split-round case for binary16: 80 pair tiles on 76 pairs, integer operands."""
+    M, N, K = 2560, 2048, 4096
+    A, B = inputs.integer_pattern(M, N, K)
+    Ab, Bb = inputs.to_f16_bits(A), inputs.to_f16_bits(B)
+    dA = torch.from_numpy(Ab.view(np.int16)).cuda().view(torch.float16)
+    dB = torch.from_numpy(Bb.view(np.int16)).cuda().view(torch.float16)
+    C = binding.gemm_f16(dA, dB)
+    assert binding.device_status() == binding.T2S_OK
+    C = C.cpu().numpy()
+    rows, cols = h.split_round_positions(M, N, np.random.default_rng(6))
+    assert h.bits_equal(C[rows, cols], oracle.gemm_f16_at(Ab, Bb, rows, cols))
+
+
 def test_f16_dyadic_exact_misaligned():
     A = inputs.dyadic(300, 77, seed=31, denom=256, span=1000)
     B = inputs.dyadic(77, 192, seed=32, denom=16, span=64)
