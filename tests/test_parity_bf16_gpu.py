@@ -94,9 +94,9 @@ def sample_positions(M, N, rng, n_random=4096):
 
 
 def split_round_positions(M, N, rng):
-    """The bottom-right 512 x 512 corner (the tiles of the last, partial round when 256 x 256
-    pair tiles do not fill whole rounds, as in 2560 x 2048 on 76 SM pairs), the last row and
-    column, and random positions."""
+    """The bottom-right 512 x 512 corner (the tiles of the last, partial round of the
+    persistent grid when 256 x 256 pair tiles do not fill whole rounds, as in 2560 x 2048 on
+    76 SM pairs), the last row and column, and random positions."""
     r0, c0 = M - 512, N - 512
     rr, cc = np.meshgrid(np.arange(r0, M), np.arange(c0, N), indexing="ij")
     rows = [rr.ravel(), np.full(N, M - 1), np.arange(M), rng.integers(0, M, 4096)]
@@ -104,10 +104,10 @@ def split_round_positions(M, N, rng):
     return np.concatenate(rows), np.concatenate(cols)
 
 
-def test_bf16_split_last_round_exact():
-    """2560 x 2048 x 4096: 80 pair tiles on 76 pairs, so the last 4 run as one unit per K
-    chunk and a fix-up adds the partial tiles. Integer-valued operands make every sum exact:
-    the split tiles must equal the definition bit for bit, like the others."""
+def test_bf16_partial_last_round_exact():
+    """2560 x 2048 x 4096: 80 pair tiles on 76 pairs, so 4 clusters run a second tile, two K
+    chunks each. Integer-valued operands make every sum exact: those tiles must equal the
+    definition bit for bit, like the others."""
     M, N, K = 2560, 2048, 4096
     A, B = inputs.integer_pattern(M, N, K)
     Ab, Bb = inputs.to_bf16_bits(A), inputs.to_bf16_bits(B)

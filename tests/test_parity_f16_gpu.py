@@ -65,8 +65,8 @@ def test_f16_integer_pattern_exact(shape):
     assert h.bits_equal(run_f16(Ab, Bb), oracle.gemm_f16(Ab, Bb))
 
 
-def test_f16_split_last_round_exact():
-    """The BF16 split-round case for binary16: 80 pair tiles on 76 pairs, integer operands."""
+def test_f16_partial_last_round_exact():
+    """The BF16 partial-round case for binary16: 80 pair tiles on 76 pairs, integer operands."""
     M, N, K = 2560, 2048, 4096
     A, B = inputs.integer_pattern(M, N, K)
     Ab, Bb = inputs.to_f16_bits(A), inputs.to_f16_bits(B)
