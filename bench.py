@@ -201,7 +201,9 @@ def run_reference(args):
     oracle.build()
     w = WORKLOAD
     A, B = inputs.uniform_pair(w["M"], w["N"], w["K"], w["config_no"])
-    per_step = float(os.environ.get("T2S_REF_STEP_SECONDS", "4"))
+    # About two minutes of CPU work for the whole run, at most 4 s a step.
+    budget = min(4.0, max(0.05, 120.0 / max(1, args.steps + args.warmup)))
+    per_step = float(os.environ.get("T2S_REF_STEP_SECONDS", budget))
     for _ in range(args.warmup):
         cpu_oracle_rate(A, B, min(per_step, 1.0))
     rates, infos = [], []
