@@ -16,7 +16,8 @@
 // 2. The persistent tcgen05 kernel of tc_gemm.cuh: 64- or 128-deep k blocks of MMAs with
 //    K = 16, K chunks of 2048 accumulated in TMEM and added into FP32 registers with
 //    round-to-nearest by the epilogue warps. With B in place and more than one 128-row tile
-//    row, pairs of CTAs on two SMs run 256-row tiles with .cta_group::2 MMAs.
+//    row, pairs of CTAs on two SMs run 256-row tiles with .cta_group::2 MMAs; the widest of
+//    them, 256 x 512, sum all of K in TMEM (K <= 16384).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -77,6 +78,11 @@ __global__ void __launch_bounds__(256) pad_rows_16bit_kernel(const uint16_t* __r
 #ifndef T2S_HALF_CHUNK_K
 #define T2S_HALF_CHUNK_K 2048
 #endif
+// Longest K for the 512-wide pair tiles, whose tensor cores sum all of K without the
+// round-to-nearest chunk additions (error at K = 8192: 2.0e-3 against a bound of 8.2e-3).
+#ifndef T2S_WIDE_MAX_K
+#define T2S_WIDE_MAX_K 16384
+#endif
 
 // The configurations of one 16-bit format (tc::kBf16 or tc::kF16). Tile widths BN (M is 128
 // per CTA), BK = 64 (128-byte rows) unless stated: wider tiles read A less per FLOP.
@@ -98,6 +104,10 @@ struct HalfConfigs {
   // 1171 against 1283 TFLOP/s for the 256-wide pair, 825 against 1060 for the 128-wide one).
   using P128 = tc::TcConfig<KIND, 128, 128, 4, C, true, true>;  // 4 stages of 48 KB
   using P256 = tc::TcConfig<KIND, 256, 128, 3, C, true, true>;
+  // 256 x 512 pair tiles: two N = 256 MMAs per k step into one 512-column accumulator, the
+  // tensor core summing all of K; 4 stages of 48 KB (64-deep K blocks).
+  // 128-deep blocks in 2 stages of 96 KB ran slower (8192^3: 1625 against 1824 TFLOP/s).
+  using P512 = tc::TcConfig<KIND, 512, 64, 4, C, true, true, true>;
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -147,18 +157,20 @@ cudaError_t launch_half(int64_t M, int64_t N, int64_t K, const uint16_t* A, cons
   if (N % 8 == 0 && aligned16(B)) {
     // Weights: measured time of one persistent round per unit of tile area, relative to the
     // 256-wide pair (4096^3: 18.5 us per round of 256 x 128 pair tiles, 26.8 of 128 x 192
-    // single-SM tiles, 26.8 of 256 x 256 pair tiles).
-    const int widths[3] = {128, 192, 256};
-    const double weight[3] = {1.38, 1.33, 1.0};
-    int best = pick_width(M, N, sms, widths, weight, 3);
+    // single-SM tiles, 26.8 of 256 x 256 pair tiles, 51.5 of 256 x 512 pair tiles).
+    const int widths[4] = {128, 192, 256, 512};
+    const double weight[4] = {1.38, 1.33, 1.0, 0.96};
+    // Pairs need two tile rows; 192 columns are three boxes and cannot be split in two.
+    const int n_widths = (M > 128 && K <= T2S_WIDE_MAX_K) ? 4 : 3;
+    int best = pick_width(M, N, sms, widths, weight, n_widths);
 #ifdef T2S_HALF_FORCE_WIDTH
     best = T2S_HALF_FORCE_WIDTH;
 #endif
-    // Pairs need two tile rows; 192 columns are three boxes and cannot be split in two.
     if (M > 128) {
       switch (best) {
         case 1: return tc::run_tc<typename Cf::M192>(p, a, nullptr, B, nullptr, lda, N, Kp);
         case 2: return tc::run_tc<typename Cf::P256>(p, a, nullptr, B, nullptr, lda, N, Kp);
+        case 3: return tc::run_tc<typename Cf::P512>(p, a, nullptr, B, nullptr, lda, N, Kp);
         default: return tc::run_tc<typename Cf::P128>(p, a, nullptr, B, nullptr, lda, N, Kp);
       }
     }

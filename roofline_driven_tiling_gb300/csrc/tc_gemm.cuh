@@ -180,25 +180,35 @@ enum TcKind : int { kTf32x3 = 0, kBf16 = 1, kF16 = 2 };
 // tcgen05 .cta_group::2 MMAs (issued by rank 0): each CTA stages its 128 rows of A and half of
 // B's columns, and accumulates its 128 rows in its own TMEM. Each SM thus receives half of
 // the B tile instead of all of it.
+//
+// WIDE (CTA pairs with B read in place only): the tile is twice the widest MMA, BN = 512; each
+// k step issues two N = 256 MMAs into the two halves of one 512-column TMEM accumulator, so an
+// SM stages 128 rows of A and 256 columns of B for 128 x 512 outputs -- a quarter fewer operand
+// bytes per FLOP than 256-wide pair tiles. TMEM then holds a single accumulator: the tensor
+// core sums all of K (no K chunks), and the epilogue streams it from TMEM to C.
 template <int KIND_, int BN_, int BK_, int STAGES_, int CHUNK_K_, bool B_MN_ = false,
-          bool PAIR_ = false>
+          bool PAIR_ = false, bool WIDE_ = false>
 struct TcConfig {
   static constexpr int KIND = KIND_;
   static constexpr bool B_MN = B_MN_;
   static constexpr bool PAIR = PAIR_;
+  static constexpr bool WIDE = WIDE_;
+  static constexpr int NH = WIDE ? 2 : 1;  // MMAs per k step, along N
+  static constexpr int MMA_N = BN_ / NH;
+  static_assert(!WIDE || (PAIR_ && B_MN_), "wide tiles are CTA-pair tiles with B in place");
   static constexpr int BM = 128, BN = BN_, BK = BK_, STAGES = STAGES_;
   static constexpr int ELEM = KIND == kTf32x3 ? 4 : 2;    // bytes per operand element
   static constexpr int MMA_K = KIND == kTf32x3 ? 8 : 16;  // K of one instruction (32 bytes)
   static constexpr int PLANES = KIND == kTf32x3 ? 2 : 1;  // smem boxes per operand per stage
-  static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "UMMA N for M = 128");
+  static_assert(MMA_N % 16 == 0 && MMA_N >= 32 && MMA_N <= 256, "UMMA N for M = 128");
   // K-major A rows are staged in swizzle atoms of up to 128 bytes: a deeper K block is several
   // atom-wide TMA boxes side by side (16-bit operands with B read in place only).
   static_assert(BK * ELEM == 64 || BK * ELEM == 128 || (BK * ELEM == 256 && B_MN_),
                 "64- or 128-byte swizzled K-major rows, or two 128-byte atoms");
   // K values accumulated inside the tensor core before the partial sum is added, with
   // round-to-nearest, into the FP32 sums the epilogue warps keep in registers.
-  static constexpr int CHUNK_KB = CHUNK_K_ / BK;
-  static_assert(CHUNK_K_ % BK == 0 && CHUNK_KB >= 1, "chunk of whole K blocks");
+  static constexpr int CHUNK_KB = WIDE ? (1 << 28) : CHUNK_K_ / BK;
+  static_assert(CHUNK_K_ % BK == 0 && CHUNK_K_ / BK >= 1, "chunk of whole K blocks");
   static constexpr int ROW_BYTES = BK * ELEM;
   static constexpr int ATOM_BYTES = ROW_BYTES > 128 ? 128 : ROW_BYTES;  // swizzle row width
   static constexpr int ATOM_COLS = ATOM_BYTES / ELEM;                   // K values per atom row
@@ -220,16 +230,20 @@ struct TcConfig {
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
   // Epilogue: groups of 4 warps (one per TMEM lane quarter), each group owning an equal
   // share of at most 128 of the tile's columns.
-  static constexpr int EPI_GROUPS = (BN + 127) / 128;
+  static constexpr int EPI_GROUPS = WIDE ? 2 : (BN + 127) / 128;
   static constexpr int EPI_WARPS = 4 * EPI_GROUPS;
   static constexpr int EPI_COLS = BN / EPI_GROUPS;
   static_assert(BN % EPI_GROUPS == 0 && EPI_COLS % 16 == 0, "epilogue reads 16 columns at a time");
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   // 10 warps leave 3 warps on some SM sub-partitions: keep them within its registers.
   static constexpr int MAX_REGS = THREADS > 256 ? 168 : 255;
-  // Two accumulators of BN FP32 columns each (double buffer), a power of two >= 32.
-  static constexpr uint32_t ACC_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
-  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
+  // Two accumulators of BN FP32 columns each (double buffer), a power of two >= 32; WIDE: one
+  // of 512.
+  static constexpr uint32_t ACC_COLS =
+      WIDE ? 512 : BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+  static constexpr int NBUF = WIDE ? 1 : 2;
+  static constexpr uint32_t TMEM_COLS = NBUF * ACC_COLS;
+  static constexpr int B_BOXES_HALF = B_BOXES_CTA / NH;  // this CTA's boxes per MMA half
   // Matrix-descriptor swizzle code (bits 61..63): 2 = 128-byte, 4 = 64-byte.
   static constexpr uint64_t LAYOUT = ATOM_BYTES == 128 ? 2 : 4;
   // Stride between 8-row core groups: 8 rows of one atom.
@@ -242,7 +256,7 @@ struct TcConfig {
   // M of one MMA: 128 rows per CTA.
   static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) |
                                     (static_cast<uint32_t>(B_MN ? 1u : 0u) << 16) |
-                                    (static_cast<uint32_t>(BN >> 3) << 17) |
+                                    (static_cast<uint32_t>(MMA_N >> 3) << 17) |
                                     (static_cast<uint32_t>(G * BM >> 4) << 24);
 };
 
@@ -389,10 +403,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
 #pragma unroll
             for (int q = 0; q < Cfg::A_SUBS; ++q)
               tma_load_2d_pair(st + q * Cfg::A_BOX_BYTES, &tmAb, k0 + q * Cfg::ATOM_COLS, m0, bar0);
+            // This CTA's half of each MMA's columns: box j of half h holds columns
+            // h MMA_N + rank MMA_N / 2 + 64 (j % B_BOXES_HALF) .. + 63.
 #pragma unroll
             for (int j = 0; j < Cfg::B_BOXES_CTA; ++j)
               tma_load_2d_pair(st + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &tmBb,
-                               n0 + (Cfg::BN / 2) * rank + 64 * j, k0, bar0);
+                               n0 + (j / Cfg::B_BOXES_HALF) * Cfg::MMA_N +
+                                   (Cfg::MMA_N / 2) * rank + 64 * (j % Cfg::B_BOXES_HALF),
+                               k0, bar0);
             continue;
           }
           mbar_arrive_expect_tx(full(s), Cfg::STAGE_BYTES);
@@ -429,12 +447,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
       bool ok = true;
       for (int u = unit0; ok && u < units; u += unit_step) {
         for (int kb0 = 0; ok && kb0 < nkb; kb0 += Cfg::CHUNK_KB, ++cc) {
-          const int b = static_cast<int>(cc & 1);
+          const int b = static_cast<int>(cc % Cfg::NBUF);
           const uint32_t acc = tmem + static_cast<uint32_t>(b) * Cfg::ACC_COLS;
           // The epilogue must have read this accumulator's previous chunk.
           if (aborted() ||
-              !mbar_wait_bounded(accEmpty + 8u * b, (static_cast<uint32_t>(cc >> 1) & 1u) ^ 1u,
-                                 status)) {
+              !mbar_wait_bounded(accEmpty + 8u * b,
+                                 (static_cast<uint32_t>(cc / Cfg::NBUF) & 1u) ^ 1u, status)) {
             set_abort();
             ok = false;
             break;
@@ -468,6 +486,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
                 mma_issue<Cfg::KIND, Cfg::G>(acc, a_small, b_big, Cfg::IDESC, acc_in);
                 mma_issue<Cfg::KIND, Cfg::G>(acc, a_big, b_small, Cfg::IDESC, 1u);
                 mma_issue<Cfg::KIND, Cfg::G>(acc, a_big, b_big, Cfg::IDESC, 1u);
+              } else if constexpr (Cfg::WIDE) {
+                // Two MMAs, one per half of the tile's columns (TMEM columns h MMA_N ..).
+#pragma unroll
+                for (int h = 0; h < Cfg::NH; ++h)
+                  mma_issue<Cfg::KIND, Cfg::G>(
+                      acc + static_cast<uint32_t>(h * Cfg::MMA_N), a_big,
+                      smem_desc_mn<Cfg>(st + Cfg::A_BYTES + h * Cfg::B_BOXES_HALF * Cfg::B_BOX_BYTES +
+                                        k * Cfg::MMA_K * 128),
+                      Cfg::IDESC, acc_in);
               } else {
                 mma_issue<Cfg::KIND, Cfg::G>(acc, a_big, b_big, Cfg::IDESC, acc_in);
               }
@@ -504,13 +531,56 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
     for (int u = unit0; ok && u < units; u += unit_step) {
       int m0, n0;
       origin(u, m0, n0);
+      if constexpr (Cfg::WIDE) {
+        // The single accumulator holds the tile's sums over all of K: stream it to C.
+        const bool done = !aborted() &&
+                          mbar_wait_bounded(accFull, static_cast<uint32_t>(cc) & 1u, status);
+        ++cc;
+        if (!__all_sync(0xffffffffu, done)) {
+          if (lane == 0) set_abort();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                               static_cast<uint32_t>(col_base);
+        const int row = m0 + 32 * q + lane;
+        float* crow = C + static_cast<int64_t>(row < M ? row : 0) * N;
+        const int col0 = n0 + col_base;
+#pragma unroll 2
+        for (int c = 0; c < Cfg::EPI_COLS; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(tbase + static_cast<uint32_t>(c), r);  // whole warp
+          if (row < M) {
+#pragma unroll
+            for (int v = 0; v < 16; v += 4) {
+              const int col = col0 + c + v;
+              if (vec_store && col + 4 <= N) {
+                *reinterpret_cast<float4*>(crow + col) =
+                    make_float4(__uint_as_float(r[v]), __uint_as_float(r[v + 1]),
+                                __uint_as_float(r[v + 2]), __uint_as_float(r[v + 3]));
+              } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  if (col + i < N) crow[col + i] = __uint_as_float(r[v + i]);
+              }
+            }
+          }
+        }
+        // All of this warp's TMEM reads are complete (tcgen05.ld waited).
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(map_to_rank(accEmpty, 0));  // rank 0 issues the MMAs
+        continue;
+      } else {
       float sum[Cfg::EPI_COLS];
 #pragma unroll
       for (int c = 0; c < Cfg::EPI_COLS; ++c) sum[c] = 0.0f;
       for (int kb0 = 0; kb0 < nkb; kb0 += Cfg::CHUNK_KB, ++cc) {
-        const int b = static_cast<int>(cc & 1);
+        const int b = static_cast<int>(cc % Cfg::NBUF);
         const bool done = !aborted() &&
-                          mbar_wait_bounded(accFull + 8u * b, static_cast<uint32_t>(cc >> 1) & 1u, status);
+                          mbar_wait_bounded(accFull + 8u * b,
+                                            static_cast<uint32_t>(cc / Cfg::NBUF) & 1u, status);
         if (!__all_sync(0xffffffffu, done)) {
           if (lane == 0) set_abort();
           ok = false;
@@ -554,6 +624,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
               if (col0 + c + i < N) crow[col0 + c + i] = sum[c + i];
           }
         }
+      }
       }
     }
   }
