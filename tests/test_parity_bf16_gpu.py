@@ -181,6 +181,39 @@ def test_bf16_large_sampled(shape):
     assert float(np.max(np.abs(C[rows, cols] - ref))) <= tolerance(Ab, Bb)
 
 
+def edge_positions(M, N, rng):
+    """Every element of the last 200 rows and of the last 520 columns (ragged 256 x 512 pair
+    tiles at the bottom and right edges), the first row and column, and random positions."""
+    rr, cc = np.meshgrid(np.arange(M - 200, M), np.arange(N), indexing="ij")
+    r2, c2 = np.meshgrid(np.arange(M), np.arange(N - 520, N), indexing="ij")
+    rows = [rr.ravel(), r2.ravel(), np.zeros(N, np.int64), np.arange(M), rng.integers(0, M, 4096)]
+    cols = [cc.ravel(), c2.ravel(), np.arange(N), np.zeros(M, np.int64), rng.integers(0, N, 4096)]
+    return np.concatenate(rows), np.concatenate(cols)
+
+
+@pytest.mark.parametrize("kind", ["integer", "uniform"])
+def test_bf16_wide_tiles_ragged_edges(kind):
+    """2500 x 2000 x 3000 runs 256 x 512 pair tiles (80 of them) with partial tiles at the
+    bottom (2500 = 9 x 256 + 196) and the right (2000 = 3 x 512 + 464) and a partial last
+    k block (K = 3000): integer operands must give the definition's bits, uniform ones stay
+    within the tolerance."""
+    M, N, K = 2500, 2000, 3000
+    if kind == "integer":
+        A, B = inputs.integer_pattern(M, N, K)
+        Ab, Bb = inputs.to_bf16_bits(A), inputs.to_bf16_bits(B)
+    else:
+        Ab, Bb = inputs.uniform_bf16(M, K, 1007), inputs.uniform_bf16(K, N, 2007)
+    C = binding.gemm_bf16(bf16_tensor(Ab), bf16_tensor(Bb))
+    assert binding.device_status() == binding.T2S_OK
+    C = C.cpu().numpy()
+    rows, cols = edge_positions(M, N, np.random.default_rng(9))
+    ref = oracle.gemm_bf16_at(Ab, Bb, rows, cols)
+    if kind == "integer":
+        assert bits_equal(C[rows, cols], ref)
+    else:
+        assert float(np.max(np.abs(C[rows, cols] - ref))) <= tolerance(Ab, Bb)
+
+
 def test_bf16_nan_and_inf_propagate():
     M, N, K = 130, 140, 96
     A = inputs.dyadic(M, K, seed=41, denom=4, span=8)
