@@ -157,9 +157,9 @@ cudaError_t launch_half(int64_t M, int64_t N, int64_t K, const uint16_t* A, cons
   if (N % 8 == 0 && aligned16(B)) {
     // Weights: measured time of one persistent round per unit of tile area, relative to the
     // 256-wide pair (4096^3: 18.5 us per round of 256 x 128 pair tiles, 26.8 of 128 x 192
-    // single-SM tiles, 26.8 of 256 x 256 pair tiles, 51.5 of 256 x 512 pair tiles).
+    // single-SM tiles, 26.8 of 256 x 256 pair tiles, 45.4 of 256 x 512 pair tiles).
     const int widths[4] = {128, 192, 256, 512};
-    const double weight[4] = {1.38, 1.33, 1.0, 0.96};
+    const double weight[4] = {1.38, 1.33, 1.0, 0.85};
     // Pairs need two tile rows; 192 columns are three boxes and cannot be split in two.
     const int n_widths = (M > 128 && K <= T2S_WIDE_MAX_K) ? 4 : 3;
     int best = pick_width(M, N, sms, widths, weight, n_widths);

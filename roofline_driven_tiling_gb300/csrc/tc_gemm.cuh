@@ -153,6 +153,34 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Epilogue TMA stores: shared-memory writes made visible to the tensor-memory-access unit,
+// a 2-D box store from shared memory, and waits on the bulk groups this thread committed.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::
+                   "l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The source shared memory of every committed store has been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every committed store has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // 32 consecutive 32-bit TMEM columns of the warp's 32 lanes: thread t gets lane base + t.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -227,7 +255,11 @@ struct TcConfig {
   static constexpr int B_BYTES = BN / G * ROW_BYTES;  // this CTA's share of the B tile
   static constexpr int STAGE_BYTES = PLANES * (A_BYTES + B_BYTES);
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atom alignment");
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  // WIDE: a 4 KB staging box per epilogue warp (32 rows x 32 FP32 columns, 128-byte swizzle)
+  // for TMA stores of C, after a 1 KB barrier area.
+  static constexpr int STAGING_BYTES = WIDE ? 8 * 4096 : 0;
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + 1024 + (WIDE ? 1024 + STAGING_BYTES : 256);
   // Epilogue: groups of 4 warps (one per TMEM lane quarter), each group owning an equal
   // share of at most 128 of the tile's columns.
   static constexpr int EPI_GROUPS = WIDE ? 2 : (BN + 127) / 128;
@@ -311,8 +343,9 @@ template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmAb, const __grid_constant__ CUtensorMap tmAs,
                    const __grid_constant__ CUtensorMap tmBb, const __grid_constant__ CUtensorMap tmBs,
+                   const __grid_constant__ CUtensorMap tmC,
                   float* __restrict__ C, int M, int N, int nkb, int tiles_m, int tiles_n,
-                  unsigned* status, int vec_store) {
+                  unsigned* status, int vec_store, int tma_c) {
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -324,6 +357,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
   const uint32_t mmaDone = accEmpty + 16u;
   const uint32_t sSlot = mmaDone + 8u;              // TMEM address written by tcgen05.alloc
   const uint32_t sAbort = sSlot + 4u;
+  // WIDE: the epilogue warps' TMA-store staging boxes, 1024-byte aligned after the barriers.
+  const uint32_t staging = sBar + 1024u;
   auto stage = [&](int s) { return base + static_cast<uint32_t>(s) * Cfg::STAGE_BYTES; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -544,6 +579,31 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
         tc_fence_after();
         const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) +
                                static_cast<uint32_t>(col_base);
+        if (tma_c) {
+          // 32 x 32 boxes through this warp's staging buffer: row `lane` in 128-byte-swizzled
+          // order (16-byte chunk k of row r at chunk k ^ (r % 8), conflict-free per 8 lanes),
+          // then one TMA store per box; the TMA unit clips what lies outside C.
+          const uint32_t stg = staging + static_cast<uint32_t>(e) * 4096u;
+          for (int c = 0; c < Cfg::EPI_COLS; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tbase + static_cast<uint32_t>(c), r);
+            if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              st_shared_v4(stg + static_cast<uint32_t>(lane) * 128u +
+                               (static_cast<uint32_t>(k ^ (lane & 7)) << 4),
+                           r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int bx = n0 + col_base + c, by = m0 + 32 * q;
+            if (lane == 0 && bx < N && by < M) tma_store_2d(&tmC, stg, bx, by);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(map_to_rank(accEmpty, 0));
+          continue;
+        }
         const int row = m0 + 32 * q + lane;
         float* crow = C + static_cast<int64_t>(row < M ? row : 0) * N;
         const int col0 = n0 + col_base;
@@ -627,6 +687,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
       }
       }
     }
+    // Stores in flight read this CTA's shared memory: let them finish before it is released.
+    if (Cfg::WIDE && tma_c && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -671,6 +733,16 @@ cudaError_t run_tc(const Problem& p, const void* a0, const void* a1, const void*
     if ((e = enc(&tAs, a1, lda, p.M, Cfg::BM)) != cudaSuccess) return e;
     if ((e = enc(&tBs, b1, ldb, p.N, Cfg::BN)) != cudaSuccess) return e;
   }
+  // C as a TMA store target (wide tiles): row stride a multiple of 16 bytes, 16-byte aligned.
+  CUtensorMap tC;
+  memset(&tC, 0, sizeof(tC));
+  int tma_c = 0;
+  if (Cfg::WIDE && p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) {
+    if ((e = encode_tmap_f32_2d(&tC, p.C, p.N, p.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        cudaSuccess)
+      return e;
+    tma_c = 1;
+  }
   auto kern = tc_gemm_kernel<Cfg>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Cfg::SMEM_BYTES)) != cudaSuccess)
@@ -708,12 +780,13 @@ cudaError_t run_tc(const Problem& p, const void* a0, const void* a1, const void*
     if (resident < 1) return cudaErrorInvalidConfiguration;
     const int64_t clusters = units < resident ? units : resident;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-    return cudaLaunchKernelEx(&cfg, kern, tAb, tAs, tBb, tBs, p.C, M32, N32, nkb, tm, tn,
-                              p.status, vec_store);
+    return cudaLaunchKernelEx(&cfg, kern, tAb, tAs, tBb, tBs, tC, p.C, M32, N32, nkb, tm, tn,
+                              p.status, vec_store, tma_c);
   } else {
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(tAb, tAs, tBb, tBs, p.C, M32, N32,
-                                                            nkb, tm, tn, p.status, vec_store);
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(tAb, tAs, tBb, tBs, tC, p.C, M32,
+                                                            N32, nkb, tm, tn, p.status, vec_store,
+                                                            tma_c);
     return cudaGetLastError();
   }
 }
