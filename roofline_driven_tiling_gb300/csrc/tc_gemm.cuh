@@ -176,6 +176,10 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// ... of all but the most recent one.
+__device__ __forceinline__ void bulk_wait_read_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Every committed store has completed.
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -255,11 +259,6 @@ struct TcConfig {
   static constexpr int B_BYTES = BN / G * ROW_BYTES;  // this CTA's share of the B tile
   static constexpr int STAGE_BYTES = PLANES * (A_BYTES + B_BYTES);
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atom alignment");
-  // WIDE: a 4 KB staging box per epilogue warp (32 rows x 32 FP32 columns, 128-byte swizzle)
-  // for TMA stores of C, after a 1 KB barrier area.
-  static constexpr int STAGING_BYTES = WIDE ? 8 * 4096 : 0;
-  static constexpr int SMEM_BYTES =
-      STAGES * STAGE_BYTES + 1024 + (WIDE ? 1024 + STAGING_BYTES : 256);
   // Epilogue: groups of 4 warps (one per TMEM lane quarter), each group owning an equal
   // share of at most 128 of the tile's columns.
   static constexpr int EPI_GROUPS = WIDE ? 2 : (BN + 127) / 128;
@@ -267,6 +266,12 @@ struct TcConfig {
   static constexpr int EPI_COLS = BN / EPI_GROUPS;
   static_assert(BN % EPI_GROUPS == 0 && EPI_COLS % 16 == 0, "epilogue reads 16 columns at a time");
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  // 4 KB of staging per epilogue warp for TMA stores of C, after a 1 KB barrier area: one box
+  // of 32 rows x 32 FP32 columns (128-byte swizzle) for WIDE tiles, two boxes of 32 rows x 16
+  // columns (64-byte swizzle, double-buffered) otherwise.
+  static constexpr int STAGING_BYTES = EPI_WARPS * 4096;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024 + STAGING_BYTES;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
   // 10 warps leave 3 warps on some SM sub-partitions: keep them within its registers.
   static constexpr int MAX_REGS = THREADS > 256 ? 168 : 255;
   // Two accumulators of BN FP32 columns each (double buffer), a power of two >= 32; WIDE: one
@@ -562,6 +567,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
     const int q = warp & 3;                        // TMEM lanes 32q .. 32q + 31 (rows)
     const int col_base = (e >> 2) * Cfg::EPI_COLS;  // this warp's columns of the tile
     int64_t cc = 0;
+    uint32_t n_boxes = 0;  // boxes this warp has stored from its staging buffer
     bool ok = true;
     for (int u = unit0; ok && u < units; u += unit_step) {
       int m0, n0;
@@ -586,7 +592,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
           const uint32_t stg = staging + static_cast<uint32_t>(e) * 4096u;
           for (int c = 0; c < Cfg::EPI_COLS; c += 32) {
             uint32_t r[32];
-            tmem_ld32(tbase + static_cast<uint32_t>(c), r);
+            tmem_ld32(tbase + static_cast<uint32_t>(c), r);  // whole warp
+            const int bx = n0 + col_base + c, by = m0 + 32 * q;  // the same for the whole warp
+            if (bx >= N || by >= M) continue;
             if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
             __syncwarp();
 #pragma unroll
@@ -596,8 +604,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
                            r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
             fence_proxy_async_smem();
             __syncwarp();
-            const int bx = n0 + col_base + c, by = m0 + 32 * q;
-            if (lane == 0 && bx < N && by < M) tma_store_2d(&tmC, stg, bx, by);
+            if (lane == 0) tma_store_2d(&tmC, stg, bx, by);
           }
           tc_fence_before();
           __syncwarp();
@@ -669,6 +676,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
         }
       }
       if (!ok) break;
+      if (tma_c) {
+        // 32 x 16 boxes through the two 2 KB halves of this warp's staging buffer, taken in
+        // turn by the boxes it stores (64-byte swizzle: 16-byte chunk k of row r at chunk
+        // k ^ ((r / 2) % 4), conflict-free per 8 lanes), one TMA store each. Boxes wholly
+        // outside C are skipped; the TMA unit clips the others at its edges.
+#pragma unroll
+        for (int c = 0; c < Cfg::EPI_COLS; c += 16) {
+          const int bx = n0 + col_base + c, by = m0 + 32 * q;  // the same for the whole warp
+          if (bx >= N || by >= M) continue;
+          const uint32_t stg = staging + static_cast<uint32_t>(e) * 4096u +
+                               static_cast<uint32_t>(n_boxes & 1) * 2048u;
+          ++n_boxes;
+          // The box stored from this half two stores ago has been read out of it.
+          if (lane == 0) bulk_wait_read_but_one();
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            st_shared_v4(stg + static_cast<uint32_t>(lane) * 64u +
+                             (static_cast<uint32_t>(k ^ ((lane >> 1) & 3)) << 4),
+                         __float_as_uint(sum[c + 4 * k]), __float_as_uint(sum[c + 4 * k + 1]),
+                         __float_as_uint(sum[c + 4 * k + 2]), __float_as_uint(sum[c + 4 * k + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tma_store_2d(&tmC, stg, bx, by);
+        }
+        continue;
+      }
       const int row = m0 + 32 * q + lane;
       if (row < M) {
         float* crow = C + static_cast<int64_t>(row) * N;
@@ -688,7 +722,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
       }
     }
     // Stores in flight read this CTA's shared memory: let them finish before it is released.
-    if (Cfg::WIDE && tma_c && lane == 0) bulk_wait_all();
+    if (tma_c && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -733,13 +767,14 @@ cudaError_t run_tc(const Problem& p, const void* a0, const void* a1, const void*
     if ((e = enc(&tAs, a1, lda, p.M, Cfg::BM)) != cudaSuccess) return e;
     if ((e = enc(&tBs, b1, ldb, p.N, Cfg::BN)) != cudaSuccess) return e;
   }
-  // C as a TMA store target (wide tiles): row stride a multiple of 16 bytes, 16-byte aligned.
+  // C as a TMA store target: row stride a multiple of 16 bytes, 16-byte aligned.
   CUtensorMap tC;
   memset(&tC, 0, sizeof(tC));
   int tma_c = 0;
-  if (Cfg::WIDE && p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) {
-    if ((e = encode_tmap_f32_2d(&tC, p.C, p.N, p.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)) !=
-        cudaSuccess)
+  if (p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) {
+    if ((e = encode_tmap_f32_2d(&tC, p.C, p.N, p.M, Cfg::WIDE ? 32 : 16, 32,
+                                Cfg::WIDE ? CU_TENSOR_MAP_SWIZZLE_128B
+                                          : CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess)
       return e;
     tma_c = 1;
   }
