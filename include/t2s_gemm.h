@@ -209,6 +209,9 @@ int t2s_gemm_f32_streamk(int64_t M, int64_t N, int64_t K, const float *A, const 
  * FP32 definition (the tensor core fixes its own summation order); it meets
  * max |C - C_fp32| <= 1e-6 * K * max|a| * max|b|, and it is exact wherever
  * every FP32 product and partial sum is exact (for example small integers).
+ * A NaN operand gives NaN where the definition does; an infinite operand may give
+ * NaN where the definition gives an infinity (a correction term multiplies it by
+ * the zero small part of an operand that TF32 represents exactly).
  *
  * `workspace` is a DEVICE buffer, 256-byte aligned, of at least
  * t2s_gemm_f32_tf32x3_workspace_size(M, N, K) bytes, owned by the caller,

@@ -62,7 +62,9 @@ __device__ __forceinline__ float tf32_round(float x) {
 }
 
 __device__ __forceinline__ void split(float x, float& big, float& small) {
-  big = tf32_round(x);
+  // The tensor core reads only the top 19 bits of an FP32 operand: a NaN whose payload lies
+  // in the 13 low bits alone would read as an infinity, so NaNs become the quiet NaN.
+  big = isnan(x) ? __uint_as_float(0x7fc00000u) : tf32_round(x);
   // x - big is exact; for non-finite x the correction term is dropped.
   small = isfinite(x) ? tf32_round(__fsub_rn(x, big)) : 0.0f;
 }

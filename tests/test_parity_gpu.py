@@ -290,6 +290,31 @@ def test_tf32x3_misaligned_inputs(shift):
     assert float(np.max(np.abs(C - oracle.sgemm(A, B, oracle.MUL_ADD)))) <= tolerance(A, B)
 
 
+@pytest.mark.parametrize("shift", [0, 1], ids=["aligned", "misaligned"])
+def test_tf32x3_special_values(shift):
+    """NaNs (quiet, and one whose payload sits only in the 13 low mantissa bits that TF32
+    drops), infinities, signed zeros and subnormal operands. A NaN in row i of A makes row i
+    of C NaN, as in the definition; an infinity makes its row non-finite (it stays infinite,
+    or a correction term multiplies it by the zero small part of an exactly representable
+    operand); every other element is finite and within the tolerance."""
+    M, N, K = 131, 136, 96
+    A, B = inputs.uniform_pair(M, N, K, 17)
+    tiny = np.float32(1.4e-45)
+    A[10, 3], A[20, 7], B[5, 9], B[6, 11] = np.float32(-0.0), tiny, np.float32(1e-40), -tiny
+    A[3, 5] = np.frombuffer(np.uint32(0x7F800001).tobytes(), dtype=np.float32)[0]  # NaN
+    A[40, 50] = np.float32(np.nan)
+    A[60, 2] = np.float32(np.inf)
+    A[70, 80] = np.float32(-np.inf)
+    C = run("tf32x3", A, B, shift=shift)
+    want = oracle.sgemm(A, B, oracle.FMA)
+    assert np.all(np.isnan(C[[3, 40]])) and np.all(np.isnan(want[[3, 40]]))
+    assert not np.any(np.isfinite(C[[60, 70]]))
+    rest = np.ones(M, bool)
+    rest[[3, 40, 60, 70]] = False
+    assert np.all(np.isfinite(C[rest]))
+    assert float(np.max(np.abs(C[rest] - want[rest]))) <= tolerance(A[rest], B)
+
+
 def test_tf32x3_workspace_checks():
     M, N, K = 64, 64, 64
     dA = torch.zeros((M, K), device="cuda")
