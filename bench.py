@@ -40,6 +40,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FFMA_PROFILE = os.path.join(ROOT, "profiles", "sgemm_ffma_4096.md")
 TF32X3_PROFILE = os.path.join(ROOT, "profiles", "gemm_tf32x3_4096.md")
 BF16_PROFILE = os.path.join(ROOT, "profiles", "gemm_bf16_4096.md")
+F16_PROFILE = os.path.join(ROOT, "profiles", "gemm_f16_4096.md")
 F64_PROFILE = os.path.join(ROOT, "profiles", "dgemm_f64_2048.md")
 # Codes of t2s_gemm_f32_plan.
 PLAN_HUGE_TAIL = 5
@@ -444,7 +445,8 @@ def extra_half(lib, M, N, K, stream, flush, args, dev, fmt="bf16"):
             "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peak,
                          "frac": flops / t / 1e12 / peak, "unit": UNIT,
                          "peak_basis": "measured cuBLAS bf16 burst (FP16 has the same nominal rate)",
-                         "traffic": profile_traffic(BF16_PROFILE, "bf16") if fmt == "bf16" else None}}
+                         "traffic": profile_traffic(BF16_PROFILE if fmt == "bf16" else F16_PROFILE,
+                                                    "bf16")}}
 
 
 def extra_f64(lib, stream, flush, args, dev):
