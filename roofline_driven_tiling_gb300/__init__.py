@@ -5,7 +5,7 @@ The compute path is the CUDA library ``libt2s_gemm.so`` (C ABI in
 performance model used for reporting and ``inputs`` the seeded synthetic inputs.
 """
 from . import binding, inputs, roofline  # noqa: F401
-from .binding import gemm, gemm_bf16, gemm_f16, gemm_f64, device_status  # noqa: F401
+from .binding import gemm, gemm_bf16, gemm_f16, gemm_f64, device_status, plan  # noqa: F401
 
 __all__ = ["binding", "inputs", "roofline", "gemm", "gemm_bf16", "gemm_f16", "gemm_f64",
-           "device_status"]
+           "device_status", "plan"]

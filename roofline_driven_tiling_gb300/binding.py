@@ -315,6 +315,31 @@ def gemm_f16(A, B, out=None, workspace=None, stream=None):
     return _gemm_16bit(A, B, out, workspace, stream, torch.float16, "t2s_gemm_f16_f32")
 
 
+def plan(M: int, N: int, K: int, sms: int = None) -> str:
+    """The CTA tiling ``gemm`` takes for an M x N x K product, by name (host-only; `sms`
+    defaults to the current device's multiprocessor count)."""
+    if sms is None:
+        import torch
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    code = lib().t2s_gemm_f32_plan(M, N, K, sms)
+    if code < 0:
+        raise ValueError("invalid shape or SM count")
+    return PLAN_NAMES[code]
+
+
+PLAN_NAMES = {
+    0: "128x128 tiles, unrolled k loop",
+    1: "128x128 tiles, compact k loop",
+    2: "128x64 tiles",
+    3: "64x64 tiles",
+    4: "256x128 tiles",
+    5: "256x128 tiles in whole rounds, the rest as 64x64 tiles",
+    6: "128x128 tiles of 8 warps",
+    7: "128x64 tiles of 8 warps",
+    8: "128x128 tiles on a persistent grid",
+}
+
+
 def device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
     import torch

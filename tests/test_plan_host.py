@@ -77,3 +77,11 @@ def test_plan_depends_on_sm_count():
                                   ((1 << 30) + 1, 4, 4, 152), (4, 4, 4, 0), (4, 4, 4, -3)])
 def test_plan_rejects_bad_arguments(args):
     assert binding.t2s_gemm_f32_plan(*args) == -1
+
+
+def test_plan_names():
+    assert binding.plan(4096, 4096, 4096, 152) == "256x128 tiles in whole rounds, the rest as 64x64 tiles"
+    assert binding.plan(1024, 1024, 1024, 152) == "128x64 tiles of 8 warps"
+    assert set(binding.PLAN_NAMES) == set(range(9))
+    with pytest.raises(ValueError):
+        binding.plan(-1, 4, 4, 152)
