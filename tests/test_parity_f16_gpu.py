@@ -79,6 +79,29 @@ def test_f16_partial_last_round_exact():
     assert h.bits_equal(C[rows, cols], oracle.gemm_f16_at(Ab, Bb, rows, cols))
 
 
+@pytest.mark.parametrize("kind", ["integer", "uniform"])
+def test_f16_wide_tiles_ragged_edges(kind):
+    """The BF16 ragged wide-tile case for binary16: 2500 x 2000 x 3000 on 256 x 512 pair
+    tiles, partial tiles at the bottom and right edges and a partial last k block."""
+    M, N, K = 2500, 2000, 3000
+    if kind == "integer":
+        A, B = inputs.integer_pattern(M, N, K)
+        Ab, Bb = inputs.to_f16_bits(A), inputs.to_f16_bits(B)
+    else:
+        Ab, Bb = inputs.uniform_f16(M, K, 1008), inputs.uniform_f16(K, N, 2008)
+    dA = torch.from_numpy(Ab.view(np.int16)).cuda().view(torch.float16)
+    dB = torch.from_numpy(Bb.view(np.int16)).cuda().view(torch.float16)
+    C = binding.gemm_f16(dA, dB)
+    assert binding.device_status() == binding.T2S_OK
+    C = C.cpu().numpy()
+    rows, cols = h.edge_positions(M, N, np.random.default_rng(10))
+    ref = oracle.gemm_f16_at(Ab, Bb, rows, cols)
+    if kind == "integer":
+        assert h.bits_equal(C[rows, cols], ref)
+    else:
+        assert float(np.max(np.abs(C[rows, cols] - ref))) <= tolerance(Ab, Bb)
+
+
 def test_f16_dyadic_exact_misaligned():
     A = inputs.dyadic(300, 77, seed=31, denom=256, span=1000)
     B = inputs.dyadic(77, 192, seed=32, denom=16, span=64)
