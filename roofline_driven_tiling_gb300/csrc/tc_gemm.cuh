@@ -1,9 +1,11 @@
-// tc_gemm.cuh -- persistent tcgen05 GEMM core shared by the 3xTF32 and BF16 products.
+// tc_gemm.cuh -- persistent tcgen05 GEMM core shared by the 3xTF32, BF16 and FP16 products.
 //
 // C (FP32, row-major) = A x B with A given as M x K K-major planes and B as N x K K-major
-// planes (B transposed), staged by TMA in 64- or 128-byte swizzled rows, multiplied by
-// tcgen05.mma with TMEM accumulators, and drained by epilogue warps that add each K chunk's
-// partial sums into FP32 registers with round-to-nearest.
+// planes (B transposed) or, for 16-bit operands, as B itself (MN-major), staged by TMA in
+// 64- or 128-byte swizzled rows, multiplied by tcgen05.mma with TMEM accumulators, and
+// drained by epilogue warps that add each K chunk's partial sums into FP32 registers with
+// round-to-nearest (WIDE tiles: one accumulator over all of K) and store C in swizzled
+// shared-memory boxes with TMA.
 #pragma once
 
 #include <cuda.h>
@@ -340,7 +342,8 @@ __device__ __forceinline__ void tile_origin(int t, int tiles_m, int tiles_n, int
 //   warps 2 .. 2 + EPI_WARPS - 1  epilogue: add each chunk's partial sums into FP32
 //           registers with round-to-nearest (the tensor core's own accumulation is not
 //           round-to-nearest, and its error would grow with K), release the accumulator,
-//           and store the sums after the tile's last chunk.
+//           and store the sums after the tile's last chunk (WIDE: copy the one accumulator
+//           out at the end of the tile), through each warp's staging boxes and TMA stores.
 // Barriers: full[s] / empty[s] per ring slot; acc_full[b] (a chunk's MMAs are done) and
 // acc_empty[b] (the epilogue has read it) per accumulator. A fresh barrier counts its
 // "previous" phase (parity 1) as complete, so first uses wait on parity 1 and pass.
