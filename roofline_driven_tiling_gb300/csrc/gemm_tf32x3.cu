@@ -69,21 +69,32 @@ __device__ __forceinline__ void split(float x, float& big, float& small) {
   small = isfinite(x) ? tf32_round(__fsub_rn(x, big)) : 0.0f;
 }
 
-// A (M x K, row-major) -> big, small (M x Kp), zeros for k >= K. Four k per thread, rows
-// along the grid's y (no 64-bit division per element); 16-byte loads when every row starts
-// on a 16-byte boundary (kVec: K % 4 == 0 and A 16-byte aligned).
+// Both splits in one launch, their blocks interleaved (even blocks A, odd blocks B) so that
+// the two run side by side: alone, neither kept HBM busy (about 5.6 and 4.2 TB/s).
+//  * A (M x K, row-major) -> big, small (M x Kp), zeros for k >= K: work items of 256 x 4
+//    consecutive k of one row, one per thread group of four; 16-byte loads when every row
+//    starts on a 16-byte boundary (kVec: K % 4 == 0 and A 16-byte aligned).
+//  * B (K x N, row-major) -> big, small (N x Kp): 32 x 32 tiles transposed through shared
+//    memory, so that both the reads (along n) and the writes (along k) are coalesced.
 template <bool kVec>
-__global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict__ A,
-                                                         float* __restrict__ big,
-                                                         float* __restrict__ small, int64_t M,
-                                                         int64_t K, int64_t Kp) {
-  const int64_t q = Kp / 4;
-  for (int64_t row = blockIdx.y; row < M; row += gridDim.y) {
-    const float* arow = A + row * K;
-    float* brow = big + row * Kp;
-    float* srow = small + row * Kp;
-    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < q;
-         c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+__global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ A,
+                                                    float* __restrict__ a_big,
+                                                    float* __restrict__ a_small,
+                                                    const float* __restrict__ B,
+                                                    float* __restrict__ b_big,
+                                                    float* __restrict__ b_small, int64_t M,
+                                                    int64_t N, int64_t K, int64_t Kp) {
+  __shared__ float tile[32][33];
+  const int64_t part_blocks = gridDim.x / 2;
+  const int64_t id = blockIdx.x / 2;
+  if ((blockIdx.x & 1) == 0) {
+    const int64_t q = Kp / 4;                 // float4 groups per row
+    const int64_t per_row = (q + 255) / 256;  // work items per row
+    for (int64_t it = id; it < M * per_row; it += part_blocks) {
+      const int64_t row = it / per_row;
+      const int64_t c = (it - row * per_row) * 256 + threadIdx.x;
+      if (c >= q) continue;
+      const float* arow = A + row * K;
       const int64_t k = 4 * c;
       float x[4];
       if (kVec && k + 3 < K) {
@@ -99,23 +110,15 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict
       float b[4], s[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) split(x[e], b[e], s[e]);
-      *reinterpret_cast<float4*>(brow + k) = make_float4(b[0], b[1], b[2], b[3]);
-      *reinterpret_cast<float4*>(srow + k) = make_float4(s[0], s[1], s[2], s[3]);
+      *reinterpret_cast<float4*>(a_big + row * Kp + k) = make_float4(b[0], b[1], b[2], b[3]);
+      *reinterpret_cast<float4*>(a_small + row * Kp + k) = make_float4(s[0], s[1], s[2], s[3]);
     }
+    return;
   }
-}
-
-// B (K x N, row-major) -> big, small (N x Kp): transposed in 32 x 32 tiles through shared
-// memory so that both the reads (along n) and the writes (along k) are coalesced.
-__global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ B,
-                                                              float* __restrict__ big,
-                                                              float* __restrict__ small,
-                                                              int64_t K, int64_t N, int64_t Kp) {
-  __shared__ float tile[32][33];
-  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 32;
-  for (int64_t kt = blockIdx.y; kt * 32 < Kp; kt += gridDim.y) {
-    const int64_t k0 = kt * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  const int64_t tiles_n = (N + 31) / 32;
+  for (int64_t t = id; t < tiles_n * (Kp / 32); t += part_blocks) {
+    const int64_t n0 = (t % tiles_n) * 32, k0 = (t / tiles_n) * 32;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t k = k0 + ty + 8 * i, n = n0 + tx;
@@ -128,8 +131,8 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
       if (n < N) {
         float b, s;
         split(tile[tx][ty + 8 * i], b, s);
-        big[n * Kp + k] = b;
-        small[n * Kp + k] = s;
+        b_big[n * Kp + k] = b;
+        b_small[n * Kp + k] = s;
       }
     }
     __syncthreads();
@@ -167,19 +170,17 @@ cudaError_t launch_tf32x3(const Problem& p, void* workspace) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   {
-    const int64_t gx = std::min<int64_t>((Kp / 4 + 255) / 256, 64);
-    const int64_t gy = std::min<int64_t>(p.M, 65535);
-    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+    const int64_t a_items = p.M * ((Kp / 4 + 255) / 256);
+    const int64_t b_items = ((p.N + 31) / 32) * (Kp / 32);
+    const int64_t part = std::min<int64_t>(std::max(a_items, b_items), 1 << 20);
+    const unsigned blocks = static_cast<unsigned>(2 * part);
     const bool vec = p.K % 4 == 0 && (reinterpret_cast<uintptr_t>(p.A) & 15u) == 0;
-    if (vec) split_rows_kernel<true><<<grid, 256, 0, p.stream>>>(p.A, a_big, a_small, p.M, p.K, Kp);
-    else split_rows_kernel<false><<<grid, 256, 0, p.stream>>>(p.A, a_big, a_small, p.M, p.K, Kp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  {
-    const int64_t gy = Kp / 32;
-    const dim3 grid(static_cast<unsigned>((p.N + 31) / 32),
-                    static_cast<unsigned>(gy < 65535 ? gy : 65535));
-    split_transpose_kernel<<<grid, dim3(32, 8), 0, p.stream>>>(p.B, b_big, b_small, p.K, p.N, Kp);
+    if (vec)
+      split_kernel<true><<<blocks, 256, 0, p.stream>>>(p.A, a_big, a_small, p.B, b_big, b_small,
+                                                       p.M, p.N, p.K, Kp);
+    else
+      split_kernel<false><<<blocks, 256, 0, p.stream>>>(p.A, a_big, a_small, p.B, b_big,
+                                                        b_small, p.M, p.N, p.K, Kp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // Persistent CTAs take tiles in rounds of `sms`; the cost of a width is its number of
