@@ -168,9 +168,12 @@ def test_bf16_small_shapes(shape, shift):
 
 @pytest.mark.parametrize("shape", [(4096, 4096, 4096), (8192, 8192, 8192), (16384, 16384, 32),
                                    (8192, 8192, 64), (512, 512, 512), (256, 256, 65536),
-                                   (130, 70, 20000)], ids=lambda s: "x".join(map(str, s)))
+                                   (130, 70, 20000), (4096, 4096, 16384), (4096, 4096, 16448)],
+                         ids=lambda s: "x".join(map(str, s)))
 def test_bf16_large_sampled(shape):
-    """Full-size shapes (the benchmarked 4096^3 among them) on sampled outputs."""
+    """Full-size shapes (the benchmarked 4096^3 among them) on sampled outputs; 4096^2 x 16384
+    is the longest K the 256 x 512 tiles take (all of K summed in TMEM), 16448 the first that
+    goes back to chunked sums."""
     M, N, K = shape
     Ab, Bb = inputs.uniform_bf16(M, K, 1005), inputs.uniform_bf16(K, N, 2005)
     C = binding.gemm_bf16(bf16_tensor(Ab), bf16_tensor(Bb))
