@@ -38,6 +38,7 @@ WORKLOAD = dict(M=4096, N=4096, K=4096, config_no=4)
 L2_FLUSH_BYTES = 256 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FFMA_PROFILE = os.path.join(ROOT, "profiles", "sgemm_ffma_4096.md")
+FFMA_1024_PROFILE = os.path.join(ROOT, "profiles", "sgemm_ffma_1024.md")
 TF32X3_PROFILE = os.path.join(ROOT, "profiles", "gemm_tf32x3_4096.md")
 BF16_PROFILE = os.path.join(ROOT, "profiles", "gemm_bf16_4096.md")
 F16_PROFILE = os.path.join(ROOT, "profiles", "gemm_f16_4096.md")
@@ -47,7 +48,9 @@ PLAN_HUGE_TAIL = 5
 PLAN_NAMES = {0: "128x128x32 tiles", 1: "128x128x32 tiles, compact k loop", 2: "128x64x32 tiles",
               3: "64x64x32 tiles", 4: "256x128x32 tiles",
               5: "256x128x32 tiles in whole rounds over the SMs, the rest as 64x64x32 tiles "
-                 "in a second launch"}
+                 "in a second launch", 6: "128x128x32 tiles of 8 warps",
+              7: "128x64x32 tiles of 8 warps", 8: "128x128x32 tiles on a persistent grid",
+              9: "56x128x32 tiles of 8 warps"}
 
 KERNEL_SOURCES = {
     "ffma": ["sgemm_ffma.cu", "t2s_device.cuh"],
@@ -514,6 +517,9 @@ def extra_1024(lib, dev, stream, flush, args, ws):
         t = sum(times) / len(times) / 1e3
         out[name] = {"ms": t * 1e3, "tflops": rl.gemm_flops(n, n, n) / t / 1e12,
                      "frac_fp32_peak": rl.gemm_flops(n, n, n) / t / 1e12 / rl.fp32_peak_tflops()}
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out["ffma"]["tiling"] = PLAN_NAMES.get(lib.t2s_gemm_f32_plan(n, n, n, sms))
+    out["ffma"]["traffic"] = profile_traffic(FFMA_1024_PROFILE, "ffma")
     return out
 
 

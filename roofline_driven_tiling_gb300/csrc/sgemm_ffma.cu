@@ -195,15 +195,16 @@ template <class Cfg>
 __device__ __forceinline__ void ffma_kblock_pipelined(uint64_t (&acc)[Cfg::TM][Cfg::TN / 2],
                                                       uint32_t a_base, uint32_t b_base,
                                                       uint32_t xr) {
-  // A in pairs of k values (one 8-byte load per row every two steps), B per step; each loaded
-  // one step (A: one pair) ahead into the other register set.
-  float a[2][Cfg::TM][2];
+  // A in groups of AV k values (one load per row every AV steps), B per step; each loaded one
+  // step (A: one group) ahead into the other register set.
+  constexpr int AV = Cfg::AV;
+  float a[2][Cfg::TM][AV];
   uint64_t b[2][Cfg::TN / 2];
-  auto load_a = [&](int k2, int buf) {
-    const uint32_t koff = ((static_cast<uint32_t>(k2 >> 2) ^ xr) << 4) + (k2 & 3) * 4;
+  auto load_a = [&](int kq, int buf) {
+    const uint32_t koff = ((static_cast<uint32_t>(kq >> 2) ^ xr) << 4) + (kq & 3) * 4;
 #pragma unroll
     for (int i = 0; i < Cfg::TM; ++i)
-      lds_vec<2>(a_base + i * Cfg::LM * Cfg::A_ROW_BYTES + koff, a[buf][i]);
+      lds_vec<AV>(a_base + i * Cfg::LM * Cfg::A_ROW_BYTES + koff, a[buf][i]);
   };
   auto load_b = [&](int k, int buf) {
     const uint32_t b_row = b_base + k * (Cfg::BN * 4);
@@ -215,12 +216,12 @@ __device__ __forceinline__ void ffma_kblock_pipelined(uint64_t (&acc)[Cfg::TM][C
   load_b(0, 0);
 #pragma unroll
   for (int k = 0; k < Cfg::BK; ++k) {
-    const int cur = k & 1, abuf = (k >> 1) & 1;
+    const int cur = k & 1, abuf = (k / AV) & 1;
     if (k + 1 < Cfg::BK) load_b(k + 1, cur ^ 1);
-    if ((k & 1) == 0 && k + 2 < Cfg::BK) load_a(k + 2, abuf ^ 1);
+    if (k % AV == 0 && k + AV < Cfg::BK) load_a(k + AV, abuf ^ 1);
     uint64_t ap[Cfg::TM];
 #pragma unroll
-    for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[abuf][i][k & 1]);
+    for (int i = 0; i < Cfg::TM; ++i) ap[i] = pack_dup(a[abuf][i][k % AV]);
 #pragma unroll
     for (int j = 0; j < Cfg::TN / 2; ++j)
 #pragma unroll
@@ -521,6 +522,14 @@ using Tall88 = FfmaConfig<128, 64, 32, 3, 2, 2, 2, 8, 8, 1>;
 // 39.9 with 4 warps of 8 x 8).
 using Big88 = FfmaConfig<128, 128, 32, 3, 2, 4, 2, 8, 8, 1>;
 using Tall84 = FfmaConfig<128, 64, 32, 3, 2, 4, 2, 8, 4, 1>;
+// 56 x 128 tiles of 8 warps (1 x 8 of 56 x 16), 7 x 4 per thread, A read 4 k values at a time:
+// a 1024 x 1024 C is 19 x 8 = 152 of them, one per SM, where 128 x 64 tiles leave 24 SMs idle
+// and give the busiest SM 14 % more work. Per SM both run the FMA pipe about 70 % busy, so the
+// gain is the balance: 1024^3 45.0 TFLOP/s against 41.4, 1024^2 x 4096 50.3 against 45.9,
+// 1000 x 1003 x 997 26.5 against 24.2. (Measured alongside: B read 8 bytes at a time, A 4 k
+// values at a time in the 128 x 64 tile, 4 x 8 per thread in it, 120 x 64 tiles of 12 warps,
+// 4 stages: none faster.)
+using Wide74 = FfmaConfig<56, 128, 32, 3, 1, 8, 4, 7, 4, 1>;
 
 bool tma_ok(const Problem& p) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.A), b = reinterpret_cast<uintptr_t>(p.B);
@@ -550,7 +559,8 @@ enum class FfmaPick {
   kHugeTail = 5,
   kBig88 = 6,
   kTall84 = 7,
-  kPersistent = 8
+  kPersistent = 8,
+  kWide74 = 9
 };
 
 // Picks the configuration whose busiest SM has the least work: ceil(tiles / SMs) tiles of the
@@ -559,14 +569,14 @@ enum class FfmaPick {
 // 1.04 (never ahead of 128 x 64, so not built); 128 x 128 tiles 1.15 from three tiles per SM on,
 // 1.05 at two and 1.03 at one (with the compact k loop; the fully unrolled one pays only from
 // three); 256 x 128 tiles 1.17 (K >= 256); the 8-warp tiles only where they come to at most
-// one per SM: 128 x 128 1.116, 128 x 64 1.091. The 256 x 128 tiles also run as whole rounds
-// followed by the rest of their tiles cut into 64 x 64 ones, which the tail spreads over all
-// SMs: floor(tiles / SMs) rounds plus ceil(8 x rest / SMs) small tiles. Every measured winner
-// of the sweep is the model's pick, up to 1 %, including the non-monotone ones (1024^3 goes to
-// 128 x 64 tiles of 8 warps, 1280^3 to 64 x 64, 1536^3 to 128 x 128 of 8 warps, 1792^3 to
-// 128 x 64, 2048^3 and 3072^3 to 256 x 128, 2560^3, 4096^3 and 6144^3 to 256 x 128 with the
-// 64 x 64 tail). `copies` products of this size share
-// the GPU; they (and K < 256) keep to the one-launch configurations of at most 128 x 128.
+// one per SM: 128 x 128 1.116, 128 x 64 1.091, 56 x 128 1.043. The 256 x 128 tiles also run
+// as whole rounds followed by the rest of their tiles cut into 64 x 64 ones, which the tail
+// spreads over all SMs: floor(tiles / SMs) rounds plus ceil(8 x rest / SMs) small tiles.
+// Every measured winner of the sweep is the model's pick, up to 1 %, including the
+// non-monotone ones (1024^3 goes to 56 x 128 tiles of 8 warps, 1280^3 to 64 x 64, 1536^3 to
+// 128 x 128 of 8 warps, 1792^3 to 128 x 64, 2048^3 and 3072^3 to 256 x 128, 2560^3, 4096^3 and
+// 6144^3 to 256 x 128 with the 64 x 64 tail). `copies` products of this size share the GPU;
+// they (and K < 256) keep to the one-launch configurations of at most 128 x 128.
 FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
   struct Cand {
     FfmaPick pick;
@@ -596,8 +606,10 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
     }
   }
   {
-    const Cand one[2] = {{FfmaPick::kBig88, 128, 128, 1.116}, {FfmaPick::kTall84, 128, 64, 1.091}};
-    for (int i = 0; i < 2; ++i) {
+    const Cand one[3] = {{FfmaPick::kBig88, 128, 128, 1.116},
+                         {FfmaPick::kTall84, 128, 64, 1.091},
+                         {FfmaPick::kWide74, 56, 128, 1.043}};
+    for (int i = 0; i < 3; ++i) {
       const int64_t tiles = ((M + one[i].bm - 1) / one[i].bm) * ((N + one[i].bn - 1) / one[i].bn) *
                             n_copies;
       if (tiles > sms) continue;
@@ -647,6 +659,7 @@ cudaError_t run_pick(FfmaPick pick, const Problem& p, Ts... args) {
     case FfmaPick::kTall88: return run_any<Tall88>(p, args...);
     case FfmaPick::kBig88: return run_any<Big88>(p, args...);
     case FfmaPick::kTall84: return run_any<Tall84>(p, args...);
+    case FfmaPick::kWide74: return run_any<Wide74>(p, args...);
     default: return run_any<Small48>(p, args...);
   }
 }

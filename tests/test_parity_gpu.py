@@ -448,7 +448,8 @@ DISPATCH_SHAPES = {
     "big_short_k": (3072, 3072, 128),      # 576 tiles of 128^2, K < 256
     "persistent_k32": (8192, 4096, 32),    # 2048 tiles of 128^2, one K block (cp.async: 1)
     "tall88_1792": (1792, 1792, 512),      # 392 tiles of 128 x 64: 8 x 8 per thread, pipelined
-    "tall84_1024": (1024, 1024, 512),      # 128 tiles of 128 x 64, 8 warps of 8 x 4
+    "tall84_1152": (1152, 1024, 512),      # 144 tiles of 128 x 64, 8 warps of 8 x 4
+    "wide74_1024": (1024, 1024, 512),      # 152 tiles of 56 x 128, 8 warps of 7 x 4
     "big88_1536": (1536, 1536, 512),       # 144 tiles of 128 x 128, 8 warps of 8 x 8
     "small48_2048": (2048, 2048, 128),     # 1024 tiles of 64 x 64: 4 x 8 per thread, pipelined
     "small48_640": (640, 700, 300),        # 110 tiles of 64 x 64

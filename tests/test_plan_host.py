@@ -9,7 +9,7 @@ import pytest
 
 from roofline_driven_tiling_gb300 import binding
 
-BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL, BIG88, TALL84, PERSISTENT = range(9)
+BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL, BIG88, TALL84, PERSISTENT, WIDE74 = range(10)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -21,7 +21,9 @@ def built():
 # (M, N, K) -> the configuration measured fastest (or within 1 % of it) on GB300.
 MEASURED = {
     (768, 768, 768): SMALL48,
-    (1024, 1024, 1024): TALL84,       # 41.4; 4 warps of 8 x 8 39.9
+    (1024, 1024, 1024): WIDE74,       # 45.0; 128 x 64 tiles of 8 warps 41.4
+    (1024, 1024, 4096): WIDE74,       # 50.3; 128 x 64 tiles of 8 warps 45.9
+    (1000, 1003, 997): WIDE74,        # 26.5; 128 x 64 tiles of 8 warps 24.2
     (1280, 1280, 1280): SMALL48,
     (1536, 1536, 1536): BIG88,        # 55.9; 128 x 64 tiles 52.6
     (1792, 1792, 1792): TALL88,
@@ -60,8 +62,10 @@ def test_plan_tail_only_with_a_whole_round():
 
 
 def test_plan_eight_warp_tiles_only_for_one_round():
-    # 128 tiles of 128 x 64 on 152 SMs: one each, 8 warps.
-    assert binding.t2s_gemm_f32_plan(1024, 1024, 512, 152) == TALL84
+    # 152 tiles of 56 x 128 on 152 SMs: one each, 8 warps (128 x 64 tiles: 128, less even).
+    assert binding.t2s_gemm_f32_plan(1024, 1024, 512, 152) == WIDE74
+    # 1152 rows are 21 tiles of 56: 168 > 152; 9 x 16 = 144 tiles of 128 x 64 fit.
+    assert binding.t2s_gemm_f32_plan(1152, 1024, 512, 152) == TALL84
     # 162 tiles of 128 x 64 would need a second round on some SMs: not the 8-warp tile.
     assert binding.t2s_gemm_f32_plan(1152, 1152, 1152, 152) != TALL84
     assert binding.t2s_gemm_f32_plan(1408, 1408, 1408, 152) == BIG88   # 121 tiles of 128^2
@@ -81,7 +85,8 @@ def test_plan_rejects_bad_arguments(args):
 
 def test_plan_names():
     assert binding.plan(4096, 4096, 4096, 152) == "256x128 tiles in whole rounds, the rest as 64x64 tiles"
-    assert binding.plan(1024, 1024, 1024, 152) == "128x64 tiles of 8 warps"
-    assert set(binding.PLAN_NAMES) == set(range(9))
+    assert binding.plan(1024, 1024, 1024, 152) == "56x128 tiles of 8 warps"
+    assert binding.plan(1152, 1024, 512, 152) == "128x64 tiles of 8 warps"
+    assert set(binding.PLAN_NAMES) == set(range(10))
     with pytest.raises(ValueError):
         binding.plan(-1, 4, 4, 152)
