@@ -162,10 +162,10 @@ int t2s_gemm_f32_smem32(int64_t M, int64_t N, int64_t K, const float *A,
  * so the result differs from t2s_gemm_f32 only by the order of the chunk sums: it is
  * deterministic and within max |C - C_fp32| <= 1e-6 * K * max|a| * max|b|, but not
  * bit-identical.
- *  - splits: 1..64 chunks requested, or <= 0 for the library's choice (no split when the
- *    product already gives every SM 2.4 tiles of 128 x 128; otherwise about three rounds of
- *    chunk tiles on two CTAs per SM, chunks of at least 128 values, at most 16 chunks). With
- *    a single chunk the call is t2s_gemm_f32.
+ *  - splits: 1..64 chunks requested, or <= 0 for the library's choice: the count from 1 (no
+ *    split) to 16, chunks of at least 128 values, whose modelled time is least. The model is
+ *    the busiest SM's work under the product's own tiling choice, plus the bytes of the plane
+ *    sum. With a single chunk the call is t2s_gemm_f32.
  *  - workspace: a DEVICE buffer, 256-byte aligned, of at least
  *    t2s_gemm_f32_splitk_workspace_size(M, N, K, splits) bytes (0 if no split is made), owned
  *    by the caller and untouched until the stream has run the call.
@@ -173,6 +173,13 @@ int t2s_gemm_f32_smem32(int64_t M, int64_t N, int64_t K, const float *A,
  *    misaligned workspace, otherwise as t2s_gemm_f32.
  */
 size_t t2s_gemm_f32_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int splits);
+
+/*
+ * The chunk count t2s_gemm_f32_splitk takes for splits <= 0 on a GPU with `sms`
+ * multiprocessors (1 means no split: the call is t2s_gemm_f32). A host-only query: it
+ * touches no device. -1 if a dimension is negative or above T2S_MAX_DIM, or sms < 1.
+ */
+int t2s_gemm_f32_splitk_plan(int64_t M, int64_t N, int64_t K, int sms);
 int t2s_gemm_f32_splitk(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
                         float *C, int splits, void *workspace, size_t workspace_bytes,
                         t2s_stream_t stream);

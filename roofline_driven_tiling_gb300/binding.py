@@ -32,6 +32,7 @@ SIGNATURES = {
     "t2s_gemm_f32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_host": ([_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_plan": ([_i64, _i64, _i64, _i], _i),
+    "t2s_gemm_f32_splitk_plan": ([_i64, _i64, _i64, _i], _i),
     "t2s_gemm_f32_naive": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_smem32": ([_i64, _i64, _i64, _p, _p, _p, _p], _i),
     "t2s_gemm_f32_splitk_workspace_size": ([_i64, _i64, _i64, _i], _sz),
@@ -95,6 +96,10 @@ def t2s_gemm_f32_host(M, N, K, hA, hB, hC, dA, dB, dC, stream=0) -> int:
 
 def t2s_gemm_f32_plan(M, N, K, sms) -> int:
     return lib().t2s_gemm_f32_plan(M, N, K, sms)
+
+
+def t2s_gemm_f32_splitk_plan(M, N, K, sms) -> int:
+    return lib().t2s_gemm_f32_splitk_plan(M, N, K, sms)
 
 
 def t2s_gemm_f32_naive(M, N, K, A, B, C, stream=0) -> int:

@@ -372,6 +372,12 @@ int t2s_gemm_f32_plan(int64_t M, int64_t N, int64_t K, int sms) {
   return ffma_plan(M, N, K, sms);
 }
 
+int t2s_gemm_f32_splitk_plan(int64_t M, int64_t N, int64_t K, int sms) {
+  if (M < 0 || N < 0 || K < 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return -1;
+  if (sms < 1) return -1;
+  return splitk_choice(M, N, K, sms);
+}
+
 int t2s_version(void) { return 100; }
 
 }  // extern "C"

@@ -576,8 +576,9 @@ enum class FfmaPick {
 // non-monotone ones (1024^3 goes to 56 x 128 tiles of 8 warps, 1280^3 to 64 x 64, 1536^3 to
 // 128 x 128 of 8 warps, 1792^3 to 128 x 64, 2048^3 and 3072^3 to 256 x 128, 2560^3, 4096^3 and
 // 6144^3 to 256 x 128 with the 64 x 64 tail). `copies` products of this size share the GPU;
-// they (and K < 256) keep to the one-launch configurations of at most 128 x 128.
-FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
+// they (and K < 256) keep to the one-launch configurations of at most 128 x 128. `cost`, when
+// given, receives the busiest SM's work per k value in the model's units (area / efficiency).
+FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, double* cost = nullptr) {
   struct Cand {
     FfmaPick pick;
     int bm, bn;
@@ -648,6 +649,7 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies) {
   // against 53.6).
   if (best == FfmaPick::kBigShortK && n_copies == 1 && K <= 32 && big_per_sm > 2)
     best = FfmaPick::kPersistent;
+  if (cost != nullptr) *cost = best_cost;
   return best;
 }
 
@@ -771,22 +773,42 @@ int64_t splitk_chunk(int64_t K, int splits) {
   return (per + 31) / 32 * 32;
 }
 
-// The number of chunks the automatic choice uses (measured on GB300): none once the product
-// alone gives 2.4 tiles of 128 x 128 per SM (the unsplit product is then as fast); below that,
-// about three rounds of chunk tiles on the 2 x SMs CTA slots (2048^3: 4 chunks, 58.0 TFLOP/s
-// against 52.3 unsplit; 1536^3: 6, 52.7; 1024^3: 8, 38.4), chunks of at least 128 values
-// (shorter chunks spend their time filling the pipeline), at most 16.
-int splitk_auto(int64_t M, int64_t N, int64_t K) {
-  const int sms = sm_count();
-  if (sms <= 0) return 1;
-  const int64_t big_tiles = ((M + 127) / 128) * ((N + 127) / 128);
-  if (5 * big_tiles >= 12 * static_cast<int64_t>(sms)) return 1;
-  int64_t s = (6 * static_cast<int64_t>(sms) + big_tiles / 2) / big_tiles;  // round(3 x 2 SMs / tiles)
-  const int64_t by_k = K / 128;
-  if (s > by_k) s = by_k;
-  if (s > 16) s = 16;
-  return s < 1 ? 1 : static_cast<int>(s);
+// The number of chunks the automatic choice uses: the one whose modelled time is least, from
+// 1 (the product alone) to 16, with chunks of at least 128 values (shorter ones spend their
+// time filling the pipeline). The model is the product's own (pick_ffma): the busiest SM's
+// work per k value for all chunks' tiles together, times the chunk length, plus the plane sum,
+// which reads every plane and writes C once. Its weight, 40.9 work units per kilobyte, is the
+// least-squares fit of time = a x work + b x plane bytes + c to 132 measured points on GB300
+// (12 shapes from 512^3 to 256^2 x 8192, 1 to 16 chunks each, L2 flushed). On those shapes the
+// choice is within 3 % of the fastest count measured (1024^2 x 4096: 7 chunks, 55.5 TFLOP/s
+// against 50.2 unsplit), except 256^2 x 8192 (9 chunks, 28.6 against 30.3 with 16); the
+// earlier rule of about three rounds of chunk tiles on two CTA slots per SM lost 4-8 % at
+// 768^3, 1024^3, 1280^3, 1536^3 and 1792^3.
+int splitk_choice(int64_t M, int64_t N, int64_t K, int sms) {
+  if (sms <= 0 || M <= 0 || N <= 0 || K <= 0) return 1;
+  constexpr double kWorkPerKB = 40.9;
+  double per_k = 0.0;
+  pick_ffma(M, N, K, sms, 1, &per_k);
+  double best = per_k * static_cast<double>(K);
+  int best_s = 1;
+  const int64_t max_s = K / 128 < 16 ? K / 128 : 16;
+  for (int s = 2; s <= max_s; ++s) {
+    const int64_t kc = splitk_chunk(K, s);
+    const int planes = splitk_planes(K, s);
+    if (planes < 2) continue;
+    pick_ffma(M, N, kc, sms, planes, &per_k);
+    const double plane_kb = static_cast<double>(planes + 1) * static_cast<double>(M) *
+                            static_cast<double>(N) * 4.0 / 1000.0;
+    const double t = per_k * static_cast<double>(kc) + kWorkPerKB * plane_kb;
+    if (t < best) {
+      best = t;
+      best_s = s;
+    }
+  }
+  return best_s;
 }
+
+int splitk_auto(int64_t M, int64_t N, int64_t K) { return splitk_choice(M, N, K, sm_count()); }
 
 int splitk_planes(int64_t K, int splits) {
   const int64_t kc = splitk_chunk(K, splits);

@@ -48,6 +48,8 @@ int gemm_f32_kchunk(int64_t M, int64_t N, int64_t K, const float* A, const float
 // Split K: `splits` requested chunks (>= 1); partial products in `workspace`
 // (splitk_planes(K, splits) planes of M x N floats), summed into p.C in plane order.
 int splitk_auto(int64_t M, int64_t N, int64_t K);
+// The automatic chunk count on a GPU with `sms` multiprocessors (1: no split).
+int splitk_choice(int64_t M, int64_t N, int64_t K, int sms);
 int splitk_planes(int64_t K, int splits);
 cudaError_t launch_ffma_splitk(const Problem& p, int splits, float* workspace);
 // Stream K: the flattened tile x k-block space shared evenly over two CTAs per SM, partial

@@ -524,8 +524,9 @@ def run_splitk(A, B, splits, shift=0):
     return dC.data()
 
 
-@pytest.mark.parametrize("shape,splits", [((1024, 1024, 1024), 0), ((512, 512, 512), 0),
+@pytest.mark.parametrize("shape,splits", [((1024, 1024, 1024), 8), ((512, 512, 512), 0),
                                           ((256, 256, 4096), 0), ((1000, 1003, 997), 0),
+                                          ((640, 640, 1280), 0), ((1000, 1003, 997), 4),
                                           ((300, 130, 1000), 3), ((64, 64, 2048), 64),
                                           ((129, 257, 33), 2)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))

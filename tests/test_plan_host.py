@@ -77,6 +77,43 @@ def test_plan_depends_on_sm_count():
     assert binding.t2s_gemm_f32_plan(4096, 4096, 4096, 128) == HUGE
 
 
+# (M, N, K) -> chunk count of the automatic split-K choice (t2s_gemm_f32_splitk_plan), with
+# the measured TFLOP/s of that count and of the best alternative (GB300, L2 flushed, mean of
+# 30 calls; 1 is the product alone).
+SPLITK_MEASURED = {
+    (512, 512, 512): 4,        # 15.2; 5 chunks 15.6, the product 12.7
+    (768, 768, 768): 1,        # 32.6; 4 chunks 32.6, 6 chunks 31.4
+    (1024, 1024, 1024): 1,     # 44.3; 8 chunks 41.2
+    (1000, 1003, 997): 1,      # 26.1; 2 chunks 26.1, 8 chunks 24.6
+    (1280, 1280, 1280): 6,     # 48.4; 3 chunks 48.4, the product 44.9
+    (1536, 1536, 1536): 1,     # 55.5; 5 chunks 53.1
+    (1792, 1792, 1792): 3,     # 56.6; 6 chunks 55.4, the product 50.0
+    (2048, 2048, 2048): 4,     # 57.9; 2 chunks 56.4, the product 55.4
+    (1024, 1024, 4096): 7,     # 55.5; 8 chunks 53.9, the product 50.2
+    (512, 512, 4096): 9,       # 43.1; 8 chunks 40.7, the product 18.0
+    (256, 256, 8192): 9,       # 28.6; 16 chunks 30.3, the product 4.6
+    (4096, 4096, 4096): 1,
+}
+
+
+@pytest.mark.parametrize("shape", sorted(SPLITK_MEASURED), ids=lambda s: "x".join(map(str, s)))
+def test_splitk_plan_matches_measured(shape):
+    assert binding.t2s_gemm_f32_splitk_plan(*shape, 152) == SPLITK_MEASURED[shape]
+
+
+def test_splitk_plan_limits():
+    # Chunks of at least 128 values: K = 255 allows one chunk, K = 256 two.
+    assert binding.t2s_gemm_f32_splitk_plan(128, 128, 255, 152) == 1
+    assert binding.t2s_gemm_f32_splitk_plan(128, 128, 256, 152) == 2
+    # At most 16 chunks, however long K is.
+    assert binding.t2s_gemm_f32_splitk_plan(128, 128, 1 << 20, 152) == 16
+    # Empty problems make no split.
+    assert binding.t2s_gemm_f32_splitk_plan(0, 128, 4096, 152) == 1
+    assert binding.t2s_gemm_f32_splitk_plan(128, 128, 0, 152) == 1
+    for args in [(-1, 4, 4, 152), (4, 4, 4, 0), ((1 << 30) + 1, 4, 4, 152)]:
+        assert binding.t2s_gemm_f32_splitk_plan(*args) == -1
+
+
 @pytest.mark.parametrize("args", [(-1, 4, 4, 152), (4, -1, 4, 152), (4, 4, -1, 152),
                                   ((1 << 30) + 1, 4, 4, 152), (4, 4, 4, 0), (4, 4, 4, -3)])
 def test_plan_rejects_bad_arguments(args):
