@@ -3,7 +3,7 @@
 // while surpassing the FP32 theoretical peak performance", 2022). Not on the pages; the
 // operation is the same C = A x B as the product kernel.
 //
-// 1. Split pre-pass (two bandwidth-bound kernels). Every x of A and B becomes
+// 1. Split pre-pass (one bandwidth-bound launch). Every x of A and B becomes
 //      big = tf32(x), small = tf32(x - big)      (x - big is exact in FP32)
 //    with tf32() = round to nearest even at 10 explicit mantissa bits (IEEE 754
 //    rounding applied to the TF32 format, written from the definition below). The planes

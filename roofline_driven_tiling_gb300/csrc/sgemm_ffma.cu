@@ -525,7 +525,7 @@ using Tall84 = FfmaConfig<128, 64, 32, 3, 2, 4, 2, 8, 4, 1>;
 // 56 x 128 tiles of 8 warps (1 x 8 of 56 x 16), 7 x 4 per thread, A read 4 k values at a time:
 // a 1024 x 1024 C is 19 x 8 = 152 of them, one per SM, where 128 x 64 tiles leave 24 SMs idle
 // and give the busiest SM 14 % more work. Per SM both run the FMA pipe about 70 % busy, so the
-// gain is the balance: 1024^3 45.0 TFLOP/s against 41.4, 1024^2 x 4096 50.3 against 45.9,
+// gain is the balance: 1024^3 44.0-45.0 TFLOP/s against 41.4, 1024^2 x 4096 50.3 against 45.9,
 // 1000 x 1003 x 997 26.5 against 24.2. (Measured alongside: B read 8 bytes at a time, A 4 k
 // values at a time in the 128 x 64 tile, 4 x 8 per thread in it, 120 x 64 tiles of 12 warps,
 // 4 stages: none faster.)
