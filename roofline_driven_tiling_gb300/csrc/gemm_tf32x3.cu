@@ -11,7 +11,8 @@
 //      A_big, A_small : M x Kp      (A is already K-major: a row-wise copy)
 //      B_big, B_small : N x Kp      (B is K x N row-major: transposed through shared memory)
 //    so that every tensor-map stride is a multiple of 128 bytes whatever K and N are.
-// 2. Product kernel, persistent: one CTA of 192 threads per SM walks 128 x BN tiles of C.
+// 2. Product kernel, persistent: one CTA per SM (64 threads plus 4 epilogue warps per 128
+//    columns of the tile: 320 threads at BN = 224) walks 128 x BN tiles of C.
 //      warp 0     -- TMA producer: per K block, one box of each of the four planes;
 //      warp 1     -- allocates TMEM, one lane issues tcgen05.mma kind::tf32 (M=128, N=BN,
 //                    K=8), three per k step into one FP32 accumulator in TMEM, in the order

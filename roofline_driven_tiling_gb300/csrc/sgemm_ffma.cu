@@ -13,8 +13,9 @@
 //
 // GB300 design:
 //  * A STAGES-deep ring of shared-memory buffers per CTA, one "full" mbarrier per slot.
-//    There is no producer warp: a CTA is 4 compute warps, so two CTAs (8 warps, two per
-//    SM sub-partition) fit one SM with up to 255 registers per thread.
+//    There is no producer warp: every warp computes. CTA tiles run from 56 x 128 to
+//    256 x 128 of 4 or 8 warps, chosen per shape (pick_ffma), and an SM holds 8 warps,
+//    two per sub-partition, at up to 255 registers per thread for the largest register tile.
 //  * Aligned case (K % 4 == 0, N % 4 == 0, 16-byte aligned pointers): the Tensor Memory
 //    Accelerator loads a BM x BK box of A and a BK x BN box of B per stage; elements
 //    outside the matrices are filled with zeros by the TMA unit, and completion is
@@ -31,8 +32,9 @@
 //    8 distinct bank groups.
 //  * B is stored as it is (rows of BN floats); a warp reads 4 consecutive 16-byte
 //    chunks of one row per load, which is conflict-free without a swizzle.
-//  * Each thread owns an 8 x 16 register tile of C: rows g + 8i of its warp's 64 rows
-//    (g = lane / 4) and columns 4h + 16j + {0..3} of its warp's 64 columns (h = lane % 4).
+//  * Each thread owns a TM x TN register tile of C (8 x 16 in the large CTA tiles; 8 x 8,
+//    8 x 4, 7 x 4 or 4 x 8 in the small ones): rows g + 8i of its warp's 8 TM rows
+//    (g = lane / 4) and columns 4h + 16j + {0..3} of its warp's 4 TN columns (h = lane % 4).
 //    Accumulators are packed in pairs along n and updated with fma.rn.f32x2: one
 //    instruction does two IEEE fused multiply-adds, which halves the issue slots the
 //    FMAs need and leaves the rest for shared loads.

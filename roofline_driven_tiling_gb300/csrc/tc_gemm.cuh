@@ -208,8 +208,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // (one plane per operand, one MMA per k step); all accumulate in FP32.
 enum TcKind : int { kTf32x3 = 0, kBf16 = 1, kF16 = 2 };
 
-// B_MN: B is read in its own row-major K x N layout (MN-major for the tensor core, BF16 only)
-// instead of as an N x K transposed plane.
+// B_MN: B is read in its own row-major K x N layout (MN-major for the tensor core; 16-bit
+// operands only) instead of as an N x K transposed plane.
 // PAIR: CTAs run in clusters of two on two SMs that compute one 256-row tile together with
 // tcgen05 .cta_group::2 MMAs (issued by rank 0): each CTA stages its 128 rows of A and half of
 // B's columns, and accumulates its 128 rows in its own TMEM. Each SM thus receives half of
