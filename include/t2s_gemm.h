@@ -103,8 +103,8 @@ int t2s_gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B
  *    second launch; 6: 128 x 128 tiles of 8 warps; 7: 128 x 64 tiles of 8 warps; 9: 56 x 128
  *    tiles of 8 warps (6, 7 and 9 only for at most one tile per multiprocessor); 8: 128 x 128
  *    tiles on a persistent grid of two CTAs per multiprocessor, one TMA ring across tiles
- *    (K <= 32; on the cp.async path the call runs 1 instead). -1 if a dimension is negative
- *    or above T2S_MAX_DIM, or sms < 1.
+ *    (K <= 32; on the cp.async path the call runs 1 instead); 10: 32 x 32 tiles (small
+ *    products). -1 if a dimension is negative or above T2S_MAX_DIM, or sms < 1.
  */
 int t2s_gemm_f32_plan(int64_t M, int64_t N, int64_t K, int sms);
 

@@ -343,6 +343,7 @@ PLAN_NAMES = {
     7: "128x64 tiles of 8 warps",
     8: "128x128 tiles on a persistent grid",
     9: "56x128 tiles of 8 warps",
+    10: "32x32 tiles",
 }
 
 

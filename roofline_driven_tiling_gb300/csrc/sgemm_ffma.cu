@@ -532,6 +532,13 @@ using Tall84 = FfmaConfig<128, 64, 32, 3, 2, 4, 2, 8, 4, 1>;
 // values at a time in the 128 x 64 tile, 4 x 8 per thread in it, 120 x 64 tiles of 12 warps,
 // 4 stages: none faster.)
 using Wide74 = FfmaConfig<56, 128, 32, 3, 1, 8, 4, 7, 4, 1>;
+// 32 x 32 tiles of 4 warps, 2 x 4 per thread: for products so small that 64 x 64 tiles leave
+// most SMs idle, four times as many CTAs, each with a quarter of the work. Its FMA issue rate
+// is low, so it pays only while 64 x 64 tiles come to at most about half an SM each: 256^3
+// 3.1 TFLOP/s against 2.6, 384^3 8.8 against 6.7, 512^3 14.1 against 12.7, 512^2 x 2048 20.7
+// against 17.0; 640^3 19.2 against 20.8 and 768^3 22.9 against 33.2 (BK = 16 in 4 stages was
+// slower everywhere, 32 x 64 tiles of 2 x 8 per thread no faster).
+using Tiny24 = FfmaConfig<32, 32, 32, 3, 2, 2, 2, 2, 4, 1>;
 
 bool tma_ok(const Problem& p) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.A), b = reinterpret_cast<uintptr_t>(p.B);
@@ -562,13 +569,14 @@ enum class FfmaPick {
   kBig88 = 6,
   kTall84 = 7,
   kPersistent = 8,
-  kWide74 = 9
+  kWide74 = 9,
+  kTiny24 = 10
 };
 
 // Picks the configuration whose busiest SM has the least work: ceil(tiles / SMs) tiles of the
 // configuration's area, divided by its relative efficiency per FLOP, fitted to a sweep of square
 // and rectangular shapes from 768 to 8192 on GB300: 64 x 64 tiles 1.0, 128 x 64 1.05, 64 x 128
-// 1.04 (never ahead of 128 x 64, so not built); 128 x 128 tiles 1.15 from three tiles per SM on,
+// 1.04 (never ahead of 128 x 64, so not built), 32 x 32 0.6 (fitted from 256^3 to 768^3); 128 x 128 tiles 1.15 from three tiles per SM on,
 // 1.05 at two and 1.03 at one (with the compact k loop; the fully unrolled one pays only from
 // three); 256 x 128 tiles 1.17 (K >= 256); the 8-warp tiles only where they come to at most
 // one per SM: 128 x 128 1.116, 128 x 64 1.091, 56 x 128 1.043. The 256 x 128 tiles also run
@@ -586,14 +594,15 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, double*
     int bm, bn;
     double eff;
   };
-  const Cand cands[3] = {{FfmaPick::kBig, 128, 128, 1.15},  // efficiency set per tiles per SM
+  const Cand cands[4] = {{FfmaPick::kBig, 128, 128, 1.15},  // efficiency set per tiles per SM
                          {FfmaPick::kTall88, 128, 64, 1.05},
-                         {FfmaPick::kSmall48, 64, 64, 1.0}};
+                         {FfmaPick::kSmall48, 64, 64, 1.0},
+                         {FfmaPick::kTiny24, 32, 32, 0.6}};
   const int64_t n_copies = copies > 1 ? copies : 1;
   FfmaPick best = FfmaPick::kSmall48;
   double best_cost = 0.0;
   int64_t big_per_sm = 0;
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < 4; ++i) {
     const int64_t tiles = ((M + cands[i].bm - 1) / cands[i].bm) * ((N + cands[i].bn - 1) / cands[i].bn) *
                           n_copies;
     const int64_t per_sm = (tiles + sms - 1) / sms;
@@ -664,6 +673,7 @@ cudaError_t run_pick(FfmaPick pick, const Problem& p, Ts... args) {
     case FfmaPick::kBig88: return run_any<Big88>(p, args...);
     case FfmaPick::kTall84: return run_any<Tall84>(p, args...);
     case FfmaPick::kWide74: return run_any<Wide74>(p, args...);
+    case FfmaPick::kTiny24: return run_any<Tiny24>(p, args...);
     default: return run_any<Small48>(p, args...);
   }
 }

@@ -453,6 +453,7 @@ DISPATCH_SHAPES = {
     "big88_1536": (1536, 1536, 512),       # 144 tiles of 128 x 128, 8 warps of 8 x 8
     "small48_2048": (2048, 2048, 128),     # 1024 tiles of 64 x 64: 4 x 8 per thread, pipelined
     "small48_640": (640, 700, 300),        # 110 tiles of 64 x 64
+    "tiny24_384": (384, 384, 384),         # 144 tiles of 32 x 32, 2 x 4 per thread
 }
 
 

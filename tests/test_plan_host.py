@@ -9,7 +9,8 @@ import pytest
 
 from roofline_driven_tiling_gb300 import binding
 
-BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL, BIG88, TALL84, PERSISTENT, WIDE74 = range(10)
+BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL, BIG88, TALL84, PERSISTENT, WIDE74, TINY24 = \
+    range(11)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -20,7 +21,12 @@ def built():
 
 # (M, N, K) -> the configuration measured fastest (or within 1 % of it) on GB300.
 MEASURED = {
-    (768, 768, 768): SMALL48,
+    (256, 256, 256): TINY24,          # 3.1 TFLOP/s; 64 x 64 tiles 2.6
+    (384, 384, 384): TINY24,          # 8.8; 64 x 64 tiles 6.7
+    (512, 512, 512): TINY24,          # 14.1; 64 x 64 tiles 12.7
+    (512, 512, 2048): TINY24,         # 20.7; 64 x 64 tiles 17.0
+    (640, 640, 640): SMALL48,         # 20.8; 32 x 32 tiles 19.2
+    (768, 768, 768): SMALL48,         # 33.2; 32 x 32 tiles 22.9
     (1024, 1024, 1024): WIDE74,       # 45.0; 128 x 64 tiles of 8 warps 41.4
     (1024, 1024, 4096): WIDE74,       # 50.3; 128 x 64 tiles of 8 warps 45.9
     (1000, 1003, 997): WIDE74,        # 26.5; 128 x 64 tiles of 8 warps 24.2
@@ -81,7 +87,7 @@ def test_plan_depends_on_sm_count():
 # the measured TFLOP/s of that count and of the best alternative (GB300, L2 flushed, mean of
 # 30 calls; 1 is the product alone).
 SPLITK_MEASURED = {
-    (512, 512, 512): 4,        # 15.2; 5 chunks 15.6, the product 12.7
+    (512, 512, 512): 4,        # 15.2; 5 chunks 15.6, the product 14.1
     (768, 768, 768): 1,        # 32.6; 4 chunks 32.6, 6 chunks 31.4
     (1024, 1024, 1024): 1,     # 44.3; 8 chunks 41.2
     (1000, 1003, 997): 1,      # 26.1; 2 chunks 26.1, 8 chunks 24.6
@@ -90,8 +96,8 @@ SPLITK_MEASURED = {
     (1792, 1792, 1792): 3,     # 56.6; 6 chunks 55.4, the product 50.0
     (2048, 2048, 2048): 4,     # 57.9; 2 chunks 56.4, the product 55.4
     (1024, 1024, 4096): 7,     # 55.5; 8 chunks 53.9, the product 50.2
-    (512, 512, 4096): 9,       # 43.1; 8 chunks 40.7, the product 18.0
-    (256, 256, 8192): 9,       # 28.6; 16 chunks 30.3, the product 4.6
+    (512, 512, 4096): 9,       # 43.1; 8 chunks 40.7, the product 18.0 (64 x 64 tiles)
+    (256, 256, 8192): 9,       # 28.6; 16 chunks 30.3, the product 4.6 (64 x 64 tiles)
     (4096, 4096, 4096): 1,
 }
 
@@ -106,7 +112,7 @@ def test_splitk_plan_limits():
     assert binding.t2s_gemm_f32_splitk_plan(128, 128, 255, 152) == 1
     assert binding.t2s_gemm_f32_splitk_plan(128, 128, 256, 152) == 2
     # At most 16 chunks, however long K is.
-    assert binding.t2s_gemm_f32_splitk_plan(128, 128, 1 << 20, 152) == 16
+    assert binding.t2s_gemm_f32_splitk_plan(64, 64, 1 << 20, 152) == 16
     # Empty problems make no split.
     assert binding.t2s_gemm_f32_splitk_plan(0, 128, 4096, 152) == 1
     assert binding.t2s_gemm_f32_splitk_plan(128, 128, 0, 152) == 1
@@ -124,6 +130,7 @@ def test_plan_names():
     assert binding.plan(4096, 4096, 4096, 152) == "256x128 tiles in whole rounds, the rest as 64x64 tiles"
     assert binding.plan(1024, 1024, 1024, 152) == "56x128 tiles of 8 warps"
     assert binding.plan(1152, 1024, 512, 152) == "128x64 tiles of 8 warps"
-    assert set(binding.PLAN_NAMES) == set(range(10))
+    assert binding.plan(384, 384, 384, 152) == "32x32 tiles"
+    assert set(binding.PLAN_NAMES) == set(range(11))
     with pytest.raises(ValueError):
         binding.plan(-1, 4, 4, 152)
