@@ -789,7 +789,9 @@ int64_t splitk_chunk(int64_t K, int splits) {
 // 1 (the product alone) to 16, with chunks of at least 128 values (shorter ones spend their
 // time filling the pipeline). The model is the product's own (pick_ffma): the busiest SM's
 // work per k value for all chunks' tiles together, times the chunk length, plus the plane sum,
-// which reads every plane and writes C once. Its weight, 40.9 work units per kilobyte, is the
+// which reads every plane and writes C once, plus the plane sum's launch (300 K work units,
+// about 1.5 us: 256^3 in two chunks measured 2.6 TFLOP/s against 3.4 for the product alone
+// with 32 x 32 tiles). The plane weight, 40.9 work units per kilobyte, is the
 // least-squares fit of time = a x work + b x plane bytes + c to 132 measured points on GB300
 // (12 shapes from 512^3 to 256^2 x 8192, 1 to 16 chunks each, L2 flushed). On those shapes the
 // choice is within 3 % of the fastest count measured (1024^2 x 4096: 7 chunks, 55.5 TFLOP/s
@@ -799,6 +801,7 @@ int64_t splitk_chunk(int64_t K, int splits) {
 int splitk_choice(int64_t M, int64_t N, int64_t K, int sms) {
   if (sms <= 0 || M <= 0 || N <= 0 || K <= 0) return 1;
   constexpr double kWorkPerKB = 40.9;
+  constexpr double kPlaneSumLaunch = 3.0e5;
   double per_k = 0.0;
   pick_ffma(M, N, K, sms, 1, &per_k);
   double best = per_k * static_cast<double>(K);
@@ -811,7 +814,7 @@ int splitk_choice(int64_t M, int64_t N, int64_t K, int sms) {
     pick_ffma(M, N, kc, sms, planes, &per_k);
     const double plane_kb = static_cast<double>(planes + 1) * static_cast<double>(M) *
                             static_cast<double>(N) * 4.0 / 1000.0;
-    const double t = per_k * static_cast<double>(kc) + kWorkPerKB * plane_kb;
+    const double t = per_k * static_cast<double>(kc) + kWorkPerKB * plane_kb + kPlaneSumLaunch;
     if (t < best) {
       best = t;
       best_s = s;

@@ -108,9 +108,12 @@ def test_splitk_plan_matches_measured(shape):
 
 
 def test_splitk_plan_limits():
-    # Chunks of at least 128 values: K = 255 allows one chunk, K = 256 two.
-    assert binding.t2s_gemm_f32_splitk_plan(128, 128, 255, 152) == 1
-    assert binding.t2s_gemm_f32_splitk_plan(128, 128, 256, 152) == 2
+    # Chunks of at least 128 values: K = 383 allows two chunks, K = 384 three.
+    assert binding.t2s_gemm_f32_splitk_plan(64, 64, 383, 152) == 2
+    assert binding.t2s_gemm_f32_splitk_plan(64, 64, 384, 152) == 3
+    # A split pays for the plane sum's launch: at 256^3 the product alone is faster (3.4
+    # TFLOP/s with 32 x 32 tiles against 2.6 in two chunks).
+    assert binding.t2s_gemm_f32_splitk_plan(256, 256, 256, 152) == 1
     # At most 16 chunks, however long K is.
     assert binding.t2s_gemm_f32_splitk_plan(64, 64, 1 << 20, 152) == 16
     # Empty problems make no split.
