@@ -137,3 +137,29 @@ def test_plan_names():
     assert set(binding.PLAN_NAMES) == set(range(11))
     with pytest.raises(ValueError):
         binding.plan(-1, 4, 4, 152)
+
+
+def test_plan_properties_on_random_shapes():
+    """Invariants of the tiling choice on seeded random shapes: a one-round 8-warp tiling
+    only when its tiles fit the SMs once, the tail split only with at least one whole round
+    of 256 x 128 tiles and K >= 256, and a split-K count that keeps chunks of 128 values."""
+    import numpy as np
+
+    rng = np.random.default_rng(20261202)
+    one_round = {BIG88: (128, 128), TALL84: (128, 64), WIDE74: (56, 128)}
+    for _ in range(2000):
+        M, N = (int(x) for x in rng.integers(1, 9000, size=2))
+        K = int(rng.integers(1, 20000))
+        sms = int(rng.choice([108, 132, 148, 152]))
+        code = binding.t2s_gemm_f32_plan(M, N, K, sms)
+        assert code in binding.PLAN_NAMES
+        if code in one_round:
+            bm, bn = one_round[code]
+            assert -(-M // bm) * -(-N // bn) <= sms
+        if code == HUGE_TAIL:
+            assert K >= 256 and -(-M // 256) * -(-N // 128) > sms
+        if code == PERSISTENT:
+            assert K <= 32
+        s = binding.t2s_gemm_f32_splitk_plan(M, N, K, sms)
+        assert 1 <= s <= 16
+        assert s == 1 or K // s >= 128
