@@ -219,7 +219,11 @@ int t2s_gemm_f32_streamk(int64_t M, int64_t N, int64_t K, const float *A, const 
  * every FP32 product and partial sum is exact (for example small integers).
  * A NaN operand gives NaN where the definition does; an infinite operand may give
  * NaN where the definition gives an infinity (a correction term multiplies it by
- * the zero small part of an operand that TF32 represents exactly).
+ * the zero small part of an operand that TF32 represents exactly). Finite operands
+ * stay finite in the split, up to FLT_MAX: a value within half a TF32 ulp of it,
+ * which would round up to infinity, keeps its truncated TF32 value as big and the
+ * exact remainder goes into small, so results that are finite in the definition
+ * stay finite and within the bound.
  *
  * `workspace` is a DEVICE buffer, 256-byte aligned, of at least
  * t2s_gemm_f32_tf32x3_workspace_size(M, N, K) bytes, owned by the caller,
@@ -243,10 +247,11 @@ int t2s_gemm_f32_tf32x3(int64_t M, int64_t N, int64_t K, const float *A,
  * T2S_TF32X3_NOALLOC_MAX_SCRATCH bytes (32 MiB) inside this library. Every GPU that loads
  * the library holds that array until the process exits. The call allocates nothing and
  * calls no allocating routine.
- *  - Limit: t2s_gemm_f32_tf32x3_workspace_size(M, N, K) must not exceed
- *    T2S_TF32X3_NOALLOC_MAX_SCRATCH, i.e. about 16 * (M + N) * ceil(K / 32) * 32 bytes
- *    (for example M = N = K = 1024 fits). Larger problems return T2S_ERR_TOO_LARGE and
- *    enqueue nothing.
+ *  - Limit: t2s_gemm_f32_tf32x3_workspace_size(M, N, K), which is about
+ *    8 * (M + N) * ceil(K / 32) * 32 bytes (four planes of 4-byte values), must not exceed
+ *    T2S_TF32X3_NOALLOC_MAX_SCRATCH. M = N = K = 1024 takes 16 MiB; the largest square
+ *    product that fits is 1440^3. Larger problems return T2S_ERR_TOO_LARGE and enqueue
+ *    nothing.
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  *    once per device); make that first call before any stream capture begins.
  *  - All calls on a device share the one array, which keeps the last call's contents. Each

@@ -75,20 +75,18 @@ __global__ void __launch_bounds__(256) pad_rows_16bit_kernel(const uint16_t* __r
   }
 }
 
-#ifndef T2S_HALF_CHUNK_K
-#define T2S_HALF_CHUNK_K 2048
-#endif
+// K values the tensor core sums from zero before the epilogue adds them into the FP32 sums
+// (shorter chunks measured 3-5 % slower; error at K = 4096: 4.0e-4 against a bound of 4.1e-3).
+constexpr int kHalfChunkK = 2048;
 // Longest K for the 512-wide pair tiles, whose tensor cores sum all of K without the
 // round-to-nearest chunk additions (error at K = 8192: 2.0e-3 against a bound of 8.2e-3).
-#ifndef T2S_WIDE_MAX_K
-#define T2S_WIDE_MAX_K 16384
-#endif
+constexpr int64_t kWideMaxK = 16384;
 
 // The configurations of one 16-bit format (tc::kBf16 or tc::kF16). Tile widths BN (M is 128
 // per CTA), BK = 64 (128-byte rows) unless stated: wider tiles read A less per FLOP.
 template <int KIND>
 struct HalfConfigs {
-  static constexpr int C = T2S_HALF_CHUNK_K;
+  static constexpr int C = kHalfChunkK;
   // B as a transposed K-major plane.
   using T128 = tc::TcConfig<KIND, 128, 64, 6, C>;  // 6 stages of 32 KB
   using T192 = tc::TcConfig<KIND, 192, 64, 4, C>;  // 4 stages of 40 KB
@@ -161,11 +159,8 @@ cudaError_t launch_half(int64_t M, int64_t N, int64_t K, const uint16_t* A, cons
     const int widths[4] = {128, 192, 256, 512};
     const double weight[4] = {1.38, 1.33, 1.0, 0.85};
     // Pairs need two tile rows; 192 columns are three boxes and cannot be split in two.
-    const int n_widths = (M > 128 && K <= T2S_WIDE_MAX_K) ? 4 : 3;
-    int best = pick_width(M, N, sms, widths, weight, n_widths);
-#ifdef T2S_HALF_FORCE_WIDTH
-    best = T2S_HALF_FORCE_WIDTH;
-#endif
+    const int n_widths = (M > 128 && K <= kWideMaxK) ? 4 : 3;
+    const int best = pick_width(M, N, sms, widths, weight, n_widths);
     if (M > 128) {
       switch (best) {
         case 1: return tc::run_tc<typename Cf::M192>(p, a, nullptr, B, nullptr, lda, N, Kp);

@@ -54,12 +54,16 @@ size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // to nearest, ties to even, by integer arithmetic on the encoding: add half an ulp of the
 // 10-bit mantissa (minus one, plus the lowest kept bit for the tie rule) and clear the 13
 // dropped bits. A carry out of the mantissa correctly increments the exponent. NaN and
-// infinity are passed through.
+// infinity are passed through. A finite value within half a TF32 ulp of FLT_MAX
+// (|x| >= 0x7F7FF000) would round up to infinity; it keeps its truncated value instead, the
+// largest TF32 value of its sign, so that x - tf32(x) stays finite and exact and the
+// correction term of the split carries the rest.
 __device__ __forceinline__ float tf32_round(float x) {
-  uint32_t u = __float_as_uint(x);
+  const uint32_t u = __float_as_uint(x);
   if ((u & 0x7f800000u) == 0x7f800000u) return x;
-  u += 0x00000fffu + ((u >> 13) & 1u);
-  return __uint_as_float(u & 0xffffe000u);
+  const uint32_t r = (u + 0x00000fffu + ((u >> 13) & 1u)) & 0xffffe000u;
+  if ((r & 0x7f800000u) == 0x7f800000u) return __uint_as_float(u & 0xffffe000u);
+  return __uint_as_float(r);
 }
 
 __device__ __forceinline__ void split(float x, float& big, float& small) {
@@ -202,9 +206,6 @@ cudaError_t launch_tf32x3(const Problem& p, void* workspace) {
     }
   }
   if (p.K < 256) best = 0;  // one short chunk: the wide epilogue does not pay
-#ifdef TF32X3_FORCE_WIDTH
-  best = TF32X3_FORCE_WIDTH;
-#endif
   switch (best) {
     case 1: return tc::run_tc<Tf32N192>(p, a_big, a_small, b_big, b_small, Kp, Kp, Kp);
     case 2: return tc::run_tc<Tf32N224>(p, a_big, a_small, b_big, b_small, Kp, Kp, Kp);

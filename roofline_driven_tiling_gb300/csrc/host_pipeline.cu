@@ -29,35 +29,19 @@
 namespace t2s {
 namespace {
 
-#ifndef T2S_PIPE_MIN_ROWS
-#define T2S_PIPE_MIN_ROWS 1024
-#endif
-#ifndef T2S_PIPE_CONCURRENT
-#define T2S_PIPE_CONCURRENT 2
-#endif
-// K values per chunk of the K-chunk schedule (a multiple of 32); the first and the last
-// chunk take 1 / T2S_PIPE_EDGE_DIV of that, so that the products start sooner. The rest of
-// K after the switch runs in row blocks of T2S_PIPE_TAIL_ROWS.
-#ifndef T2S_PIPE_KCHUNK
-#define T2S_PIPE_KCHUNK 1024
-#endif
-#ifndef T2S_PIPE_EDGE_DIV
-#define T2S_PIPE_EDGE_DIV 2
-#endif
-#ifndef T2S_PIPE_TAIL_ROWS
-#define T2S_PIPE_TAIL_ROWS 1024
-#endif
-// The K-chunk schedule switches to row blocks over the rest of K once the operands have
-// arrived, estimated from these rates (percent scale on the estimate for tuning).
-#ifndef T2S_PIPE_COPY_GBS
-#define T2S_PIPE_COPY_GBS 200.0
-#endif
-#ifndef T2S_PIPE_TFLOPS
-#define T2S_PIPE_TFLOPS 60.0
-#endif
-#ifndef T2S_PIPE_SWITCH_PCT
-#define T2S_PIPE_SWITCH_PCT 100
-#endif
+// Schedule settings (measured at 2048^3 to 8192^3 on GB300; the alternatives tried are
+// within 1.5 % or slower). Row blocks have at least kMinRows rows and run on kConcurrent
+// compute streams. K chunks hold about kKChunk values (a multiple of 32); the first and the
+// last take 1 / kEdgeDiv of that, so that the products start sooner. The rest of K after the
+// switch runs in row blocks of kTailRows. The switch comes once the operands have arrived,
+// estimated from a copy rate of kCopyGBs and a product rate of kTflops.
+constexpr int64_t kMinRows = 1024;
+constexpr int kConcurrent = 2;
+constexpr int64_t kKChunk = 1024;
+constexpr int64_t kEdgeDiv = 2;
+constexpr int64_t kTailRows = 1024;
+constexpr double kCopyGBs = 200.0;
+constexpr double kTflops = 60.0;
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxBlocks = 8;
@@ -132,16 +116,16 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
   if (e != cudaSuccess) return fail(e);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  // Row blocks of at least T2S_PIPE_MIN_ROWS rows (1024 measured best at 3072^3 to 4096^3),
+  // Row blocks of at least kMinRows rows (1024 measured best at 3072^3 to 4096^3),
   // at most kMaxBlocks of them.
-  int nb = static_cast<int>(M / T2S_PIPE_MIN_ROWS);
+  int nb = static_cast<int>(M / kMinRows);
   nb = nb < 1 ? 1 : nb > kMaxBlocks ? kMaxBlocks : nb;
   const int64_t rows_per = (M + nb - 1) / nb;
 
-  // K chunk boundaries: an edge chunk, whole chunks of about T2S_PIPE_KCHUNK values, an
+  // K chunk boundaries: an edge chunk, whole chunks of about kKChunk values, an
   // edge chunk; at most kMaxBlocks chunks, every boundary but K a multiple of 32.
-  const int64_t kt = T2S_PIPE_KCHUNK / 32 * 32;
-  const int64_t edge = (kt / T2S_PIPE_EDGE_DIV + 31) / 32 * 32;
+  const int64_t kt = kKChunk / 32 * 32;
+  const int64_t edge = (kt / kEdgeDiv + 31) / 32 * 32;
   int64_t kb[kMaxBlocks + 1] = {0};
   int nk = 0;
   if (has_ab && K > 2 * edge) {
@@ -155,9 +139,9 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
   }
   // The K-chunk schedule when it has at least two chunks and exposes fewer bytes.
   const bool by_k = nk >= 2 && kb[1] * (M + N) < K * (N + rows_per);
-  // The rest of K after the switch runs in row blocks of T2S_PIPE_TAIL_ROWS.
+  // The rest of K after the switch runs in row blocks of kTailRows.
   if (by_k) {
-    nb = static_cast<int>(M / T2S_PIPE_TAIL_ROWS);
+    nb = static_cast<int>(M / kTailRows);
     nb = nb < 1 ? 1 : nb > kMaxBlocks ? kMaxBlocks : nb;
   }
   const int64_t rows_blk = (M + nb - 1) / nb;
@@ -187,9 +171,9 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
     // the row blocks take the rest of K (their C blocks then go back while later blocks
     // compute). The copy of the operands takes about (M + N) K 4 bytes / copy rate, the
     // product 2 M N K / FLOP rate.
-    const double copy_s = 4.0 * static_cast<double>(M + N) * K / (T2S_PIPE_COPY_GBS * 1e9);
-    const double per_k_s = 2.0 * static_cast<double>(M) * N / (T2S_PIPE_TFLOPS * 1e12);
-    const double k_cover = copy_s / per_k_s * (T2S_PIPE_SWITCH_PCT / 100.0);
+    const double copy_s = 4.0 * static_cast<double>(M + N) * K / (kCopyGBs * 1e9);
+    const double per_k_s = 2.0 * static_cast<double>(M) * N / (kTflops * 1e12);
+    const double k_cover = copy_s / per_k_s;
     int p = 1;
     while (p < nk - 1 && static_cast<double>(kb[p]) < k_cover) ++p;
     for (int j = 0; j < p; ++j) {
@@ -225,7 +209,7 @@ extern "C" int t2s_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* h
       if ((e = cudaStreamWaitEvent(cs, r->a_ready[i], 0)) != cudaSuccess) return fail(e);
     }
     // Blocks alternate between two compute streams, so two of them share the GPU.
-    const int conc = nb > 1 ? T2S_PIPE_CONCURRENT : 1;
+    const int conc = nb > 1 ? kConcurrent : 1;
     const float* a_blk = has_ab ? dA + r0 * K : nullptr;
     const float* b_all = has_ab ? dB : nullptr;
     const t2s_stream_t ts = reinterpret_cast<t2s_stream_t>(cs);

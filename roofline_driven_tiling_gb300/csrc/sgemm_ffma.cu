@@ -53,23 +53,6 @@
 #include "t2s_internal.h"
 #include "t2s_tmap.h"
 
-// Tuning knobs of the 128 x 128 configuration (defaults are the measured best).
-#ifndef BIG_AV
-#define BIG_AV 2
-#endif
-#ifndef BIG_BK
-#define BIG_BK 32
-#endif
-#ifndef BIG_STAGES
-#define BIG_STAGES 3
-#endif
-#ifndef FFMA_KG_UNROLL
-#define FFMA_KG_UNROLL 4
-#endif
-#ifndef FFMA_FORCE_CFG
-#define FFMA_FORCE_CFG -1
-#endif
-
 namespace t2s {
 namespace {
 
@@ -423,9 +406,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
     if (lane == 0) {
       if (kTma) {
         // The last warp to finish with this slot refills it with stage kb + S.
-        uint32_t old;
-        asm volatile("atom.shared.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(sCnt + 4u * s) : "memory");
-        if (old == Cfg::WARPS - 1) {
+        if (slot_done_count(sCnt + 4u * s) == Cfg::WARPS - 1) {
           asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
           if (kb + S < nkb)
             tma_stage<Cfg>(&tmA, &tmB, m0, n0, kbeg + (kb + S) * Cfg::BK, a_stage(s), b_stage(s),
@@ -504,13 +485,13 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
 // 128 x 128 CTA tile, 4 warps (2 x 2 of 64 x 64), 8 x 16 per thread, BK = 32, 3 stages:
 // 96 KB of ring per CTA, two CTAs (8 warps) per SM. The k loop is fully unrolled over a K
 // block when K is long enough to pay for the larger code.
-using Big = FfmaConfig<128, 128, BIG_BK, BIG_STAGES, 2, 2, BIG_AV, 8, 16, FFMA_KG_UNROLL>;
+using Big = FfmaConfig<128, 128, 32, 3, 2, 2, 2, 8, 16, 4>;
 using BigShortK = FfmaConfig<128, 128, 32, 3, 2, 2, 2, 8, 16, 1>;
 // 256 x 128 CTA tile, 8 warps (4 x 2 of 64 x 64), 8 x 16 per thread, BK = 32, 3 stages: 144 KB
 // of ring, one CTA (8 warps) per SM. The same warps per SM as two 128 x 128 CTAs, with three
 // quarters of the staged bytes and half the barrier rounds per FLOP: in whole rounds 4-5 %
 // faster (3072^3: 63.4 against 60.5 TFLOP/s), while its coarser rounds leave longer tails.
-using Huge = FfmaConfig<256, 128, 32, 3, 4, 2, 2, 8, 16, FFMA_KG_UNROLL>;
+using Huge = FfmaConfig<256, 128, 32, 3, 4, 2, 2, 8, 16, 4>;
 // 4 x 8 per thread (64 x 64 CTA tiles of 4 warps, BK = 32, 3 stages): many small CTAs (four
 // per SM) that even out the last wave. Measured fastest up to ~2.4 tiles of 128 x 128 per SM:
 // 1024^3 37.0 TFLOP/s (BK = 16 and 4 stages: 32.4; 128 x 64 tiles of 8 x 8: 35.8), 2048^3 52.3
@@ -712,15 +693,6 @@ cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int6
   range.accumulate = accumulate ? 1 : 0;
   // The configuration is chosen by the K values this launch covers.
   const int64_t span = kc > 0 ? (p.K - k0 < kc ? p.K - k0 : kc) : p.K;
-  switch (FFMA_FORCE_CFG) {
-    case 0: return run_any<Big>(p, 1, 0, nullptr, range);
-    case 1: return run_any<BigShortK>(p, 1, 0, nullptr, range);
-    case 3: return run_any<Small48>(p, 1, 0, nullptr, range);
-    case 4: return run_any<Tall88>(p, 1, 0, nullptr, range);
-    case 5: return run_any<Huge>(p, 1, 0, nullptr, range);
-    case 6: return run_huge_tail(p, sms, range);
-    default: break;
-  }
   // Blocks of a larger product that overlap on two streams (the host pipeline) run 128 x 128
   // tiles: their copies stagger them, so they share the GPU only in part, and the end-to-end
   // leg at 4096^3 measured 50.8 TFLOP/s with these tiles against 49.2 with the single-product
@@ -981,9 +953,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
       __syncwarp();
       if (lane == 0) {
         // The last warp to finish with this slot refills it with iteration j + S.
-        uint32_t old;
-        asm volatile("atom.shared.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(sCnt + 4u * s) : "memory");
-        if (old == Cfg::WARPS - 1) {
+        if (slot_done_count(sCnt + 4u * s) == Cfg::WARPS - 1) {
           asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
           if (j + S < count) issue_next(s);
         }

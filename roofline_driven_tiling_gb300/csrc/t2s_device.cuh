@@ -81,6 +81,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Counts one more warp done with a ring slot and returns the count before it. Acquire-release
+// at CTA scope: every warp's reads of the slot (ordered before its lane 0 by __syncwarp) happen
+// before the last warp's refill of it, and whatever the last warp of one slot wrote (the
+// stream-K load cursor) is visible to the last warp of the next slot, because every warp
+// counts slots in the same order and each count continues the release sequence of the ones
+// before it.
+__device__ __forceinline__ uint32_t slot_done_count(uint32_t counter) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+               : "=r"(old)
+               : "r"(counter)
+               : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------------------
 // Tensor Memory Accelerator: 2-D tiled load into shared memory, completion
 // reported to an mbarrier as transaction bytes.
@@ -95,19 +110,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// The same load written into the shared memory of every CTA of the cluster named in `mask`
-// (bit r = CTA rank r), at the same offset `dst`; each destination CTA's mbarrier at offset
-// `bar` receives the transaction bytes of its copy.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map,
-                                                      int32_t x, int32_t y, uint32_t bar,
-                                                      uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
       : "memory");
 }
 

@@ -315,6 +315,33 @@ def test_tf32x3_special_values(shift):
     assert float(np.max(np.abs(C[rest] - want[rest]))) <= tolerance(A[rest], B)
 
 
+@pytest.mark.parametrize("operand", ["A", "B"])
+def test_tf32x3_finite_operands_next_to_flt_max(operand):
+    """Finite operands within half a TF32 ulp of FLT_MAX (which round up to infinity in TF32)
+    and a few more of the largest binary32 values, in one operand; the other operand is
+    scaled by 2^-24 so that every element of the definition stays finite. The split must keep
+    them finite: the result is finite everywhere and within the tolerance of the oracle."""
+    M, N, K = 131, 136, 96
+    A, B = inputs.uniform_pair(M, N, K, 23)
+    big = np.frombuffer(np.array([0x7F7FFFFF, 0xFF7FFFFF, 0x7F7FF000, 0xFF7FF800, 0x7F7FEFFF,
+                                  0x7F7FC99E], dtype=np.uint32).tobytes(), dtype=np.float32)
+    if operand == "A":
+        B *= np.float32(2.0 ** -24)
+        pos = [(3, 5), (3, 6), (40, 50), (60, 2), (70, 80), (130, 95)]
+        for (i, k), v in zip(pos, big):
+            A[i, k] = v
+    else:
+        A *= np.float32(2.0 ** -24)
+        pos = [(5, 3), (6, 3), (50, 40), (2, 60), (80, 70), (95, 135)]
+        for (k, j), v in zip(pos, big):
+            B[k, j] = v
+    want = oracle.sgemm(A, B, oracle.MUL_ADD)
+    assert np.all(np.isfinite(want))
+    C = run("tf32x3", A, B)
+    assert np.all(np.isfinite(C)), "a finite operand near FLT_MAX gave a non-finite result"
+    assert float(np.max(np.abs(C - want))) <= tolerance(A, B)
+
+
 def test_tf32x3_workspace_checks():
     M, N, K = 64, 64, 64
     dA = torch.zeros((M, K), device="cuda")

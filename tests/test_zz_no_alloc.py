@@ -8,8 +8,10 @@ caller-provided workspace.
 
 The GPU test compares it, through the C ABI, with the workspace entry point on the same
 inputs, for two calls in a row with different shapes (so the second call runs on scratch
-left by the first), within the tolerance the parity tests use. It also checks that the
-device's free memory does not move across the second call. This file is collected last,
+left by the first). Both run the same deterministic kernels on the same split operands, so
+the results must agree bit for bit; each is also checked against the CPU oracle within the
+tolerance the parity tests use. It also checks that the device's free memory does not move
+across the second call. This file is collected last,
 so a run that stops at the first failure has already run every other test.
 """
 from __future__ import annotations
@@ -17,6 +19,7 @@ from __future__ import annotations
 import numpy as np
 import pytest
 
+import oracle
 from roofline_driven_tiling_gb300 import binding, inputs
 
 
@@ -29,14 +32,17 @@ def test_noalloc_rejects_problems_beyond_the_scratch_array():
     __graft_entry__.build()
     f = binding.t2s_gemm_f32_tf32x3_noalloc
     fake = 1 << 20  # never dereferenced: the size check comes first
-    # 16 * (4096 + 4096) * 4096 bytes of planes: far beyond 32 MiB.
+    # 8 * (4096 + 4096) * 4096 bytes of planes: far beyond 32 MiB.
     assert f(4096, 4096, 4096, fake, fake, fake + 4096) == binding.T2S_ERR_TOO_LARGE
     assert f(-1, 4, 4, fake, fake, fake + 4096) == binding.T2S_ERR_INVALID
     assert "32 MiB" in binding.t2s_status_string(binding.T2S_ERR_TOO_LARGE)
-    biggest_square = 1024
-    assert binding.t2s_gemm_f32_tf32x3_workspace_size(biggest_square, biggest_square,
-                                                      biggest_square) <= \
-        binding.T2S_TF32X3_NOALLOC_MAX_SCRATCH
+    size = binding.t2s_gemm_f32_tf32x3_workspace_size
+    cap = binding.T2S_TF32X3_NOALLOC_MAX_SCRATCH
+    # Four planes of 4-byte values, K padded to a multiple of 32: 1024^3 takes 16 MiB, and
+    # 1440^3 is the largest square product that fits (1441 pads K to 1472).
+    assert size(1024, 1024, 1024) == 16 << 20
+    assert size(1440, 1440, 1440) <= cap < size(1441, 1441, 1441)
+    assert f(1441, 1441, 1441, fake, fake, fake + 4096) == binding.T2S_ERR_TOO_LARGE
 
 
 @pytest.mark.gpu
@@ -78,6 +84,9 @@ def test_noalloc_matches_workspace_entry_point_twice():
             # The scratch array was set up by the first call; later calls take no memory.
             assert free_after == free_before
         got = C_new.cpu().numpy()
-        want = C_ref.cpu().numpy()
+        same_kernels = C_ref.cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), same_kernels.view(np.uint32)), \
+            "call %d differs from the workspace entry point" % call
+        want = oracle.sgemm(A, B, oracle.MUL_ADD)
         assert np.all(np.isfinite(got))
         assert float(np.max(np.abs(got - want))) <= _tolerance(A, B)
