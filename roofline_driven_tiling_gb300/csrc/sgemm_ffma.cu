@@ -94,28 +94,78 @@ __device__ __forceinline__ uint32_t a_swizzled(uint32_t off) {
   return off ^ (((off >> 7) & Cfg::SWZ_MASK) << 4);
 }
 
-// All threads of the CTA copy one stage (A box and B box) with 4-byte cp.async and zero
-// fill, then arrive on the stage's full barrier when their copies have landed.
+// Ring depth of the general (cp.async) path: one stage more than the TMA path where the
+// extra stage still fits the CTAs per SM the configuration is built for. The general path
+// issues a stage's copies S - 2 K blocks before it is needed (see sgemm_ffma_general_kernel),
+// so the extra stage is what hides the copies' latency.
 template <class Cfg>
-__device__ __forceinline__ void cp_async_stage(const float* __restrict__ A,
+struct GenRing {
+  static constexpr int ringBytes(int s) { return s * Cfg::STAGE_BYTES + 2 * s * 8 + 1024; }
+  // 228 KB of shared memory per SM, 1 KB of it reserved per CTA.
+  static constexpr bool kDeeper = Cfg::MIN_BLOCKS * (ringBytes(Cfg::STAGES + 1) + 1024) <= 228 * 1024;
+  static constexpr int STAGES = kDeeper ? Cfg::STAGES + 1 : Cfg::STAGES;
+  static constexpr int SMEM_BYTES = ringBytes(STAGES);
+};
+
+// One stage of the general path: the BM x BK block of A at (m0, k0) and the BK x BN block of B
+// at (k0, n0), copied by every thread of the CTA with 4-byte cp.async into the same
+// shared-memory image the TMA path writes (A K-major with the 128-byte swizzle, B as stored),
+// zeros for rows >= M, k >= kend and columns >= N. Warp w copies the A rows w, w + WARPS, ...
+// (lane = k, one instruction per row); the threads copy B rows THREADS / BN at a time (thread
+// t: column t % BN). A stage wholly inside the matrices takes no bounds checks. The thread
+// arrives on the stage's full barrier once its copies have landed.
+template <class Cfg>
+__device__ __forceinline__ void gen_copy_stage(const float* __restrict__ A,
                                                const float* __restrict__ B, int M, int N, int K,
                                                int kend, int m0, int n0, int k0, uint32_t a_dst,
                                                uint32_t b_dst, uint32_t full_bar) {
-#pragma unroll 4
-  for (int e = threadIdx.x; e < Cfg::BM * Cfg::BK; e += Cfg::THREADS) {
-    const int r = e / Cfg::BK, c = e % Cfg::BK;
-    const int gm = m0 + r, gk = k0 + c;
-    const bool v = gm < M && gk < kend;
-    const float* src = v ? A + (static_cast<int64_t>(gm) * K + gk) : A;
-    cp_async_4(a_dst + a_swizzled<Cfg>(r * Cfg::A_ROW_BYTES + c * 4), src, v ? 4u : 0u);
-  }
-#pragma unroll 4
-  for (int e = threadIdx.x; e < Cfg::BK * Cfg::BN; e += Cfg::THREADS) {
-    const int r = e / Cfg::BN, c = e % Cfg::BN;
-    const int gk = k0 + r, gn = n0 + c;
-    const bool v = gk < kend && gn < N;
-    const float* src = v ? B + (static_cast<int64_t>(gk) * N + gn) : B;
-    cp_async_4(b_dst + (r * Cfg::BN + c) * 4, src, v ? 4u : 0u);
+  static_assert(Cfg::BK == 32, "one warp instruction per A row");
+  static_assert(Cfg::BM % Cfg::WARPS == 0 && Cfg::THREADS % Cfg::BN == 0, "copy mapping");
+  constexpr int A_ROWS = Cfg::BM / Cfg::WARPS;    // A rows per warp
+  constexpr int B_STEP = Cfg::THREADS / Cfg::BN;  // B rows per pass of the CTA
+  constexpr int B_PASSES = Cfg::BK / B_STEP;
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const int bcol = static_cast<int>(threadIdx.x) % Cfg::BN;
+  const int brow = static_cast<int>(threadIdx.x) / Cfg::BN;
+  // This thread's first A element and destination (row `warp`, k = k0 + lane), and its first
+  // B element (row k0 + brow, column n0 + bcol).
+  const float* a_src = A + static_cast<int64_t>(m0 + warp) * K + (k0 + lane);
+  const float* b_src = B + static_cast<int64_t>(k0 + brow) * N + (n0 + bcol);
+  const uint32_t b_dst0 = b_dst + static_cast<uint32_t>((brow * Cfg::BN + bcol) * 4);
+  auto a_off = [&](int r) {  // swizzled offset of (row r, k = lane) in the A stage
+    return static_cast<uint32_t>(r * Cfg::A_ROW_BYTES +
+                                 ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2)));
+  };
+  if (m0 + Cfg::BM <= M && k0 + Cfg::BK <= kend && n0 + Cfg::BN <= N) {
+#pragma unroll
+    for (int i = 0; i < A_ROWS; ++i) {
+      const int r = warp + Cfg::WARPS * i;
+      cp_async_4_full(a_dst + a_off(r), a_src + static_cast<int64_t>(Cfg::WARPS) * i * K);
+    }
+#pragma unroll
+    for (int i = 0; i < B_PASSES; ++i)
+      cp_async_4_full(b_dst0 + static_cast<uint32_t>(i * B_STEP * Cfg::BN * 4),
+                      b_src + static_cast<int64_t>(B_STEP) * i * N);
+  } else {
+    // Out-of-range elements are zero-filled; their source pointer is replaced by the
+    // matrix's first element, which nothing reads (0 source bytes).
+    const bool k_ok = k0 + lane < kend;
+    const int rows_left = M - m0 - warp;
+#pragma unroll
+    for (int i = 0; i < A_ROWS; ++i) {
+      const int r = warp + Cfg::WARPS * i;
+      const bool v = k_ok && Cfg::WARPS * i < rows_left;
+      cp_async_4(a_dst + a_off(r), v ? a_src + static_cast<int64_t>(Cfg::WARPS) * i * K : A,
+                 v ? 4u : 0u);
+    }
+    const bool n_ok = n0 + bcol < N;
+    const int k_left = kend - k0 - brow;
+#pragma unroll
+    for (int i = 0; i < B_PASSES; ++i) {
+      const bool v = n_ok && B_STEP * i < k_left;
+      cp_async_4(b_dst0 + static_cast<uint32_t>(i * B_STEP * Cfg::BN * 4),
+                 v ? b_src + static_cast<int64_t>(B_STEP) * i * N : B, v ? 4u : 0u);
+    }
   }
   cp_async_arrive_noinc(full_bar);
 }
@@ -286,7 +336,32 @@ __device__ __forceinline__ void load_tile(uint64_t (&acc)[Cfg::TM][Cfg::TN / 2],
   }
 }
 
-template <class Cfg, bool kTma>
+// The CTA's tile and K range. Grouped tile order over the tiles_m x tiles_n grid of wbm x wbn
+// tiles: 8 tile-rows at a time sweep the columns, so that the A rows and B columns in flight
+// stay resident in L2. A launch covers tiles tile_off, tile_off + 1, ... of that order, each as
+// dm x dn CTA tiles of BM x BN (wbm = dm BM, wbn = dn BN); CTA tiles wholly outside C have no
+// work (returns false). The K range is chunk blockIdx.y of k_chunk values from k_base on (the
+// whole of K when the grid has one row and k_base is 0), written to plane blockIdx.y of C;
+// k_chunk and k_base are multiples of BK.
+template <class Cfg>
+__device__ __forceinline__ bool cta_work(int M, int N, int K, int tiles_m, int tiles_n, int wbm,
+                                         int wbn, int tile_off, int dm, int dn, int k_chunk,
+                                         int k_base, int& m0, int& n0, int& kbeg, int& kend) {
+  constexpr int kGroup = 8;
+  const int tile = tile_off + static_cast<int>(blockIdx.x) / (dm * dn);
+  const int sub = static_cast<int>(blockIdx.x) % (dm * dn);
+  const int per_group = kGroup * tiles_n;
+  const int first_m = (tile / per_group) * kGroup;
+  const int gsz = min(tiles_m - first_m, kGroup);
+  m0 = (first_m + (tile % per_group) % gsz) * wbm + (sub / dn) * Cfg::BM;
+  n0 = ((tile % per_group) / gsz) * wbn + (sub % dn) * Cfg::BN;
+  kbeg = k_base + static_cast<int>(blockIdx.y) * k_chunk;
+  kend = min(K, kbeg + k_chunk);
+  return m0 < M && n0 < N;
+}
+
+// The product on the TMA path (K % 4 == 0, N % 4 == 0, 16-byte aligned A and B).
+template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const float* __restrict__ A,
@@ -299,56 +374,32 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sA = base;
   const uint32_t sB = sA + S * Cfg::A_STAGE_BYTES;
-  const uint32_t sBar = sB + S * Cfg::B_STAGE_BYTES;  // full[S], empty[S]
-  const uint32_t sCnt = sBar + 16u * S;                // refill counters (TMA path)
+  const uint32_t sBar = sB + S * Cfg::B_STAGE_BYTES;  // full[S] (the empty[S] words are unused)
+  const uint32_t sCnt = sBar + 16u * S;                // refill counters
   auto full = [&](int s) { return sBar + 8u * s; };
-  auto empty = [&](int s) { return sBar + 8u * (S + s); };
   auto a_stage = [&](int s) { return sA + static_cast<uint32_t>(s) * Cfg::A_STAGE_BYTES; };
   auto b_stage = [&](int s) { return sB + static_cast<uint32_t>(s) * Cfg::B_STAGE_BYTES; };
 
-  // Grouped tile order over the tiles_m x tiles_n grid of wbm x wbn tiles: 8 tile-rows at a
-  // time sweep the columns, so that the A rows and B columns in flight stay resident in L2.
-  // This launch covers tiles tile_off, tile_off + 1, ... of that order, each as dm x dn CTA
-  // tiles of BM x BN (wbm = dm BM, wbn = dn BN); CTA tiles wholly outside C have no work.
-  constexpr int kGroup = 8;
-  const int tile = tile_off + static_cast<int>(blockIdx.x) / (dm * dn);
-  const int sub = static_cast<int>(blockIdx.x) % (dm * dn);
-  const int per_group = kGroup * tiles_n;
-  const int first_m = (tile / per_group) * kGroup;
-  const int gsz = min(tiles_m - first_m, kGroup);
-  const int m0 = (first_m + (tile % per_group) % gsz) * wbm + (sub / dn) * Cfg::BM;
-  const int n0 = ((tile % per_group) / gsz) * wbn + (sub % dn) * Cfg::BN;
-  if (m0 >= M || n0 >= N) return;
-  // K range of this CTA: chunk blockIdx.y of k_chunk values from k_base on (the whole of K
-  // when the grid has one row and k_base is 0), written to plane blockIdx.y of C. k_chunk and
-  // k_base are multiples of BK.
-  const int kbeg = k_base + static_cast<int>(blockIdx.y) * k_chunk;
-  const int kend = min(K, kbeg + k_chunk);
+  int m0, n0, kbeg, kend;
+  if (!cta_work<Cfg>(M, N, K, tiles_m, tiles_n, wbm, wbn, tile_off, dm, dn, k_chunk, k_base, m0,
+                     n0, kbeg, kend))
+    return;
   C += static_cast<int64_t>(blockIdx.y) * c_plane;
   const int nkb = (kend - kbeg + Cfg::BK - 1) / Cfg::BK;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full(s), kTma ? 1u : static_cast<uint32_t>(Cfg::THREADS));
-      mbar_init(empty(s), Cfg::WARPS);
+      mbar_init(full(s), 1u);
       asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
     }
     mbar_fence_init();
-    if (kTma) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
-      for (int kb = 0; kb < S && kb < nkb; ++kb)
-        tma_stage<Cfg>(&tmA, &tmB, m0, n0, kbeg + kb * Cfg::BK, a_stage(kb), b_stage(kb), full(kb));
-    }
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    for (int kb = 0; kb < S && kb < nkb; ++kb)
+      tma_stage<Cfg>(&tmA, &tmB, m0, n0, kbeg + kb * Cfg::BK, a_stage(kb), b_stage(kb), full(kb));
   }
   __syncthreads();
-  if (!kTma) {
-    // Prologue of the cp.async ring: stages 0 .. S-2 (stage kb + S - 1 is issued at kb).
-    for (int kb = 0; kb < S - 1 && kb < nkb; ++kb)
-      cp_async_stage<Cfg>(A, B, M, N, K, kend, m0, n0, kbeg + kb * Cfg::BK, a_stage(kb),
-                          b_stage(kb), full(kb));
-  }
 
   const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
   const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
@@ -375,26 +426,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
 
   for (int kb = 0; kb < nkb; ++kb) {
     const int s = kb % S;
-    if (!kTma) {
-      // Refill the slot freed at kb - 1 with stage kb + S - 1, once every warp is done with it.
-      const int nk = kb + S - 1;
-      if (nk < nkb) {
-        const int ns = nk % S;
-        bool freed = true;
-        if (kb >= 1) freed = mbar_wait_bounded(empty(ns), static_cast<uint32_t>((kb - 1) / S) & 1u, status);
-        if (!__all_sync(0xffffffffu, freed)) {
-          asm volatile("cp.async.wait_all;" ::: "memory");
-          return;
-        }
-        cp_async_stage<Cfg>(A, B, M, N, K, kend, m0, n0, kbeg + nk * Cfg::BK, a_stage(ns),
-                            b_stage(ns), full(ns));
-      }
-    }
     // Every lane polls; the decision to give up is taken by the whole warp at once.
     const bool landed = mbar_wait_bounded(full(s), static_cast<uint32_t>(kb / S) & 1u, status);
     if (!__all_sync(0xffffffffu, landed)) {
-      if (!kTma) asm volatile("cp.async.wait_all;" ::: "memory");
-      if (kTma && lane == 0) {
+      if (lane == 0) {
         // Let copies already issued into this CTA's ring land before leaving.
         for (int j = kb; j < kb + S && j < nkb; ++j)
           mbar_wait_bounded(full(j % S), static_cast<uint32_t>(j / S) & 1u, status, 10000000ull);
@@ -404,17 +439,114 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
     ffma_kblock<Cfg>(acc, a_stage(s) + a_row0, b_stage(s) + b_col0, xr);
     __syncwarp();
     if (lane == 0) {
-      if (kTma) {
-        // The last warp to finish with this slot refills it with stage kb + S.
-        if (slot_done_count(sCnt + 4u * s) == Cfg::WARPS - 1) {
-          asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
-          if (kb + S < nkb)
-            tma_stage<Cfg>(&tmA, &tmB, m0, n0, kbeg + (kb + S) * Cfg::BK, a_stage(s), b_stage(s),
-                           full(s));
-        }
-      } else {
-        mbar_arrive(empty(s));
+      // The last warp to finish with this slot refills it with stage kb + S.
+      if (slot_done_count(sCnt + 4u * s) == Cfg::WARPS - 1) {
+        asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
+        if (kb + S < nkb)
+          tma_stage<Cfg>(&tmA, &tmB, m0, n0, kbeg + (kb + S) * Cfg::BK, a_stage(s), b_stage(s),
+                         full(s));
       }
+    }
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  store_tile<Cfg>(acc, C, M, N, m0 + wm0 + g, n0 + wn0 + 4 * h, vec_store);
+}
+
+// The product on the general path (any K and N, 4-byte aligned A and B): the same register
+// tiles and k order as the TMA path, over a ring of GenRing<Cfg>::STAGES slots that every
+// thread fills with gen_copy_stage. Per K block kb, a warp waits for stage kb to land (a full
+// barrier counting every thread's copies), multiplies it, and marks the slot done (an empty
+// barrier counting warps). Only then does it wait for every warp to be done with stage
+// kb - 1 and copy its share of stage kb - 1 + S into that slot: a warp may run a K block ahead
+// of the slowest one without waiting, and each stage is issued S - 2 K blocks before it is
+// used.
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
+    sgemm_ffma_general_kernel(const __grid_constant__ CUtensorMap tmA,
+                              const __grid_constant__ CUtensorMap tmB, const float* __restrict__ A,
+                              const float* __restrict__ B, float* __restrict__ C, int M, int N,
+                              int K, int tiles_m, int tiles_n, unsigned* status, int vec_store,
+                              int k_chunk, int64_t c_plane, int wbm, int wbn, int tile_off, int dm,
+                              int dn, int k_base, int accumulate) {
+  (void)tmA;
+  (void)tmB;
+  constexpr int S = GenRing<Cfg>::STAGES;
+  static_assert(S >= 3, "a stage is issued S - 2 K blocks ahead");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sA = base;
+  const uint32_t sB = sA + S * Cfg::A_STAGE_BYTES;
+  const uint32_t sBar = sB + S * Cfg::B_STAGE_BYTES;  // full[S], empty[S]
+  auto full = [&](int s) { return sBar + 8u * s; };
+  auto empty = [&](int s) { return sBar + 8u * (S + s); };
+  auto a_stage = [&](int s) { return sA + static_cast<uint32_t>(s) * Cfg::A_STAGE_BYTES; };
+  auto b_stage = [&](int s) { return sB + static_cast<uint32_t>(s) * Cfg::B_STAGE_BYTES; };
+
+  int m0, n0, kbeg, kend;
+  if (!cta_work<Cfg>(M, N, K, tiles_m, tiles_n, wbm, wbn, tile_off, dm, dn, k_chunk, k_base, m0,
+                     n0, kbeg, kend))
+    return;
+  C += static_cast<int64_t>(blockIdx.y) * c_plane;
+  const int nkb = (kend - kbeg + Cfg::BK - 1) / Cfg::BK;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), static_cast<uint32_t>(Cfg::THREADS));
+      mbar_init(empty(s), static_cast<uint32_t>(Cfg::WARPS));
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+  // Prologue: stages 0 .. S - 2 (slot S - 1 is filled after the first K block).
+  for (int kb = 0; kb < S - 1 && kb < nkb; ++kb)
+    gen_copy_stage<Cfg>(A, B, M, N, K, kend, m0, n0, kbeg + kb * Cfg::BK, a_stage(kb),
+                        b_stage(kb), full(kb));
+
+  const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
+  const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
+  const int g = lane >> 2, h = lane & 3;
+
+  uint64_t acc[Cfg::TM][Cfg::TN / 2];
+  if (accumulate) {
+    load_tile<Cfg>(acc, C, M, N, m0 + wm0 + g, n0 + wn0 + 4 * h, vec_store);
+  } else {
+#pragma unroll
+    for (int i = 0; i < Cfg::TM; ++i)
+#pragma unroll
+      for (int j = 0; j < Cfg::TN / 2; ++j) acc[i][j] = 0ull;  // two +0.0f
+  }
+
+  const uint32_t a_row0 = static_cast<uint32_t>((wm0 + g) * Cfg::A_ROW_BYTES);
+  const uint32_t xr = (a_row0 >> 7) & Cfg::SWZ_MASK;
+  const uint32_t b_col0 = static_cast<uint32_t>((wn0 + 4 * h) * 4);
+
+  for (int kb = 0; kb < nkb; ++kb) {
+    const int s = kb % S;
+    // Every lane polls; the decision to give up is taken by the whole warp at once. A thread
+    // that gives up first waits for its own copies to land, so none lands after it exits.
+    const bool landed = mbar_wait_bounded(full(s), static_cast<uint32_t>(kb / S) & 1u, status);
+    if (!__all_sync(0xffffffffu, landed)) {
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      return;
+    }
+    ffma_kblock<Cfg>(acc, a_stage(s) + a_row0, b_stage(s) + b_col0, xr);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(s));
+    // Refill: stage kb + S - 1 goes into the slot of stage kb - 1 once every warp is done
+    // with that (the slot S - 1 is still free after the first K block).
+    const int nk = kb + S - 1;
+    if (nk < nkb) {
+      const int ns = nk % S;
+      bool freed = true;
+      if (kb >= 1) freed = mbar_wait_bounded(empty(ns), static_cast<uint32_t>((kb - 1) / S) & 1u, status);
+      if (!__all_sync(0xffffffffu, freed)) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        return;
+      }
+      gen_copy_stage<Cfg>(A, B, M, N, K, kend, m0, n0, kbeg + nk * Cfg::BK, a_stage(ns),
+                          b_stage(ns), full(ns));
     }
   }
 
@@ -451,9 +583,9 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
     e = encode_tmap_f32_2d(&tb, p.B, p.N, p.K, Cfg::BN, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
   }
-  auto kern = sgemm_ffma_kernel<Cfg, kTma>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  auto kern = kTma ? sgemm_ffma_kernel<Cfg> : sgemm_ffma_general_kernel<Cfg>;
+  const int smem = kTma ? Cfg::SMEM_BYTES : GenRing<Cfg>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int wbm = part.wbm > 0 ? part.wbm : Cfg::BM, wbn = part.wbn > 0 ? part.wbn : Cfg::BN;
   if (wbm % Cfg::BM != 0 || wbn % Cfg::BN != 0) return cudaErrorInvalidConfiguration;
@@ -474,7 +606,7 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
   const int chunk = part.kc > 0 ? static_cast<int>(part.kc)
                     : splits == 1 ? static_cast<int>(p.K) : k_chunk;
   const dim3 grid(static_cast<unsigned>(count * dm * dn), static_cast<unsigned>(splits));
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, p.stream>>>(
+  kern<<<grid, Cfg::THREADS, smem, p.stream>>>(
       ta, tb, p.A, p.B, c, static_cast<int>(p.M), static_cast<int>(p.N), static_cast<int>(p.K),
       static_cast<int>(tiles_m), static_cast<int>(tiles_n), p.status, vec_store, chunk,
       p.M * p.N, wbm, wbn, static_cast<int>(part.off), dm, dn, static_cast<int>(part.k0),

@@ -146,6 +146,11 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32
                : "memory");
 }
 
+// The same copy of 4 bytes that are known to be in range (no zero fill).
+__device__ __forceinline__ void cp_async_4_full(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // Arrives on `bar` once all of this thread's earlier cp.async copies have
 // landed. The barrier's expected count must include this arrival.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
