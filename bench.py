@@ -196,6 +196,49 @@ def cpu_oracle_rate(A, B, target_s: float):
     return flops / dt / 1e12, info
 
 
+def cpu_blocked_rate(A, B, target_s: float = 4.0):
+    """Times the cache-blocked multi-core CPU GEMM (a stronger CPU baseline than the oracle;
+    it checks nothing) on a row block of C = A x B sized to take about target_s; returns the
+    bench-line entry."""
+    import cpu_baseline
+    M, K = A.shape
+    N = B.shape[1]
+    nt = cpu_baseline.num_threads()
+    rows = min(M, 256)
+    t0 = time.perf_counter()
+    cpu_baseline.sgemm(A[:rows], B)
+    per_row = max(time.perf_counter() - t0, 1e-4) / rows
+    rows = int(min(M, max(rows, target_s / per_row)))
+    t0 = time.perf_counter()
+    cpu_baseline.sgemm(A[:rows], B)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * rows * N * K / dt / 1e12, "unit": UNIT, "cores": nt,
+            "kind": "cache-blocked multi-core C (fused multiply-adds in ascending k, bit-identical "
+                    "to the oracle's FMA reading; a baseline, not a checker)",
+            "sample": "rows 0..%d of the %dx%dx%d product" % (rows - 1, M, N, K), "seconds": dt}
+
+
+def cpu_literal_loop_1024():
+    """The literal i / j / k triple loop (the oracle's two-rounding reading, one thread) at
+    1024^3, to set beside the CPU time the third page reports for the same loop and size."""
+    import oracle
+    from roofline_driven_tiling_gb300 import inputs
+    A, B = inputs.constant(1024, 1024, 1024)  # the page's A = 0.5, B = 0.4
+    nt = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        C = oracle.sgemm(A, B, oracle.MUL_ADD)
+        dt = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(nt)
+    return {"seconds": dt, "gflops": 2.0 * 1024 ** 3 / dt / 1e9, "cores": 1,
+            "c00": float(C[0, 0]),
+            "workload": "C = A x B, 1024^3, A = 0.5, B = 0.4, plain C triple loop (i, j, k), "
+                        "one thread; the page's own figure for this loop is about 16-17 s on an "
+                        "unstated CPU"}
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -263,6 +306,31 @@ def time_steps(fn, steps, warmup, stream, flush_buf):
     return [s.elapsed_time(e) for s, e in ev]
 
 
+def measure_probes(lib, dev, stream):
+    """Measured ceilings from the library's throughput probes (the best of 5 launches, each
+    timed alone with CUDA events on `stream`): the FP32 FMA pipe at the product kernels' 8
+    warps per SM, and the TF32 tensor pipe (tcgen05.mma kind::tf32, M 128, N 256)."""
+    import torch
+    from roofline_driven_tiling_gb300 import binding
+    out = torch.empty(binding.t2s_probe_outputs(), dtype=torch.float32, device=dev)
+    sp = stream.cuda_stream
+    res = {}
+    for kind, iters in (("fp32_fma", 1 << 17), ("tf32_mma", 1 << 14)):
+        binding.probe(kind, iters, out.data_ptr(), sp)
+        best = 0.0
+        for _ in range(5):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            flops = binding.probe(kind, iters, out.data_ptr(), sp)
+            e.record(stream)
+            torch.cuda.synchronize()
+            best = max(best, flops / (s.elapsed_time(e) * 1e-3) / 1e12)
+        res[kind + "_tflops"] = best
+    if binding.t2s_device_status(sp) != binding.T2S_OK:
+        raise RuntimeError("device status reports a timed-out wait in a probe")
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -321,6 +389,11 @@ def run_ours(args):
             "ai_algorithmic": rl.gemm_ai(M, N, K),
             "ridge_ai": rl.ridge_ai(fp32_peak, bw / 1e3),
             "hbm_gbs_measured": bw}
+    probes = measure_probes(lib, dev, stream)
+    roof["peak_ffma_probe"] = probes["fp32_fma_tflops"]
+    roof["frac_ffma_probe"] = achieved / probes["fp32_fma_tflops"]
+    roof["peak_ffma_probe_basis"] = ("t2s_probe_fp32_fma: fma.rn.f32x2 chains only, 8 warps per "
+                                     "SM, best of 5 launches (measured, burst)")
     if clocks and clocks.get("sm_mhz"):
         at_clock = rl.fp32_peak_tflops(mhz=clocks["sm_mhz"])
         roof["peak_at_observed_clock"] = at_clock
@@ -358,7 +431,8 @@ def run_ours(args):
 
     # ---- reported separately: 3xTF32 tensor-core kernel and the 1024^3 shape
     if not args.skip_extras:
-        line["tf32x3"] = extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws)
+        line["tf32x3"] = extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws,
+                                      probes["tf32_mma_tflops"])
         line["bf16"] = extra_half(lib, M, N, K, stream, flush, args, dev, "bf16")
         line["f16"] = extra_half(lib, M, N, K, stream, flush, args, dev, "f16")
         line["f64"] = extra_f64(lib, stream, flush, args, dev)
@@ -369,6 +443,8 @@ def run_ours(args):
         rate, info = cpu_oracle_rate(A, B, float(os.environ.get("T2S_CPU_SECONDS", "12")))
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": info["cores"],
                                 "kind": "oracle", "sample": info["sample"]}
+        line["cpu_baseline_blocked"] = cpu_blocked_rate(A, B)
+        line["cpu_literal_loop_1024"] = cpu_literal_loop_1024()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -376,7 +452,7 @@ def run_ours(args):
     return 0
 
 
-def extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws):
+def extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws, tf32_probe=None):
     import torch
     from roofline_driven_tiling_gb300 import binding
     from roofline_driven_tiling_gb300 import roofline as rl
@@ -397,16 +473,21 @@ def extra_tf32x3(lib, dA, dB, M, N, K, stream, flush, args, dev, ws):
         return {"unavailable": str(e)}
     flops = rl.gemm_flops(M, N, K)
     t = sum(times) / len(times) / 1e3
-    peaks = measured_peaks()
-    # TF32 dense peak: the measured bf16 burst figure x the nominal tf32 : bf16 ratio (1.1 : 2.25).
-    tf32_peak = float(peaks.get("bf16_tflops", 1898.5)) * 1.1 / 2.25
+    if tf32_probe:
+        tf32_peak = tf32_probe
+        basis = ("t2s_probe_tf32_mma: back-to-back tcgen05.mma kind::tf32 M128 N256 K8 on "
+                 "shared-memory operands, one CTA per SM (measured, burst)")
+    else:
+        # Fallback: the measured bf16 burst figure x the nominal tf32 : bf16 ratio (1.1 : 2.25).
+        tf32_peak = float(measured_peaks().get("bf16_tflops", 1898.5)) * 1.1 / 2.25
+        basis = "measured bf16 burst x 1.1/2.25 (nominal tf32:bf16)"
     return {"value": flops / t / 1e12, "unit": UNIT, "ms_per_step": t * 1e3,
             "kernel": "t2s_gemm_f32_tf32x3 (split pre-pass + tcgen05 kind::tf32, 3 MMAs)",
             "roofline": {"bound": "tensor", "achieved_effective": flops / t / 1e12,
                          "tensor_flops_per_launch": 3 * flops,
                          "achieved_tensor": 3 * flops / t / 1e12, "peak": tf32_peak,
                          "frac": 3 * flops / t / 1e12 / tf32_peak, "unit": UNIT,
-                         "peak_basis": "measured bf16 burst x 1.1/2.25 (nominal tf32:bf16)",
+                         "peak_basis": basis,
                          "traffic": profile_traffic(TF32X3_PROFILE, "tf32x3")}}
 
 

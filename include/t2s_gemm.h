@@ -356,6 +356,28 @@ int t2s_last_cuda_error(void);
  */
 int t2s_selftest_wait_timeout(int64_t limit_ns, t2s_stream_t stream);
 
+/*
+ * Throughput probes: the measured ceilings of the roofline (page "4주차: Roofline과 Tiling",
+ * section "2. Roofline": a kernel's attainable performance is min(peak FLOP/s, bandwidth x
+ * arithmetic intensity); the pages give no GB300 peaks, so they are measured). Each launches
+ * one kernel on `stream` and stores in *flops (host memory) the floating-point operations it
+ * performs; the caller times the launch (CUDA events on `stream`) and divides.
+ *  - t2s_probe_fp32_fma: every thread of 2 CTAs of 128 threads per SM (the product kernels'
+ *    8 warps per SM) runs `iters` rounds of 16 independent packed fused multiply-adds
+ *    (fma.rn.f32x2, 4 FLOP each) with no memory traffic. iters in [1, 2^24].
+ *  - t2s_probe_tf32_mma: one CTA per SM issues `iters` x 4 back-to-back tcgen05.mma
+ *    kind::tf32 of M = 128, N = 256, K = 8 (2 x 128 x 256 x 8 FLOP each) on operands resident
+ *    in shared memory, accumulating in TMEM: the instruction and operand layout of the 3xTF32
+ *    product. iters in [1, 2^16]; the wait for the MMAs is bounded (T2S_ERR_TIMEOUT through
+ *    t2s_device_status).
+ * `out` is a DEVICE buffer of at least t2s_probe_outputs() floats (one value per thread,
+ * written so that the work is observable). Returns T2S_OK, T2S_ERR_INVALID (iters out of
+ * range, NULL pointer) or T2S_ERR_CUDA.
+ */
+int t2s_probe_outputs(void);
+int t2s_probe_fp32_fma(int64_t iters, float *out, int64_t *flops, t2s_stream_t stream);
+int t2s_probe_tf32_mma(int64_t iters, float *out, int64_t *flops, t2s_stream_t stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int t2s_version(void);
 

@@ -54,6 +54,9 @@ SIGNATURES = {
     "t2s_device_status": ([_p], _i),
     "t2s_last_cuda_error": ([], _i),
     "t2s_selftest_wait_timeout": ([_i64, _p], _i),
+    "t2s_probe_outputs": ([], _i),
+    "t2s_probe_fp32_fma": ([_i64, _p, _p, _p], _i),
+    "t2s_probe_tf32_mma": ([_i64, _p, _p, _p], _i),
     "t2s_version": ([], _i),
 }
 
@@ -189,6 +192,21 @@ def t2s_selftest_wait_timeout(limit_ns: int, stream=0) -> int:
 
 def t2s_version() -> int:
     return lib().t2s_version()
+
+
+def t2s_probe_outputs() -> int:
+    return lib().t2s_probe_outputs()
+
+
+def probe(kind: str, iters: int, out_ptr: int, stream=0) -> int:
+    """Launches a throughput probe ("fp32_fma" or "tf32_mma") on `stream`; returns the FLOPs
+    of the launch (raises T2SError on a bad status)."""
+    flops = ctypes.c_int64(0)
+    fn = lib().t2s_probe_fp32_fma if kind == "fp32_fma" else lib().t2s_probe_tf32_mma
+    rc = fn(iters, out_ptr, ctypes.addressof(flops), stream)
+    if rc != T2S_OK:
+        raise T2SError(rc, "t2s_probe_" + kind)
+    return int(flops.value)
 
 
 status_string = t2s_status_string

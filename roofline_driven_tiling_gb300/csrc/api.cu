@@ -366,6 +366,28 @@ int t2s_selftest_wait_timeout(int64_t limit_ns, t2s_stream_t stream) {
   return e == cudaSuccess ? T2S_OK : fail_cuda(e);
 }
 
+int t2s_probe_outputs(void) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return 256 * sms;
+}
+
+int t2s_probe_fp32_fma(int64_t iters, float* out, int64_t* flops, t2s_stream_t stream) {
+  if (iters < 1 || iters > (1LL << 24) || out == nullptr || flops == nullptr) return T2S_ERR_INVALID;
+  const cudaError_t e = launch_ffma_probe(iters, out, reinterpret_cast<cudaStream_t>(stream), flops);
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
+int t2s_probe_tf32_mma(int64_t iters, float* out, int64_t* flops, t2s_stream_t stream) {
+  if (iters < 1 || iters > (1LL << 16) || out == nullptr || flops == nullptr) return T2S_ERR_INVALID;
+  unsigned* word = nullptr;
+  cudaError_t e = status_word(&word);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_tf32_mma_probe(iters, out, word, reinterpret_cast<cudaStream_t>(stream), flops);
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
 int t2s_gemm_f32_plan(int64_t M, int64_t N, int64_t K, int sms) {
   if (M < 0 || N < 0 || K < 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return -1;
   if (sms < 1) return -1;

@@ -78,6 +78,10 @@ cudaError_t launch_naive_f64(int64_t M, int64_t N, int64_t K, const double* A, c
 cudaError_t launch_smem32_f64(int64_t M, int64_t N, int64_t K, const double* A, const double* B,
                               double* C, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
+// Throughput probes (probes.cu); *flops receives the FLOPs of the launch.
+cudaError_t launch_ffma_probe(int64_t iters, float* out, cudaStream_t stream, int64_t* flops);
+cudaError_t launch_tf32_mma_probe(int64_t iters, float* out, unsigned* status, cudaStream_t stream,
+                                  int64_t* flops);
 // Records a CUDA error for t2s_last_cuda_error() on this host thread.
 void set_last_cuda_error(cudaError_t e);
 

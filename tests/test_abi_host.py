@@ -184,3 +184,18 @@ def test_streamk_arguments(lib):
     assert f(-1, 4, 4, fake, fake + 64, fake + 128, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
     assert f(4, 4, 4, fake, fake + 64, fake, fake, 1 << 20, 0) == binding.T2S_ERR_INVALID
     assert f(0, 4, 4, 0, fake + 64, 0, 0, 0, 0) == binding.T2S_OK
+
+
+def test_probes_reject_bad_arguments(lib):
+    """The throughput probes check their arguments before touching a device."""
+    import ctypes
+    flops = ctypes.c_int64(0)
+    fake = 1 << 20  # never dereferenced: the checks come first
+    fp = ctypes.addressof(flops)
+    assert lib.t2s_probe_fp32_fma(0, fake, fp, 0) == binding.T2S_ERR_INVALID
+    assert lib.t2s_probe_fp32_fma((1 << 24) + 1, fake, fp, 0) == binding.T2S_ERR_INVALID
+    assert lib.t2s_probe_fp32_fma(10, None, fp, 0) == binding.T2S_ERR_INVALID
+    assert lib.t2s_probe_fp32_fma(10, fake, None, 0) == binding.T2S_ERR_INVALID
+    assert lib.t2s_probe_tf32_mma(0, fake, fp, 0) == binding.T2S_ERR_INVALID
+    assert lib.t2s_probe_tf32_mma((1 << 16) + 1, fake, fp, 0) == binding.T2S_ERR_INVALID
+    assert lib.t2s_probe_tf32_mma(10, None, fp, 0) == binding.T2S_ERR_INVALID
