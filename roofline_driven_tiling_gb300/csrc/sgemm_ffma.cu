@@ -108,27 +108,28 @@ struct GenRing {
 };
 
 // One stage of the general path: the BM x BK block of A at (m0, k0) and the BK x BN block of B
-// at (k0, n0), copied by every thread of the CTA with 4-byte cp.async into the same
-// shared-memory image the TMA path writes (A K-major with the 128-byte swizzle, B as stored),
-// zeros for rows >= M, k >= kend and columns >= N. Warp w copies the A rows w, w + WARPS, ...
-// (lane = k, one instruction per row); the threads copy B rows THREADS / BN at a time (thread
-// t: column t % BN). A stage wholly inside the matrices takes no bounds checks. The thread
-// arrives on the stage's full barrier once its copies have landed.
-template <class Cfg>
+// at (k0, n0), copied with 4-byte cp.async by the NT threads of a copy group (t = 0 .. NT - 1:
+// every thread of the CTA, or its producer warps) into the same shared-memory image the TMA
+// path writes (A K-major with the 128-byte swizzle, B as stored), zeros for rows >= M,
+// k >= kend and columns >= N. Warp w of the group copies the A rows w, w + NT / 32, ... (lane =
+// k, one instruction per row); the group copies B rows NT / BN at a time (thread t: column
+// t % BN). A stage wholly inside the matrices takes no bounds checks. The thread arrives on the
+// stage's full barrier once its copies have landed.
+template <class Cfg, int NT>
 __device__ __forceinline__ void gen_copy_stage(const float* __restrict__ A,
                                                const float* __restrict__ B, int M, int N, int K,
                                                int kend, int m0, int n0, int k0, uint32_t a_dst,
-                                               uint32_t b_dst, uint32_t full_bar) {
+                                               uint32_t b_dst, uint32_t full_bar, int t) {
+  constexpr int NW = NT / 32;
   static_assert(Cfg::BK == 32, "one warp instruction per A row");
-  static_assert(Cfg::BM % Cfg::WARPS == 0 && Cfg::THREADS % Cfg::BN == 0, "copy mapping");
-  constexpr int A_ROWS = Cfg::BM / Cfg::WARPS;    // A rows per warp
-  constexpr int B_STEP = Cfg::THREADS / Cfg::BN;  // B rows per pass of the CTA
+  static_assert(NT % 32 == 0 && Cfg::BM % NW == 0 && NT % Cfg::BN == 0, "copy mapping");
+  constexpr int A_ROWS = Cfg::BM / NW;   // A rows per warp
+  constexpr int B_STEP = NT / Cfg::BN;   // B rows per pass of the group
   constexpr int B_PASSES = Cfg::BK / B_STEP;
-  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
-  const int bcol = static_cast<int>(threadIdx.x) % Cfg::BN;
-  const int brow = static_cast<int>(threadIdx.x) / Cfg::BN;
-  // This thread's first A element and destination (row `warp`, k = k0 + lane), and its first
-  // B element (row k0 + brow, column n0 + bcol).
+  const int warp = t >> 5, lane = t & 31;
+  const int bcol = t % Cfg::BN, brow = t / Cfg::BN;
+  // This thread's first A element (row `warp`, k = k0 + lane) and first B element (row
+  // k0 + brow, column n0 + bcol).
   const float* a_src = A + static_cast<int64_t>(m0 + warp) * K + (k0 + lane);
   const float* b_src = B + static_cast<int64_t>(k0 + brow) * N + (n0 + bcol);
   const uint32_t b_dst0 = b_dst + static_cast<uint32_t>((brow * Cfg::BN + bcol) * 4);
@@ -139,8 +140,8 @@ __device__ __forceinline__ void gen_copy_stage(const float* __restrict__ A,
   if (m0 + Cfg::BM <= M && k0 + Cfg::BK <= kend && n0 + Cfg::BN <= N) {
 #pragma unroll
     for (int i = 0; i < A_ROWS; ++i) {
-      const int r = warp + Cfg::WARPS * i;
-      cp_async_4_full(a_dst + a_off(r), a_src + static_cast<int64_t>(Cfg::WARPS) * i * K);
+      const int r = warp + NW * i;
+      cp_async_4_full(a_dst + a_off(r), a_src + static_cast<int64_t>(NW) * i * K);
     }
 #pragma unroll
     for (int i = 0; i < B_PASSES; ++i)
@@ -153,9 +154,9 @@ __device__ __forceinline__ void gen_copy_stage(const float* __restrict__ A,
     const int rows_left = M - m0 - warp;
 #pragma unroll
     for (int i = 0; i < A_ROWS; ++i) {
-      const int r = warp + Cfg::WARPS * i;
-      const bool v = k_ok && Cfg::WARPS * i < rows_left;
-      cp_async_4(a_dst + a_off(r), v ? a_src + static_cast<int64_t>(Cfg::WARPS) * i * K : A,
+      const int r = warp + NW * i;
+      const bool v = k_ok && NW * i < rows_left;
+      cp_async_4(a_dst + a_off(r), v ? a_src + static_cast<int64_t>(NW) * i * K : A,
                  v ? 4u : 0u);
     }
     const bool n_ok = n0 + bcol < N;
@@ -169,6 +170,24 @@ __device__ __forceinline__ void gen_copy_stage(const float* __restrict__ A,
   }
   cp_async_arrive_noinc(full_bar);
 }
+
+// The general path with producer warps, for the 8-warp tiles that run one CTA per SM and
+// leave registers for 4 more warps: the producers make every copy, S stages ahead, and the
+// compute warps only wait for stages to land. Ring depth: the most stages up to 6 that fit.
+constexpr int kProducerThreads = 128;
+template <class Cfg>
+struct WsRing {
+  static constexpr int ringBytes(int s) { return s * Cfg::STAGE_BYTES + 2 * s * 8 + 1024; }
+  static constexpr int STAGES = ringBytes(6) <= 200 * 1024   ? 6
+                                : ringBytes(5) <= 200 * 1024 ? 5
+                                : ringBytes(4) <= 200 * 1024 ? 4
+                                                             : 3;
+  static constexpr int SMEM_BYTES = ringBytes(STAGES);
+  static constexpr int THREADS = Cfg::THREADS + kProducerThreads;
+  // The compute warps' registers (tiles of at most 64 accumulators per thread) plus the
+  // producers' must fit one CTA per SM.
+  static constexpr bool kUsable = Cfg::WARPS == 8 && Cfg::TM * Cfg::TN <= 64;
+};
 
 // One TMA stage: a BM x BK box of A and a BK x BN box of B, completion counted in bytes.
 template <class Cfg>
@@ -501,8 +520,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
   __syncthreads();
   // Prologue: stages 0 .. S - 2 (slot S - 1 is filled after the first K block).
   for (int kb = 0; kb < S - 1 && kb < nkb; ++kb)
-    gen_copy_stage<Cfg>(A, B, M, N, K, kend, m0, n0, kbeg + kb * Cfg::BK, a_stage(kb),
-                        b_stage(kb), full(kb));
+    gen_copy_stage<Cfg, Cfg::THREADS>(A, B, M, N, K, kend, m0, n0, kbeg + kb * Cfg::BK,
+                                      a_stage(kb), b_stage(kb), full(kb),
+                                      static_cast<int>(threadIdx.x));
 
   const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
   const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
@@ -545,9 +565,102 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
         asm volatile("cp.async.wait_all;" ::: "memory");
         return;
       }
-      gen_copy_stage<Cfg>(A, B, M, N, K, kend, m0, n0, kbeg + nk * Cfg::BK, a_stage(ns),
-                          b_stage(ns), full(ns));
+      gen_copy_stage<Cfg, Cfg::THREADS>(A, B, M, N, K, kend, m0, n0, kbeg + nk * Cfg::BK,
+                                        a_stage(ns), b_stage(ns), full(ns),
+                                        static_cast<int>(threadIdx.x));
     }
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  store_tile<Cfg>(acc, C, M, N, m0 + wm0 + g, n0 + wn0 + 4 * h, vec_store);
+}
+
+// The general path with producer warps (WsRing<Cfg>::kUsable configurations): warps
+// 0 .. WARPS - 1 compute as in the TMA kernel; warps WARPS .. WARPS + 3 copy stage j into ring
+// slot j % S once every compute warp is done with stage j - S (an empty barrier counting compute
+// warps), then arrive on the slot's full barrier (counting producer threads) when their copies
+// land. A compute warp never waits for another, only for its stages to land.
+template <class Cfg>
+__global__ void __launch_bounds__(WsRing<Cfg>::THREADS, 1)
+    sgemm_ffma_general_ws_kernel(const __grid_constant__ CUtensorMap tmA,
+                                 const __grid_constant__ CUtensorMap tmB,
+                                 const float* __restrict__ A, const float* __restrict__ B,
+                                 float* __restrict__ C, int M, int N, int K, int tiles_m,
+                                 int tiles_n, unsigned* status, int vec_store, int k_chunk,
+                                 int64_t c_plane, int wbm, int wbn, int tile_off, int dm, int dn,
+                                 int k_base, int accumulate) {
+  (void)tmA;
+  (void)tmB;
+  constexpr int S = WsRing<Cfg>::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sA = base;
+  const uint32_t sB = sA + S * Cfg::A_STAGE_BYTES;
+  const uint32_t sBar = sB + S * Cfg::B_STAGE_BYTES;  // full[S], empty[S]
+  auto full = [&](int s) { return sBar + 8u * s; };
+  auto empty = [&](int s) { return sBar + 8u * (S + s); };
+  auto a_stage = [&](int s) { return sA + static_cast<uint32_t>(s) * Cfg::A_STAGE_BYTES; };
+  auto b_stage = [&](int s) { return sB + static_cast<uint32_t>(s) * Cfg::B_STAGE_BYTES; };
+
+  int m0, n0, kbeg, kend;
+  if (!cta_work<Cfg>(M, N, K, tiles_m, tiles_n, wbm, wbn, tile_off, dm, dn, k_chunk, k_base, m0,
+                     n0, kbeg, kend))
+    return;
+  C += static_cast<int64_t>(blockIdx.y) * c_plane;
+  const int nkb = (kend - kbeg + Cfg::BK - 1) / Cfg::BK;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), static_cast<uint32_t>(kProducerThreads));
+      mbar_init(empty(s), static_cast<uint32_t>(Cfg::WARPS));
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp >= Cfg::WARPS) {
+    // ------------------------------------------------ producers
+    const int t = static_cast<int>(threadIdx.x) - Cfg::THREADS;
+    for (int j = 0; j < nkb; ++j) {
+      const int s = j % S;
+      if (j >= S) {
+        const bool freed = mbar_wait_bounded(empty(s), static_cast<uint32_t>((j - S) / S) & 1u, status);
+        if (!__all_sync(0xffffffffu, freed)) break;
+      }
+      gen_copy_stage<Cfg, kProducerThreads>(A, B, M, N, K, kend, m0, n0, kbeg + j * Cfg::BK,
+                                            a_stage(s), b_stage(s), full(s), t);
+    }
+    // None of this thread's copies lands after it exits.
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
+
+  // ------------------------------------------------ compute warps
+  const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
+  const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
+  const int g = lane >> 2, h = lane & 3;
+
+  uint64_t acc[Cfg::TM][Cfg::TN / 2];
+  if (accumulate) {
+    load_tile<Cfg>(acc, C, M, N, m0 + wm0 + g, n0 + wn0 + 4 * h, vec_store);
+  } else {
+#pragma unroll
+    for (int i = 0; i < Cfg::TM; ++i)
+#pragma unroll
+      for (int j = 0; j < Cfg::TN / 2; ++j) acc[i][j] = 0ull;  // two +0.0f
+  }
+  const uint32_t a_row0 = static_cast<uint32_t>((wm0 + g) * Cfg::A_ROW_BYTES);
+  const uint32_t xr = (a_row0 >> 7) & Cfg::SWZ_MASK;
+  const uint32_t b_col0 = static_cast<uint32_t>((wn0 + 4 * h) * 4);
+
+  for (int kb = 0; kb < nkb; ++kb) {
+    const int s = kb % S;
+    const bool landed = mbar_wait_bounded(full(s), static_cast<uint32_t>(kb / S) & 1u, status);
+    if (!__all_sync(0xffffffffu, landed)) return;  // compute warps issue no copies
+    ffma_kblock<Cfg>(acc, a_stage(s) + a_row0, b_stage(s) + b_col0, xr);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(s));
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -583,8 +696,25 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
     e = encode_tmap_f32_2d(&tb, p.B, p.N, p.K, Cfg::BN, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
   }
-  auto kern = kTma ? sgemm_ffma_kernel<Cfg> : sgemm_ffma_general_kernel<Cfg>;
-  const int smem = kTma ? Cfg::SMEM_BYTES : GenRing<Cfg>::SMEM_BYTES;
+  // The kernel of this path; only the ones a configuration can run are instantiated.
+  using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const float*, const float*, float*,
+                          int, int, int, int, int, unsigned*, int, int, int64_t, int, int, int,
+                          int, int, int, int);
+  Kernel kern;
+  int smem, threads;
+  if constexpr (kTma) {
+    kern = sgemm_ffma_kernel<Cfg>;
+    smem = Cfg::SMEM_BYTES;
+    threads = Cfg::THREADS;
+  } else if constexpr (WsRing<Cfg>::kUsable) {
+    kern = sgemm_ffma_general_ws_kernel<Cfg>;
+    smem = WsRing<Cfg>::SMEM_BYTES;
+    threads = WsRing<Cfg>::THREADS;
+  } else {
+    kern = sgemm_ffma_general_kernel<Cfg>;
+    smem = GenRing<Cfg>::SMEM_BYTES;
+    threads = Cfg::THREADS;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int wbm = part.wbm > 0 ? part.wbm : Cfg::BM, wbn = part.wbn > 0 ? part.wbn : Cfg::BN;
@@ -606,7 +736,7 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
   const int chunk = part.kc > 0 ? static_cast<int>(part.kc)
                     : splits == 1 ? static_cast<int>(p.K) : k_chunk;
   const dim3 grid(static_cast<unsigned>(count * dm * dn), static_cast<unsigned>(splits));
-  kern<<<grid, Cfg::THREADS, smem, p.stream>>>(
+  kern<<<grid, threads, smem, p.stream>>>(
       ta, tb, p.A, p.B, c, static_cast<int>(p.M), static_cast<int>(p.N), static_cast<int>(p.K),
       static_cast<int>(tiles_m), static_cast<int>(tiles_n), p.status, vec_store, chunk,
       p.M * p.N, wbm, wbn, static_cast<int>(part.off), dm, dn, static_cast<int>(part.k0),
