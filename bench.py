@@ -50,7 +50,8 @@ PLAN_NAMES = {0: "128x128x32 tiles", 1: "128x128x32 tiles, compact k loop", 2: "
               5: "256x128x32 tiles in whole rounds over the SMs, the rest as 64x64x32 tiles "
                  "in a second launch", 6: "128x128x32 tiles of 8 warps",
               7: "128x64x32 tiles of 8 warps", 8: "128x128x32 tiles on a persistent grid",
-              9: "56x128x32 tiles of 8 warps", 10: "32x32x32 tiles"}
+              9: "56x128x32 tiles of 8 warps", 10: "32x32x32 tiles",
+              11: "256x128x32 tiles on a persistent grid with TMA stores of C"}
 
 KERNEL_SOURCES = {
     "ffma": ["sgemm_ffma.cu", "t2s_device.cuh"],

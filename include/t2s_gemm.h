@@ -104,7 +104,10 @@ int t2s_gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B
  *    tiles of 8 warps (6, 7 and 9 only for at most one tile per multiprocessor); 8: 128 x 128
  *    tiles on a persistent grid of two CTAs per multiprocessor, one TMA ring across tiles
  *    (K <= 32; on the cp.async path the call runs 1 instead); 10: 32 x 32 tiles (small
- *    products). -1 if a dimension is negative or above T2S_MAX_DIM, or sms < 1.
+ *    products); 11: 256 x 128 tiles on a persistent grid of one CTA per multiprocessor whose
+ *    warps hand C to TMA stores while they go on to the next tile (K <= 96 and at least two
+ *    rounds of such tiles; on the cp.async path, or when C is not 16-byte aligned, the call
+ *    runs 1 instead). -1 if a dimension is negative or above T2S_MAX_DIM, or sms < 1.
  */
 int t2s_gemm_f32_plan(int64_t M, int64_t N, int64_t K, int sms);
 

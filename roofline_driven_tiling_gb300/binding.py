@@ -362,6 +362,7 @@ PLAN_NAMES = {
     8: "128x128 tiles on a persistent grid",
     9: "56x128 tiles of 8 warps",
     10: "32x32 tiles",
+    11: "256x128 tiles on a persistent grid with TMA stores of C",
 }
 
 

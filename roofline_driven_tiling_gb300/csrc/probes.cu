@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Zero operands, made visible to the tensor core (async proxy).
   for (uint32_t off = threadIdx.x * 16u; off < kProbeA + kProbeB; off += kMmaThreads * 16u)
-    tc::st_shared_v4(sA + off, 0u, 0u, 0u, 0u);
-  tc::fence_proxy_async_smem();
+    st_shared_v4(sA + off, 0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     mbar_fence_init();

@@ -667,6 +667,146 @@ __global__ void __launch_bounds__(WsRing<Cfg>::THREADS, 1)
   store_tile<Cfg>(acc, C, M, N, m0 + wm0 + g, n0 + wn0 + 4 * h, vec_store);
 }
 
+// Persistent product with a TMA-store epilogue, for short K, where storing C takes about as
+// long as the multiply-adds (a 16384 x 16384 C is 1 GB): one CTA per SM walks tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ... of the grouped order, and its TMA ring of S stages
+// runs on across tiles (iteration j of the CTA is K block j % nkb of its tile j / nkb, so the
+// last warp to finish with a slot refills it with iteration j + S). Each warp multiplies its
+// 64 x 64 part of a tile exactly as the product kernel does (one CTA per tile, k ascending: the
+// same bits), then copies its sums into its own 16 KB of shared memory (two 64-row x 32-column
+// boxes, 128-byte swizzle) and hands them to the TMA unit, which stores them while the warp
+// goes on to the next tile. Before reusing the boxes a warp waits until its previous stores
+// have read them; before exiting, until they are complete.
+template <class Cfg, int S>
+struct PStore {
+  static_assert(Cfg::WM == 64 && Cfg::WN == 64, "64 x 64 warp tiles: two 64 x 32 boxes each");
+  static constexpr int BOX_BYTES = 64 * 128;
+  static constexpr int STAGING_BYTES = Cfg::WARPS * 2 * BOX_BYTES;
+  static constexpr int SMEM_BYTES =
+      S * Cfg::STAGE_BYTES + STAGING_BYTES + 2 * S * 8 + S * 4 + 1024;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
+};
+
+template <class Cfg, int S>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    sgemm_ffma_pstore_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmC, int M, int N, int K,
+                             int tiles_m, int tiles_n, unsigned* status) {
+  using P = PStore<Cfg, S>;
+  (void)M;
+  (void)N;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sA = base;
+  const uint32_t sB = sA + S * Cfg::A_STAGE_BYTES;
+  const uint32_t sStg = sB + S * Cfg::B_STAGE_BYTES;  // 1024-byte aligned (stage sizes are)
+  const uint32_t sBar = sStg + P::STAGING_BYTES;      // full[S], then refill counters
+  const uint32_t sCnt = sBar + 16u * S;
+  auto full = [&](int s) { return sBar + 8u * s; };
+  auto a_stage = [&](int s) { return sA + static_cast<uint32_t>(s) * Cfg::A_STAGE_BYTES; };
+  auto b_stage = [&](int s) { return sB + static_cast<uint32_t>(s) * Cfg::B_STAGE_BYTES; };
+  auto origin = [&](int tile, int& m0, int& n0) {
+    constexpr int kGroup = 8;
+    const int per_group = kGroup * tiles_n;
+    const int first_m = (tile / per_group) * kGroup;
+    const int gsz = min(tiles_m - first_m, kGroup);
+    m0 = (first_m + (tile % per_group) % gsz) * Cfg::BM;
+    n0 = ((tile % per_group) / gsz) * Cfg::BN;
+  };
+  const int tiles = tiles_m * tiles_n;
+  const int nkb = (K + Cfg::BK - 1) / Cfg::BK;
+  const int my_tiles = (tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                       static_cast<int>(gridDim.x);
+  const int64_t iters = static_cast<int64_t>(my_tiles) * nkb;
+  // Loads iteration q of this CTA into ring slot s.
+  auto issue = [&](int64_t q, int s) {
+    int m0, n0;
+    origin(static_cast<int>(blockIdx.x + (q / nkb) * gridDim.x), m0, n0);
+    tma_stage<Cfg>(&tmA, &tmB, m0, n0, static_cast<int>(q % nkb) * Cfg::BK, a_stage(s),
+                   b_stage(s), full(s));
+  };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1u);
+      asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
+    }
+    mbar_fence_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+    for (int s = 0; s < S && s < iters; ++s) issue(s, s);
+  }
+  __syncthreads();
+
+  const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
+  const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
+  const int g = lane >> 2, h = lane & 3;
+  const uint32_t a_row0 = static_cast<uint32_t>((wm0 + g) * Cfg::A_ROW_BYTES);
+  const uint32_t xr = (a_row0 >> 7) & Cfg::SWZ_MASK;
+  const uint32_t b_col0 = static_cast<uint32_t>((wn0 + 4 * h) * 4);
+  const uint32_t stg = sStg + static_cast<uint32_t>(warp) * 2u * P::BOX_BYTES;
+  int64_t j = 0;  // iterations consumed
+  for (int t = 0; t < my_tiles; ++t) {
+    uint64_t acc[Cfg::TM][Cfg::TN / 2];
+#pragma unroll
+    for (int i = 0; i < Cfg::TM; ++i)
+#pragma unroll
+      for (int q = 0; q < Cfg::TN / 2; ++q) acc[i][q] = 0ull;  // two +0.0f
+    for (int kb = 0; kb < nkb; ++kb, ++j) {
+      const int s = static_cast<int>(j % S);
+      const bool landed = mbar_wait_bounded(full(s), static_cast<uint32_t>(j / S) & 1u, status);
+      if (!__all_sync(0xffffffffu, landed)) {
+        if (lane == 0) {
+          // Let copies already issued into this CTA's ring land, and this warp's stores
+          // complete, before leaving.
+          for (int64_t q = j; q < j + S && q < iters; ++q)
+            mbar_wait_bounded(full(static_cast<int>(q % S)), static_cast<uint32_t>(q / S) & 1u,
+                              status, 10000000ull);
+          bulk_wait_all();
+        }
+        return;
+      }
+      ffma_kblock<Cfg>(acc, a_stage(s) + a_row0, b_stage(s) + b_col0, xr);
+      __syncwarp();
+      if (lane == 0 && slot_done_count(sCnt + 4u * s) == Cfg::WARPS - 1) {
+        // The last warp to finish with this slot refills it with iteration j + S.
+        asm volatile("st.shared.u32 [%0], 0;" ::"r"(sCnt + 4u * s) : "memory");
+        if (j + S < iters) issue(j + S, s);
+      }
+    }
+    // Epilogue: once this warp's previous stores have read its boxes, rows g + 8i and column
+    // chunk h + 4q of its 64 x 64 part go to box q / 2, 16-byte chunk (h + 4 (q % 2)) ^ g of
+    // row g + 8i (the 128-byte swizzle; conflict-free).
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < Cfg::TM; ++i) {
+      const uint32_t row = static_cast<uint32_t>(g + 8 * i) * 128u;
+#pragma unroll
+      for (int q = 0; q < Cfg::TN / 4; ++q) {
+        const uint32_t chunk = static_cast<uint32_t>((h + 4 * (q % 2)) ^ g);
+        const float2 lo = unpack2(acc[i][2 * q]), hi = unpack2(acc[i][2 * q + 1]);
+        st_shared_v4(stg + static_cast<uint32_t>(q / 2) * P::BOX_BYTES + row + (chunk << 4),
+                     __float_as_uint(lo.x), __float_as_uint(lo.y), __float_as_uint(hi.x),
+                     __float_as_uint(hi.y));
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      int m0, n0;
+      origin(static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x), m0, n0);
+      // The TMA unit clips the boxes at the edges of C.
+      tma_store_2d(&tmC, stg, n0 + wn0, m0 + wm0);
+      tma_store_2d(&tmC, stg + P::BOX_BYTES, n0 + wn0 + 32, m0 + wm0);
+    }
+  }
+  // Every store has completed before the CTA's shared memory goes away.
+  if (lane == 0) bulk_wait_all();
+}
+
 // A run of the grouped tile order: tiles [off, off + count) of C cut into wbm x wbn tiles
 // (count < 0: to the end). Zero sizes stand for the configuration's own tile.
 struct TilePart {
@@ -813,7 +953,8 @@ enum class FfmaPick {
   kTall84 = 7,
   kPersistent = 8,
   kWide74 = 9,
-  kTiny24 = 10
+  kTiny24 = 10,
+  kPersistentStore = 11
 };
 
 // Picks the configuration whose busiest SM has the least work: ceil(tiles / SMs) tiles of the
@@ -831,6 +972,12 @@ enum class FfmaPick {
 // 6144^3 to 256 x 128 with the 64 x 64 tail). `copies` products of this size share the GPU;
 // they (and K < 256) keep to the one-launch configurations of at most 128 x 128. `cost`, when
 // given, receives the busiest SM's work per k value in the model's units (area / efficiency).
+// Measured against the one-launch tilings (L2 flushed): 16384^2 x 32 51.1 against 47.6 TFLOP/s,
+// 16384^2 x 16 25.4 against 23.5, 8192 x 4096 x 32 43.1 against 39.8, 8192^2 x 64 54.2
+// against 53.6, 6144^2 x 96 54.2 against 53.4; from K = 128 on the plain tiles win (8192^2 x
+// 128: 58.1 against 59.4).
+constexpr int64_t kPStoreMaxK = 96;
+
 FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, double* cost = nullptr) {
   struct Cand {
     FfmaPick pick;
@@ -903,6 +1050,12 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, double*
   // against 53.6).
   if (best == FfmaPick::kBigShortK && n_copies == 1 && K <= 32 && big_per_sm > 2)
     best = FfmaPick::kPersistent;
+  // Short K (at most three K blocks) with at least two rounds of 256 x 128 tiles: storing C
+  // takes about as long as the multiply-adds, and the persistent kernel with a TMA-store
+  // epilogue overlaps the two.
+  if (n_copies == 1 && K <= kPStoreMaxK &&
+      ((M + 255) / 256) * ((N + 127) / 128) >= 2 * static_cast<int64_t>(sms))
+    best = FfmaPick::kPersistentStore;
   if (cost != nullptr) *cost = best_cost;
   return best;
 }
@@ -917,6 +1070,9 @@ cudaError_t run_pick(FfmaPick pick, const Problem& p, Ts... args) {
     case FfmaPick::kTall84: return run_any<Tall84>(p, args...);
     case FfmaPick::kWide74: return run_any<Wide74>(p, args...);
     case FfmaPick::kTiny24: return run_any<Tiny24>(p, args...);
+    // The persistent grids run through their own launchers; a launch of tiles gets their tile.
+    case FfmaPick::kPersistent:
+    case FfmaPick::kPersistentStore: return run_any<BigShortK>(p, args...);
     default: return run_any<Small48>(p, args...);
   }
 }
@@ -961,7 +1117,12 @@ cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int6
   // choice for two copies (128 x 64).
   if (concurrent > 1)
     return run_pick(span >= 256 ? FfmaPick::kBig : FfmaPick::kBigShortK, p, 1, 0, nullptr, range);
-  const FfmaPick pick = pick_ffma(p.M, p.N, span, sms, 1);
+  FfmaPick pick = pick_ffma(p.M, p.N, span, sms, 1);
+  if (pick == FfmaPick::kPersistentStore) {
+    // Whole products on the TMA path with an aligned C; otherwise the product's own tiles.
+    if (kc == 0 && pstore_ok(p)) return launch_ffma_pstore(p);
+    pick = span >= 256 ? FfmaPick::kBig : FfmaPick::kBigShortK;
+  }
   if (pick == FfmaPick::kPersistent) {
     // The persistent loop covers whole products on the TMA path only.
     if (kc == 0 && tma_ok(p)) return launch_ffma_persistent(p);
@@ -1342,6 +1503,38 @@ cudaError_t launch_ffma_persistent(const Problem& p) {
       static_cast<int>(tiles_m), static_cast<int>(tiles_n), static_cast<int>(nkb),
       static_cast<int>(tiles), 0, p.status, vec_store);
   return cudaGetLastError();
+}
+
+// The persistent product with the TMA-store epilogue (sgemm_ffma_pstore_kernel): 256 x 128
+// tiles, one CTA per SM, 2 ring stages. TMA path only, and C 16-byte aligned.
+cudaError_t launch_ffma_pstore(const Problem& p) {
+  using Cfg = Huge;
+  constexpr int S = 2;
+  using P = PStore<Cfg, S>;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  CUtensorMap ta, tb, tc;
+  cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BK, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e == cudaSuccess) e = encode_tmap_f32_2d(&tb, p.B, p.N, p.K, Cfg::BN, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e == cudaSuccess) e = encode_tmap_f32_2d(&tc, p.C, p.N, p.M, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  auto kern = sgemm_ffma_pstore_kernel<Cfg, S>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES)) !=
+      cudaSuccess)
+    return e;
+  const int64_t tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
+  const int64_t tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
+  const int64_t tiles = tiles_m * tiles_n;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int64_t ctas = tiles < sms ? tiles : sms;
+  kern<<<static_cast<unsigned>(ctas), Cfg::THREADS, P::SMEM_BYTES, p.stream>>>(
+      ta, tb, tc, static_cast<int>(p.M), static_cast<int>(p.N), static_cast<int>(p.K),
+      static_cast<int>(tiles_m), static_cast<int>(tiles_n), p.status);
+  return cudaGetLastError();
+}
+
+bool pstore_ok(const Problem& p) {
+  return tma_ok(p) && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0;
 }
 
 cudaError_t launch_ffma_streamk(const Problem& p, float* workspace) {

@@ -61,6 +61,10 @@ cudaError_t launch_ffma_streamk(const Problem& p, float* workspace);
 // The product on a persistent grid (2 CTAs per SM, one TMA ring across tiles); TMA path
 // only (K % 4 == 0, N % 4 == 0, 16-byte aligned A and B). The bits of launch_ffma.
 cudaError_t launch_ffma_persistent(const Problem& p);
+// The persistent product with a TMA-store epilogue (256 x 128 tiles, one CTA per SM) for short
+// K; the bits of launch_ffma. Needs the TMA path and a 16-byte aligned C (pstore_ok).
+cudaError_t launch_ffma_pstore(const Problem& p);
+bool pstore_ok(const Problem& p);
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tf32x3(const Problem& p, void* workspace);
 // BF16 or FP16 operands (uint16_t bit patterns), FP32 C; workspace for the transposed/padded

@@ -479,7 +479,9 @@ DISPATCH_SHAPES = {
     "huge_tail_2500": (2500, 2000, 512),   # 160 tiles of 256 x 128: 152, then 8 as 64 x 64
     "huge_tail_4096": (4096, 4096, 1024),  # 512 tiles of 256 x 128: 456, then 56 as 64 x 64
     "big_short_k": (3072, 3072, 128),      # 576 tiles of 128^2, K < 256
-    "persistent_k32": (8192, 4096, 32),    # 2048 tiles of 128^2, one K block (cp.async: 1)
+    "persistent_k32": (2560, 2560, 32),    # 400 tiles of 128^2, one K block (cp.async: 1)
+    "pstore_k32": (8192, 4096, 32),        # 1024 tiles of 256 x 128, TMA stores (cp.async: 1)
+    "pstore_k96": (3000, 4100, 96),        # 384 tiles of 256 x 128, ragged edges of C
     "tall88_1792": (1792, 1792, 512),      # 392 tiles of 128 x 64: 8 x 8 per thread, pipelined
     "tall84_1152": (1152, 1024, 512),      # 144 tiles of 128 x 64, 8 warps of 8 x 4
     "wide74_1024": (1024, 1024, 512),      # 152 tiles of 56 x 128, 8 warps of 7 x 4

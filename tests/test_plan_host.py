@@ -9,8 +9,8 @@ import pytest
 
 from roofline_driven_tiling_gb300 import binding
 
-BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL, BIG88, TALL84, PERSISTENT, WIDE74, TINY24 = \
-    range(11)
+(BIG, BIG_SHORT_K, TALL88, SMALL48, HUGE, HUGE_TAIL, BIG88, TALL84, PERSISTENT, WIDE74, TINY24,
+ PERSISTENT_STORE) = range(12)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -51,10 +51,18 @@ def test_plan_matches_measured_winner(shape):
 def test_plan_short_k_and_copies():
     # K < 256 keeps to tiles of at most 128 x 128 with the compact k loop.
     assert binding.t2s_gemm_f32_plan(3072, 3072, 128, 152) == BIG_SHORT_K
-    assert binding.t2s_gemm_f32_plan(8192, 8192, 64, 152) == BIG_SHORT_K
-    # One K block per tile: the persistent grid (47.6 against 42.3 TFLOP/s at 16384^2 x 32).
-    assert binding.t2s_gemm_f32_plan(16384, 16384, 32, 152) == PERSISTENT
-    assert binding.t2s_gemm_f32_plan(16384, 16384, 33, 152) == BIG_SHORT_K
+    assert binding.t2s_gemm_f32_plan(8192, 8192, 128, 152) == BIG_SHORT_K
+    # At most three K blocks and two rounds of 256 x 128 tiles or more: the persistent grid
+    # with TMA stores of C (16384^2 x 32: 51.1 against 47.6 TFLOP/s; 8192^2 x 64: 54.2
+    # against 53.6).
+    assert binding.t2s_gemm_f32_plan(16384, 16384, 32, 152) == PERSISTENT_STORE
+    assert binding.t2s_gemm_f32_plan(8192, 8192, 64, 152) == PERSISTENT_STORE
+    assert binding.t2s_gemm_f32_plan(6144, 6144, 96, 152) == PERSISTENT_STORE
+    assert binding.t2s_gemm_f32_plan(8192, 8192, 97, 152) == BIG_SHORT_K
+    # One K block but fewer than two rounds of 256 x 128 tiles: the persistent grid of 128 x 128
+    # tiles (400 of them, 200 of 256 x 128).
+    assert binding.t2s_gemm_f32_plan(2560, 2560, 32, 152) == PERSISTENT
+    assert binding.t2s_gemm_f32_plan(2560, 2560, 33, 152) == BIG_SHORT_K
     # One tile row of 128: the 256-row tile would be half empty.
     assert binding.t2s_gemm_f32_plan(128, 131072, 288, 152) == BIG
 
@@ -134,7 +142,8 @@ def test_plan_names():
     assert binding.plan(1024, 1024, 1024, 152) == "56x128 tiles of 8 warps"
     assert binding.plan(1152, 1024, 512, 152) == "128x64 tiles of 8 warps"
     assert binding.plan(384, 384, 384, 152) == "32x32 tiles"
-    assert set(binding.PLAN_NAMES) == set(range(11))
+    assert binding.plan(16384, 16384, 32, 152) == "256x128 tiles on a persistent grid with TMA stores of C"
+    assert set(binding.PLAN_NAMES) == set(range(12))
     with pytest.raises(ValueError):
         binding.plan(-1, 4, 4, 152)
 
