@@ -677,23 +677,28 @@ __global__ void __launch_bounds__(WsRing<Cfg>::THREADS, 1)
 // boxes, 128-byte swizzle) and hands them to the TMA unit, which stores them while the warp
 // goes on to the next tile. Before reusing the boxes a warp waits until its previous stores
 // have read them; before exiting, until they are complete.
-template <class Cfg, int S>
+// PASSES: the warp stores its 64 x 64 part in that many passes of 64 / PASSES rows (two boxes
+// of 64 / PASSES rows x 32 columns each), so that its staging holds one pass; between passes
+// the warp waits until the previous pass's stores have read the boxes.
+template <class Cfg, int S, int PASSES>
 struct PStore {
-  static_assert(Cfg::WM == 64 && Cfg::WN == 64, "64 x 64 warp tiles: two 64 x 32 boxes each");
-  static constexpr int BOX_BYTES = 64 * 128;
+  static_assert(Cfg::WM == 64 && Cfg::WN == 64, "64 x 64 warp tiles: two 32-column boxes each");
+  static_assert(PASSES == 1 || PASSES == 2, "whole 8-row groups per pass");
+  static constexpr int ROWS = 64 / PASSES;
+  static constexpr int BOX_BYTES = ROWS * 128;
   static constexpr int STAGING_BYTES = Cfg::WARPS * 2 * BOX_BYTES;
   static constexpr int SMEM_BYTES =
       S * Cfg::STAGE_BYTES + STAGING_BYTES + 2 * S * 8 + S * 4 + 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
 };
 
-template <class Cfg, int S>
-__global__ void __launch_bounds__(Cfg::THREADS, 1)
+template <class Cfg, int S, int PASSES>
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
     sgemm_ffma_pstore_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC, int M, int N, int K,
                              int tiles_m, int tiles_n, unsigned* status) {
-  using P = PStore<Cfg, S>;
+  using P = PStore<Cfg, S, PASSES>;
   (void)M;
   (void)N;
   extern __shared__ uint8_t smem_raw[];
@@ -776,31 +781,37 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (j + S < iters) issue(j + S, s);
       }
     }
-    // Epilogue: once this warp's previous stores have read its boxes, rows g + 8i and column
-    // chunk h + 4q of its 64 x 64 part go to box q / 2, 16-byte chunk (h + 4 (q % 2)) ^ g of
-    // row g + 8i (the 128-byte swizzle; conflict-free).
-    if (lane == 0) bulk_wait_read_all();
-    __syncwarp();
+    // Epilogue, pass by pass: once this warp's previous stores have read its boxes, rows
+    // g + 8i of the pass and column chunk h + 4q of its 64 x 64 part go to box q / 2, 16-byte
+    // chunk (h + 4 (q % 2)) ^ g of row g + 8i within the pass (the 128-byte swizzle;
+    // conflict-free).
+    int m0, n0;
+    origin(static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x), m0, n0);
 #pragma unroll
-    for (int i = 0; i < Cfg::TM; ++i) {
-      const uint32_t row = static_cast<uint32_t>(g + 8 * i) * 128u;
+    for (int pass = 0; pass < PASSES; ++pass) {
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
 #pragma unroll
-      for (int q = 0; q < Cfg::TN / 4; ++q) {
-        const uint32_t chunk = static_cast<uint32_t>((h + 4 * (q % 2)) ^ g);
-        const float2 lo = unpack2(acc[i][2 * q]), hi = unpack2(acc[i][2 * q + 1]);
-        st_shared_v4(stg + static_cast<uint32_t>(q / 2) * P::BOX_BYTES + row + (chunk << 4),
-                     __float_as_uint(lo.x), __float_as_uint(lo.y), __float_as_uint(hi.x),
-                     __float_as_uint(hi.y));
+      for (int ii = 0; ii < Cfg::TM / PASSES; ++ii) {
+        const int i = pass * (Cfg::TM / PASSES) + ii;
+        const uint32_t row = static_cast<uint32_t>(g + 8 * ii) * 128u;
+#pragma unroll
+        for (int q = 0; q < Cfg::TN / 4; ++q) {
+          const uint32_t chunk = static_cast<uint32_t>((h + 4 * (q % 2)) ^ g);
+          const float2 lo = unpack2(acc[i][2 * q]), hi = unpack2(acc[i][2 * q + 1]);
+          st_shared_v4(stg + static_cast<uint32_t>(q / 2) * P::BOX_BYTES + row + (chunk << 4),
+                       __float_as_uint(lo.x), __float_as_uint(lo.y), __float_as_uint(hi.x),
+                       __float_as_uint(hi.y));
+        }
       }
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      int m0, n0;
-      origin(static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x), m0, n0);
-      // The TMA unit clips the boxes at the edges of C.
-      tma_store_2d(&tmC, stg, n0 + wn0, m0 + wm0);
-      tma_store_2d(&tmC, stg + P::BOX_BYTES, n0 + wn0 + 32, m0 + wm0);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        // The TMA unit clips the boxes at the edges of C.
+        const int y = m0 + wm0 + pass * P::ROWS;
+        tma_store_2d(&tmC, stg, n0 + wn0, y);
+        tma_store_2d(&tmC, stg + P::BOX_BYTES, n0 + wn0 + 32, y);
+      }
     }
   }
   // Every store has completed before the CTA's shared memory goes away.
@@ -1507,18 +1518,17 @@ cudaError_t launch_ffma_persistent(const Problem& p) {
 
 // The persistent product with the TMA-store epilogue (sgemm_ffma_pstore_kernel): 256 x 128
 // tiles, one CTA per SM, 2 ring stages. TMA path only, and C 16-byte aligned.
-cudaError_t launch_ffma_pstore(const Problem& p) {
-  using Cfg = Huge;
-  constexpr int S = 2;
-  using P = PStore<Cfg, S>;
+template <class Cfg, int S, int PASSES>
+cudaError_t launch_pstore(const Problem& p) {
+  using P = PStore<Cfg, S, PASSES>;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   CUtensorMap ta, tb, tc;
   cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BK, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e == cudaSuccess) e = encode_tmap_f32_2d(&tb, p.B, p.N, p.K, Cfg::BN, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (e == cudaSuccess) e = encode_tmap_f32_2d(&tc, p.C, p.N, p.M, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e == cudaSuccess) e = encode_tmap_f32_2d(&tc, p.C, p.N, p.M, 32, P::ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  auto kern = sgemm_ffma_pstore_kernel<Cfg, S>;
+  auto kern = sgemm_ffma_pstore_kernel<Cfg, S, PASSES>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES)) !=
       cudaSuccess)
     return e;
@@ -1526,12 +1536,19 @@ cudaError_t launch_ffma_pstore(const Problem& p) {
   const int64_t tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
   const int64_t tiles = tiles_m * tiles_n;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const int64_t ctas = tiles < sms ? tiles : sms;
+  const int64_t slots = static_cast<int64_t>(sms) * Cfg::MIN_BLOCKS;
+  const int64_t ctas = tiles < slots ? tiles : slots;
   kern<<<static_cast<unsigned>(ctas), Cfg::THREADS, P::SMEM_BYTES, p.stream>>>(
       ta, tb, tc, static_cast<int>(p.M), static_cast<int>(p.N), static_cast<int>(p.K),
       static_cast<int>(tiles_m), static_cast<int>(tiles_n), p.status);
   return cudaGetLastError();
 }
+
+// One CTA of 256 x 128 tiles per SM, staging whole warp parts. Measured alongside and not kept:
+// two CTAs of 128 x 128 tiles per SM staging half a warp part at a time (so that one CTA's
+// stores overlap the other's multiply-adds), 16384^2 x 32 47.5 against 51.1 TFLOP/s, 8192^2 x 64
+// 49.8 against 54.2; raster groups of 1, 2 or 32 tile rows instead of 8: within 2 %.
+cudaError_t launch_ffma_pstore(const Problem& p) { return launch_pstore<Huge, 2, 1>(p); }
 
 bool pstore_ok(const Problem& p) {
   return tma_ok(p) && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0;

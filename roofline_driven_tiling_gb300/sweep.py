@@ -1,6 +1,7 @@
 """Roofline sweep: every FP32 entry point over the sweep shapes, placed on the GB300 roofline.
 
     python -m roofline_driven_tiling_gb300.sweep [--iters 50] [--no-flush] [--out FILE]
+        [--shapes MxNxK,...] [--kernels ffma,...] [--splitk-chunks S] [--misalign]
 
 The pages this library follows time a GEMM at one size and read the result against the
 roofline (page "4주차: Roofline과 Tiling", sections "2. Roofline" and "실제 Kernel을 plot 해보면":
@@ -22,6 +23,10 @@ the ragged 1000 x 1003 x 997, for the product and the other FP32 entry points.
 * Each result is compared with the product's: bit for bit for the naive and smem32 kernels
   (the same fused multiply-adds in the same order), within 1e-6 K max|a| max|b| for the
   others. A mismatch is reported in the line and fails the run.
+* --shapes replaces the sweep's shapes (one small shape and one kernel make a short run that
+  a profiler can capture), --splitk-chunks fixes the split-K chunk count (0: the automatic
+  choice), and --misalign offsets A, B and C by one float so that every kernel takes its
+  general (non-TMA) load path.
 """
 from __future__ import annotations
 
@@ -48,9 +53,10 @@ def _hbm_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _calls(binding, lib, M, N, K, dA, dB, dC, ws, stream):
+def _calls(binding, lib, M, N, K, dA, dB, dC, ws, stream, chunks=0, shift=0):
     """One closure per entry point (the workspace tensor is large enough for all)."""
-    a, b, c, s = dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), stream
+    a, b, c, s = (dA.data_ptr() + 4 * shift, dB.data_ptr() + 4 * shift,
+                  dC.data_ptr() + 4 * shift, stream)
     w, wn = ws.data_ptr(), ws.numel()
 
     def check(rc, name):
@@ -61,7 +67,7 @@ def _calls(binding, lib, M, N, K, dA, dB, dC, ws, stream):
         "ffma": lambda: check(lib.t2s_gemm_f32(M, N, K, a, b, c, s), "t2s_gemm_f32"),
         "tf32x3": lambda: check(lib.t2s_gemm_f32_tf32x3(M, N, K, a, b, c, w, wn, s),
                                 "t2s_gemm_f32_tf32x3"),
-        "splitk": lambda: check(lib.t2s_gemm_f32_splitk(M, N, K, a, b, c, 0, w, wn, s),
+        "splitk": lambda: check(lib.t2s_gemm_f32_splitk(M, N, K, a, b, c, chunks, w, wn, s),
                                 "t2s_gemm_f32_splitk"),
         "streamk": lambda: check(lib.t2s_gemm_f32_streamk(M, N, K, a, b, c, w, wn, s),
                                  "t2s_gemm_f32_streamk"),
@@ -71,9 +77,9 @@ def _calls(binding, lib, M, N, K, dA, dB, dC, ws, stream):
     }
 
 
-def _workspace_bytes(lib, M, N, K):
+def _workspace_bytes(lib, M, N, K, chunks=0):
     return max(lib.t2s_gemm_f32_tf32x3_workspace_size(M, N, K),
-               lib.t2s_gemm_f32_splitk_workspace_size(M, N, K, 0),
+               lib.t2s_gemm_f32_splitk_workspace_size(M, N, K, chunks),
                lib.t2s_gemm_f32_streamk_workspace_size(M, N, K), 256)
 
 
@@ -101,7 +107,14 @@ def main(argv=None) -> int:
     ap.add_argument("--no-flush", action="store_true", help="time back-to-back calls")
     ap.add_argument("--kernels", default=",".join(KERNELS))
     ap.add_argument("--out", default=None, help="also write the JSON lines to this file")
+    ap.add_argument("--shapes", default=None, help="MxNxK[,MxNxK...] instead of the sweep")
+    ap.add_argument("--splitk-chunks", type=int, default=0, help="split-K chunks (0: automatic)")
+    ap.add_argument("--misalign", action="store_true",
+                    help="offset A, B and C by one float (the general load path)")
     args = ap.parse_args(argv)
+    shapes = SHAPES if not args.shapes else [tuple(int(x) for x in t.split("x"))
+                                             for t in args.shapes.split(",") if t]
+    shift = 1 if args.misalign else 0
 
     import torch
 
@@ -118,12 +131,18 @@ def main(argv=None) -> int:
     kernels = [k for k in args.kernels.split(",") if k]
     out = open(args.out, "w") if args.out else None
     rows, bad = [], 0
-    for (M, N, K) in SHAPES:
+    for (M, N, K) in shapes:
         A, B = inputs.uniform(M, K, SEED_A), inputs.uniform(K, N, SEED_B)
-        dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
-        dC = torch.empty((M, N), dtype=torch.float32, device=dev)
-        ws = torch.empty(_workspace_bytes(lib, M, N, K), dtype=torch.uint8, device=dev)
-        calls = _calls(binding, lib, M, N, K, dA, dB, dC, ws, stream.cuda_stream)
+        dA = torch.zeros(M * K + shift, dtype=torch.float32, device=dev)
+        dB = torch.zeros(K * N + shift, dtype=torch.float32, device=dev)
+        dA[shift:] = torch.from_numpy(A.ravel()).to(dev)
+        dB[shift:] = torch.from_numpy(B.ravel()).to(dev)
+        dC_buf = torch.empty(M * N + shift, dtype=torch.float32, device=dev)
+        dC = dC_buf[shift:].view(M, N)
+        ws = torch.empty(_workspace_bytes(lib, M, N, K, args.splitk_chunks), dtype=torch.uint8,
+                         device=dev)
+        calls = _calls(binding, lib, M, N, K, dA, dB, dC_buf, ws, stream.cuda_stream,
+                       args.splitk_chunks, shift)
         flops = rl.gemm_flops(M, N, K)
         tol = 1e-6 * K * float(abs(A).max()) * float(abs(B).max())
         ref = None
@@ -166,14 +185,14 @@ def main(argv=None) -> int:
             if out:
                 out.write(line + "\n")
             rows.append(rec)
-        del dA, dB, dC, ws
+        del dA, dB, dC, dC_buf, ws
         torch.cuda.empty_cache()
     if out:
         out.close()
     # Summary table: TFLOP/s (fraction of the roof) per shape and kernel.
     print("\n| shape | AI | roof | " + " | ".join(kernels) + " |")
     print("|---|---|---|" + "---|" * len(kernels))
-    for (M, N, K) in SHAPES:
+    for (M, N, K) in shapes:
         pts = {r["kernel"]: r for r in rows if r["shape"] == [M, N, K]}
         first = next(iter(pts.values()))
         cells = ["%.1f (%.0f %%)" % (pts[k]["tflops"], 100 * pts[k]["frac_of_roof"]) if k in pts
