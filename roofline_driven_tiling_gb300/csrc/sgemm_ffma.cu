@@ -783,8 +783,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
     }
     // Epilogue, pass by pass: once this warp's previous stores have read its boxes, rows
     // g + 8i of the pass and column chunk h + 4q of its 64 x 64 part go to box q / 2, 16-byte
-    // chunk (h + 4 (q % 2)) ^ g of row g + 8i within the pass (the 128-byte swizzle;
-    // conflict-free).
+    // chunk (h + 4 (q % 2)) ^ g of row g + 8i within the pass (the 128-byte swizzle). A
+    // 16-byte store is served a quarter-warp (lanes of g = 2t, 2t + 1) at a time, and those two
+    // rows' swizzles differ in bit 0 only, so at step q lanes of odd g store chunk q ^ 1 of the
+    // box instead of q: the eight lanes then fill the eight 16-byte bank groups once each.
     int m0, n0;
     origin(static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x), m0, n0);
 #pragma unroll
@@ -797,8 +799,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
         const uint32_t row = static_cast<uint32_t>(g + 8 * ii) * 128u;
 #pragma unroll
         for (int q = 0; q < Cfg::TN / 4; ++q) {
-          const uint32_t chunk = static_cast<uint32_t>((h + 4 * (q % 2)) ^ g);
-          const float2 lo = unpack2(acc[i][2 * q]), hi = unpack2(acc[i][2 * q + 1]);
+          const bool odd = (g & 1) != 0;
+          const int qq = q ^ 1;  // the other chunk of the same box
+          const uint64_t v0 = odd ? acc[i][2 * qq] : acc[i][2 * q];
+          const uint64_t v1 = odd ? acc[i][2 * qq + 1] : acc[i][2 * q + 1];
+          const int qs = odd ? qq : q;
+          const uint32_t chunk = static_cast<uint32_t>((h + 4 * (qs % 2)) ^ g);
+          const float2 lo = unpack2(v0), hi = unpack2(v1);
           st_shared_v4(stg + static_cast<uint32_t>(q / 2) * P::BOX_BYTES + row + (chunk << 4),
                        __float_as_uint(lo.x), __float_as_uint(lo.y), __float_as_uint(hi.x),
                        __float_as_uint(hi.y));
@@ -1547,7 +1554,10 @@ cudaError_t launch_pstore(const Problem& p) {
 // One CTA of 256 x 128 tiles per SM, staging whole warp parts. Measured alongside and not kept:
 // two CTAs of 128 x 128 tiles per SM staging half a warp part at a time (so that one CTA's
 // stores overlap the other's multiply-adds), 16384^2 x 32 47.5 against 51.1 TFLOP/s, 8192^2 x 64
-// 49.8 against 54.2; raster groups of 1, 2 or 32 tile rows instead of 8: within 2 %.
+// 49.8 against 54.2; raster groups of 1, 2 or 32 tile rows instead of 8: within 2 %; 128 x 256
+// tiles (1 KB of each C row per tile instead of 512 bytes): within 1 %. At K = 16 and 32 a tile
+// takes the same time (16384^2: 0.33 ms), so there the stores of C set the pace, at about
+// 3.25 TB/s, although plain writes reach 7.3 TB/s on GB300.
 cudaError_t launch_ffma_pstore(const Problem& p) { return launch_pstore<Huge, 2, 1>(p); }
 
 bool pstore_ok(const Problem& p) {
