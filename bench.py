@@ -87,11 +87,38 @@ def barrier():
         dist.barrier()
 
 
+def code_only(text: str) -> str:
+    """CUDA/C++ source with comments removed and whitespace collapsed: what the compiler sees,
+    so that a change of comments alone keeps a profile's recorded hash valid. String and
+    character literals are kept as they are (a "//" inside one is not a comment)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_hash(kind: str) -> str:
+    """First 16 hex digits of the SHA-256 of the kernel's sources, comments removed."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, "roofline_driven_tiling_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "roofline_driven_tiling_gb300", "csrc", name),
+                  encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

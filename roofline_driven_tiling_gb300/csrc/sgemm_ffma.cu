@@ -13,19 +13,28 @@
 //
 // GB300 design:
 //  * A STAGES-deep ring of shared-memory buffers per CTA, one "full" mbarrier per slot.
-//    There is no producer warp: every warp computes. CTA tiles run from 56 x 128 to
-//    256 x 128 of 4 or 8 warps, chosen per shape (pick_ffma), and an SM holds 8 warps,
-//    two per sub-partition, at up to 255 registers per thread for the largest register tile.
+//    On the TMA path there is no producer warp: every warp computes. CTA tiles run from
+//    32 x 32 to 256 x 128 of 4 or 8 warps, chosen per shape (pick_ffma), and an SM holds 8
+//    warps, two per sub-partition, at up to 255 registers per thread for the largest
+//    register tile.
 //  * Aligned case (K % 4 == 0, N % 4 == 0, 16-byte aligned pointers): the Tensor Memory
 //    Accelerator loads a BM x BK box of A and a BK x BN box of B per stage; elements
 //    outside the matrices are filled with zeros by the TMA unit, and completion is
 //    counted in transaction bytes on the full barrier. The last warp to finish reading a
 //    slot (a shared-memory counter per slot) issues the refill, so no warp ever blocks
 //    waiting for another to free a slot.
-//  * General case: every thread copies its share of a stage with 4-byte cp.async and zero
-//    fill, writing the same shared-memory image, and arrives on the full barrier when its
-//    copies land (cp.async.mbarrier.arrive.noinc); an "empty" barrier per slot tells the
-//    threads when all warps are done with a slot so it can be refilled.
+//  * General case (K or N not a multiple of 4, or A or B not 16-byte aligned: row strides
+//    TMA cannot take): stages are copied with 4-byte cp.async and zero fill into the same
+//    shared-memory image, a whole A row per warp instruction, and a copying thread arrives
+//    on the full barrier when its copies land (cp.async.mbarrier.arrive.noinc); an "empty"
+//    barrier per slot counts the warps done with it. The 8-warp tiles, which run one CTA
+//    per SM, add 4 producer warps that make every copy up to 6 stages ahead
+//    (sgemm_ffma_general_ws_kernel); the others copy with every thread, each warp
+//    refilling the slot of the previous K block after its current one
+//    (sgemm_ffma_general_kernel).
+//  * Short K (at most 3 K blocks, at least two rounds of 256 x 128 tiles): a persistent grid
+//    whose warps hand C to TMA stores while the ring loads the next tile
+//    (sgemm_ffma_pstore_kernel).
 //  * A is stored K-major as it is in global memory (TMA cannot transpose 4-byte
 //    elements). Rows of BK floats are XOR-swizzled in 16-byte chunks (the TMA
 //    128/64/32-byte swizzle), so that the 8 rows a warp reads at one k chunk fall in

@@ -56,3 +56,17 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The profile summaries record a hash of the kernel sources that bench.py checks before
+    reading their DRAM bytes; it is taken over the code with comments removed, so that a
+    comment edit keeps the counters valid while any change of code invalidates them."""
+    import bench
+    a = 'int f(int x) { // add one\n  return x + 1; /* done */ }\nconst char* s = "a // b";\n'
+    b = 'int f(int x) {\n  return x + 1;  }\n// a new comment\nconst char* s = "a // b";\n'
+    c = 'int f(int x) {\n  return x + 2;  }\nconst char* s = "a // b";\n'
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
+    assert '"a // b"' in bench.code_only(a)
+    assert len(bench.kernel_hash("ffma")) == 16
