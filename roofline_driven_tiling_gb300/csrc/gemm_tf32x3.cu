@@ -12,7 +12,9 @@
 //      B_big, B_small : N x Kp      (B is K x N row-major: transposed through shared memory)
 //    so that every tensor-map stride is a multiple of 128 bytes whatever K and N are.
 // 2. Product kernel, persistent: one CTA per SM (64 threads plus 4 epilogue warps per 128
-//    columns of the tile: 320 threads at BN = 224) walks 128 x BN tiles of C.
+//    columns of the tile: 320 threads at BN = 224) walks 128 x BN tiles of C; for large
+//    products, clusters of two CTAs on two SMs walk 256 x BN tiles with cta_group::2 MMAs
+//    (M 256, issued by the first CTA), each CTA staging half of the B planes.
 //      warp 0     -- TMA producer: per K block, one box of each of the four planes;
 //      warp 1     -- allocates TMEM, one lane issues tcgen05.mma kind::tf32 (M=128, N=BN,
 //                    K=8), three per k step into one FP32 accumulator in TMEM, in the order
@@ -150,6 +152,11 @@ using Tf32N128 = tc::TcConfig<tc::kTf32x3, 128, 32, 3, 256>;  // 3 stages of 64 
 using Tf32N192 = tc::TcConfig<tc::kTf32x3, 192, 16, 4, 256>;  // 4 stages of 40 KB, 8 epilogue warps
 using Tf32N224 = tc::TcConfig<tc::kTf32x3, 224, 16, 4, 256>;  // 4 stages of 44 KB, 8 epilogue warps
 using Tf32N256 = tc::TcConfig<tc::kTf32x3, 256, 16, 4, 256>;  // 4 stages of 48 KB, 8 epilogue warps
+// 256-row tiles on CTA pairs (tcgen05 cta_group::2, M 256): each CTA stages its 128 rows of the
+// A planes and half of the tile's rows of the B planes, so an SM's shared memory receives and
+// feeds a quarter fewer operand bytes per MMA; 6 stages (30 KB at 224 columns, 32 KB at 256).
+using Tf32P224 = tc::TcConfig<tc::kTf32x3, 224, 16, 6, 256, false, true>;
+using Tf32P256 = tc::TcConfig<tc::kTf32x3, 256, 16, 6, 256, false, true>;
 
 }  // namespace
 
@@ -188,17 +195,25 @@ cudaError_t launch_tf32x3(const Problem& p, void* workspace) {
                                                         b_small, p.M, p.N, p.K, Kp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  // Persistent CTAs take tiles in rounds of `sms`; the cost of a width is its number of
-  // rounds times its width, weighted by the per-tile efficiency measured on GB300 (narrow
-  // tiles re-read A more often: 128-wide tiles run about 15 % slower per FLOP than 256).
-  const int widths[4] = {128, 192, 224, 256};
-  const double weight[4] = {1.15, 1.03, 1.01, 1.0};
+  // Persistent CTAs take tiles in rounds of `sms` (CTA pairs: 256-row tiles in rounds of
+  // sms / 2); the cost of a configuration is its number of rounds times its width, weighted by
+  // the per-tile efficiency measured on GB300 (narrow tiles re-read A more often: 128-wide tiles
+  // run about 15 % slower per FLOP than 256; pairs, fed half of B per SM, about 6-7 % faster
+  // than single CTAs of the same width: 4096^3 0.510 against 0.541 ms per call, 8192^3 3.46
+  // against 3.75, 2048^3 0.089 against 0.091; with few tiles they leave SMs idle, 1024^3 0.045
+  // against 0.038).
+  const int widths[6] = {128, 192, 224, 256, 224, 256};
+  const bool pair[6] = {false, false, false, false, true, true};
+  const double weight[6] = {1.15, 1.03, 1.01, 1.0, 0.94, 0.93};
   const int64_t tm = (p.M + 127) / 128;
   int best = 0;
   double best_cost = 0.0;
-  for (int i = 0; i < 4; ++i) {
-    const int64_t tiles = tm * ((p.N + widths[i] - 1) / widths[i]);
-    const int64_t rounds = (tiles + sms - 1) / sms;
+  for (int i = 0; i < 6; ++i) {
+    if (pair[i] && (p.M <= 128 || p.K < 256)) continue;  // pairs need two tile rows
+    const int64_t rows = pair[i] ? (tm + 1) / 2 : tm;
+    const int64_t units = rows * ((p.N + widths[i] - 1) / widths[i]);
+    const int64_t slots = pair[i] ? sms / 2 : sms;
+    const int64_t rounds = (units + slots - 1) / slots;
     const double cost = static_cast<double>(rounds) * widths[i] * weight[i];
     if (i == 0 || cost < best_cost) {
       best = i;
@@ -210,6 +225,8 @@ cudaError_t launch_tf32x3(const Problem& p, void* workspace) {
     case 1: return tc::run_tc<Tf32N192>(p, a_big, a_small, b_big, b_small, Kp, Kp, Kp);
     case 2: return tc::run_tc<Tf32N224>(p, a_big, a_small, b_big, b_small, Kp, Kp, Kp);
     case 3: return tc::run_tc<Tf32N256>(p, a_big, a_small, b_big, b_small, Kp, Kp, Kp);
+    case 4: return tc::run_tc<Tf32P224>(p, a_big, a_small, b_big, b_small, Kp, Kp, Kp);
+    case 5: return tc::run_tc<Tf32P256>(p, a_big, a_small, b_big, b_small, Kp, Kp, Kp);
     default: return tc::run_tc<Tf32N128>(p, a_big, a_small, b_big, b_small, Kp, Kp, Kp);
   }
 }

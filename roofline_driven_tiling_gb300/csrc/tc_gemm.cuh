@@ -180,8 +180,8 @@ enum TcKind : int { kTf32x3 = 0, kBf16 = 1, kF16 = 2 };
 // operands only) instead of as an N x K transposed plane.
 // PAIR: CTAs run in clusters of two on two SMs that compute one 256-row tile together with
 // tcgen05 .cta_group::2 MMAs (issued by rank 0): each CTA stages its 128 rows of A and half of
-// B's columns, and accumulates its 128 rows in its own TMEM. Each SM thus receives half of
-// the B tile instead of all of it.
+// B's columns (MN-major boxes, or BN / 2 rows of each K-major B plane), and accumulates its 128
+// rows in its own TMEM. Each SM thus receives half of the B tile instead of all of it.
 //
 // WIDE (CTA pairs with B read in place only): the tile is twice the widest MMA, BN = 512; each
 // k step issues two N = 256 MMAs into the two halves of one 512-column TMEM accumulator, so an
@@ -221,7 +221,9 @@ struct TcConfig {
   // another; a box is a column of 128-byte swizzle atoms (8 K-rows x 64 columns each).
   static constexpr int B_BOX_BYTES = BK * 128;
   static constexpr int B_BOXES = B_MN ? BN / 64 : 1;
-  static_assert(!PAIR || (B_MN && B_BOXES % 2 == 0), "pairs split an even number of B boxes");
+  static_assert(!PAIR || (B_MN ? B_BOXES % 2 == 0 : (BN / 2) % 8 == 0),
+                "pairs split B in two: an even number of MN-major boxes, or whole 8-row groups of "
+                "a K-major plane");
   static constexpr int G = PAIR ? 2 : 1;                  // CTAs per MMA
   static constexpr int B_BOXES_CTA = B_BOXES / G;          // B boxes this CTA stages
   static constexpr int A_BOX_BYTES = BM * ATOM_BYTES;
@@ -414,14 +416,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) __maxnreg__(Cfg::MAX_REGS)
 #pragma unroll
             for (int q = 0; q < Cfg::A_SUBS; ++q)
               tma_load_2d_pair(st + q * Cfg::A_BOX_BYTES, &tmAb, k0 + q * Cfg::ATOM_COLS, m0, bar0);
-            // This CTA's half of each MMA's columns: box j of half h holds columns
-            // h MMA_N + rank MMA_N / 2 + 64 (j % B_BOXES_HALF) .. + 63.
+            if constexpr (Cfg::B_MN) {
+              // This CTA's half of each MMA's columns: box j of half h holds columns
+              // h MMA_N + rank MMA_N / 2 + 64 (j % B_BOXES_HALF) .. + 63.
 #pragma unroll
-            for (int j = 0; j < Cfg::B_BOXES_CTA; ++j)
-              tma_load_2d_pair(st + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &tmBb,
-                               n0 + (j / Cfg::B_BOXES_HALF) * Cfg::MMA_N +
-                                   (Cfg::MMA_N / 2) * rank + 64 * (j % Cfg::B_BOXES_HALF),
-                               k0, bar0);
+              for (int j = 0; j < Cfg::B_BOXES_CTA; ++j)
+                tma_load_2d_pair(st + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &tmBb,
+                                 n0 + (j / Cfg::B_BOXES_HALF) * Cfg::MMA_N +
+                                     (Cfg::MMA_N / 2) * rank + 64 * (j % Cfg::B_BOXES_HALF),
+                                 k0, bar0);
+            } else {
+              // K-major B planes: this CTA's BN / 2 rows (columns of B), n0 + rank BN / 2 ..
+              const int nb0 = n0 + rank * (Cfg::BN / 2);
+              tma_load_2d_pair(st + Cfg::PLANES * Cfg::A_BYTES, &tmBb, k0, nb0, bar0);
+              if constexpr (Cfg::PLANES == 2) {
+                tma_load_2d_pair(st + Cfg::A_BYTES, &tmAs, k0, m0, bar0);
+                tma_load_2d_pair(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES, &tmBs, k0, nb0, bar0);
+              }
+            }
             continue;
           }
           mbar_arrive_expect_tx(full(s), Cfg::STAGE_BYTES);
@@ -732,11 +744,12 @@ cudaError_t run_tc(const Problem& p, const void* a0, const void* a1, const void*
         cudaSuccess)
       return e;
   } else {
-    if ((e = enc(&tBb, b0, ldb, p.N, Cfg::BN)) != cudaSuccess) return e;
+    // K-major B: each CTA of a pair stages half of the tile's rows of each plane.
+    if ((e = enc(&tBb, b0, ldb, p.N, Cfg::BN / Cfg::G)) != cudaSuccess) return e;
   }
   if (Cfg::PLANES == 2) {
     if ((e = enc(&tAs, a1, lda, p.M, Cfg::BM)) != cudaSuccess) return e;
-    if ((e = enc(&tBs, b1, ldb, p.N, Cfg::BN)) != cudaSuccess) return e;
+    if ((e = enc(&tBs, b1, ldb, p.N, Cfg::BN / Cfg::G)) != cudaSuccess) return e;
   }
   // C as a TMA store target: row stride a multiple of 16 bytes, 16-byte aligned.
   CUtensorMap tC;

@@ -348,6 +348,24 @@ def test_tf32x3_finite_operands_next_to_flt_max(operand):
     assert float(np.max(np.abs(C - want))) <= tolerance(A, B)
 
 
+@pytest.mark.parametrize("shape", [(4000, 4100, 520), (4096, 4096, 1024), (1324, 2500, 300)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tf32x3_pair_tiles(shape):
+    """Shapes the 3xTF32 dispatch runs on CTA pairs (256-row tiles, cta_group::2 MMAs, each CTA
+    staging half of the B planes): ragged M (the last pair's second CTA holds rows past M, or
+    none), ragged N (a partial last tile of 224 or 256 columns), K not a multiple of the
+    32-value padding. Checked on whole rows and columns at the edges and on random elements
+    against both readings of the oracle, within the FP32 tolerance."""
+    M, N, K = shape
+    A, B = inputs.uniform_pair(M, N, K, 29)
+    C = run("tf32x3", A, B)
+    assert np.all(np.isfinite(C))
+    rows, cols = sample_positions(M, N, np.random.default_rng(M + N + K), n_random=8192)
+    for mode in (oracle.FMA, oracle.MUL_ADD):
+        want = oracle.sgemm_at(A, B, rows, cols, mode)
+        assert float(np.max(np.abs(C[rows, cols] - want))) <= tolerance(A, B)
+
+
 def test_tf32x3_workspace_checks():
     M, N, K = 64, 64, 64
     dA = torch.zeros((M, K), device="cuda")
