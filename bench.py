@@ -359,6 +359,33 @@ def measure_probes(lib, dev, stream):
     return res
 
 
+def extra_store_probe(dev, stream):
+    """The store path's ceiling: t2s_probe_store_f32 writes a 16384 x 16384 FP32 matrix (the
+    1.07 GB C of the 16384^2 x 32 product, above L2) with no arithmetic in the short-K product's
+    store pattern, through TMA boxes (mode 0) and with 16-byte stores from registers (mode 1);
+    the best of 5 launches each."""
+    import torch
+    from roofline_driven_tiling_gb300 import binding
+    M = N = 16384
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    sp = stream.cuda_stream
+    res = {"matrix": "%d x %d FP32 (%d MB)" % (M, N, 4 * M * N // 10**6), "call": "t2s_probe_store_f32",
+           "unit": "GB/s"}
+    for mode, key in ((0, "tma_boxes_gbs"), (1, "plain_stores_gbs")):
+        binding.probe_store(M, N, C.data_ptr(), mode, 1.0, sp)
+        best = 0.0
+        for _ in range(5):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            nbytes = binding.probe_store(M, N, C.data_ptr(), mode, 1.0, sp)
+            e.record(stream)
+            torch.cuda.synchronize()
+            best = max(best, nbytes / (s.elapsed_time(e) * 1e-3) / 1e9)
+        res[key] = best
+    del C
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -466,6 +493,7 @@ def run_ours(args):
         line["f64"] = extra_f64(lib, stream, flush, args, dev)
         line["also_1024"] = extra_1024(lib, dev, stream, flush, args, ws)
         line["memory_roof"] = extra_vector_add(lib, dev, stream, flush, args)
+        line["memory_roof"]["c_store_probe"] = extra_store_probe(dev, stream)
 
     if rank == 0 and ws == 1 and not args.skip_cpu:
         rate, info = cpu_oracle_rate(A, B, float(os.environ.get("T2S_CPU_SECONDS", "12")))

@@ -381,6 +381,24 @@ int t2s_probe_outputs(void);
 int t2s_probe_fp32_fma(int64_t iters, float *out, int64_t *flops, t2s_stream_t stream);
 int t2s_probe_tf32_mma(int64_t iters, float *out, int64_t *flops, t2s_stream_t stream);
 
+/*
+ * Store-path probe: the rate at which a matrix leaves the SMs, the ceiling of every product
+ * whose C is as large as its arithmetic (short K). Writes `value` to every element of the
+ * row-major M x N FP32 matrix C with no arithmetic, in the short-K product's store pattern:
+ * one CTA of 8 warps per SM walks 256 x 128 tiles in the product's grouped order (groups of 8
+ * tile rows), each warp writing a 64 x 64 part, either
+ *  - mode 0: staged in shared memory and stored as two 64 x 32 TMA boxes (128-byte swizzle),
+ *    restaged once the previous stores have read the boxes (the short-K kernel's epilogue), or
+ *  - mode 1: as 16-byte stores from registers in the register-tile layout (the epilogue of
+ *    the other product kernels).
+ * C is a DEVICE pointer, 16-byte aligned; M a multiple of 256 and N a multiple of 128, both
+ * positive and at most T2S_MAX_DIM. *bytes (host memory) receives the bytes written, 4 M N;
+ * the caller times the launch on `stream`. Returns T2S_OK, T2S_ERR_INVALID (sizes, alignment,
+ * mode, NULL pointers; checked before any device call) or T2S_ERR_CUDA.
+ */
+int t2s_probe_store_f32(int64_t M, int64_t N, float *C, int mode, float value, int64_t *bytes,
+                        t2s_stream_t stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int t2s_version(void);
 

@@ -57,6 +57,7 @@ SIGNATURES = {
     "t2s_probe_outputs": ([], _i),
     "t2s_probe_fp32_fma": ([_i64, _p, _p, _p], _i),
     "t2s_probe_tf32_mma": ([_i64, _p, _p, _p], _i),
+    "t2s_probe_store_f32": ([_i64, _i64, _p, _i, ctypes.c_float, _p, _p], _i),
     "t2s_version": ([], _i),
 }
 
@@ -207,6 +208,17 @@ def probe(kind: str, iters: int, out_ptr: int, stream=0) -> int:
     if rc != T2S_OK:
         raise T2SError(rc, "t2s_probe_" + kind)
     return int(flops.value)
+
+
+def probe_store(M: int, N: int, c_ptr: int, mode: int, value: float = 0.0, stream=0) -> int:
+    """Launches the store-path probe on `stream`: writes `value` to the M x N matrix at c_ptr
+    in the short-K product's store pattern (mode 0: TMA boxes, 1: 16-byte stores from
+    registers); returns the bytes written (raises T2SError on a bad status)."""
+    nbytes = ctypes.c_int64(0)
+    rc = lib().t2s_probe_store_f32(M, N, c_ptr, mode, value, ctypes.addressof(nbytes), stream)
+    if rc != T2S_OK:
+        raise T2SError(rc, "t2s_probe_store_f32")
+    return int(nbytes.value)
 
 
 status_string = t2s_status_string

@@ -388,6 +388,19 @@ int t2s_probe_tf32_mma(int64_t iters, float* out, int64_t* flops, t2s_stream_t s
   return e == cudaSuccess ? T2S_OK : fail_cuda(e);
 }
 
+int t2s_probe_store_f32(int64_t M, int64_t N, float* C, int mode, float value, int64_t* bytes,
+                        t2s_stream_t stream) {
+  if (M < 256 || N < 128 || M % 256 != 0 || N % 128 != 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM)
+    return T2S_ERR_INVALID;
+  if ((M / 256) * (N / 128) > 0x7fffffffLL) return T2S_ERR_INVALID;
+  if (C == nullptr || (reinterpret_cast<uintptr_t>(C) & 15u) != 0 || bytes == nullptr)
+    return T2S_ERR_INVALID;
+  if (mode != 0 && mode != 1) return T2S_ERR_INVALID;
+  const cudaError_t e =
+      launch_store_probe(M, N, C, mode, value, reinterpret_cast<cudaStream_t>(stream), bytes);
+  return e == cudaSuccess ? T2S_OK : fail_cuda(e);
+}
+
 int t2s_gemm_f32_plan(int64_t M, int64_t N, int64_t K, int sms) {
   if (M < 0 || N < 0 || K < 0 || M > T2S_MAX_DIM || N > T2S_MAX_DIM || K > T2S_MAX_DIM) return -1;
   if (sms < 1) return -1;

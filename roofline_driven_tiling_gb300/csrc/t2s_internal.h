@@ -86,6 +86,10 @@ cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream
 cudaError_t launch_ffma_probe(int64_t iters, float* out, cudaStream_t stream, int64_t* flops);
 cudaError_t launch_tf32_mma_probe(int64_t iters, float* out, unsigned* status, cudaStream_t stream,
                                   int64_t* flops);
+// Writes `value` to the M x N matrix C (M % 256 == 0, N % 128 == 0, checked by the caller) in
+// the short-K product's store pattern: mode 0 TMA boxes, mode 1 16-byte stores from registers.
+cudaError_t launch_store_probe(int64_t M, int64_t N, float* C, int mode, float value,
+                               cudaStream_t stream, int64_t* bytes);
 // Records a CUDA error for t2s_last_cuda_error() on this host thread.
 void set_last_cuda_error(cudaError_t e);
 

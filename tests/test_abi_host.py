@@ -199,3 +199,10 @@ def test_probes_reject_bad_arguments(lib):
     assert lib.t2s_probe_tf32_mma(0, fake, fp, 0) == binding.T2S_ERR_INVALID
     assert lib.t2s_probe_tf32_mma((1 << 16) + 1, fake, fp, 0) == binding.T2S_ERR_INVALID
     assert lib.t2s_probe_tf32_mma(10, None, fp, 0) == binding.T2S_ERR_INVALID
+    # The store probe: whole 256 x 128 tiles, a 16-byte aligned C, mode 0 or 1.
+    st = lib.t2s_probe_store_f32
+    for args in [(0, 128, fake, 0), (255, 128, fake, 0), (256, 127, fake, 0), (512, 100, fake, 1),
+                 (256, 128, None, 0), (256, 128, fake + 4, 0), (256, 128, fake, 2),
+                 (256, 128, fake, -1), ((1 << 30) + 256, 128, fake, 0)]:
+        assert st(*args, 1.0, fp, 0) == binding.T2S_ERR_INVALID, args
+    assert st(256, 128, fake, 0, 1.0, None, 0) == binding.T2S_ERR_INVALID
