@@ -1567,12 +1567,15 @@ cudaError_t launch_pstore(const Problem& p) {
 // tiles (1 KB of each C row per tile instead of 512 bytes): within 1 %; warps 4-7 started 1000 to
 // 4000 cycles late, so that the two warps of a sub-partition stage at different times: +1-3 %
 // (the offset drifts away within a few tiles); the stores issued during the first K groups of the
-// next tile: no gain at K = 32, slower from K = 64 on. Per-warp cycle counts at 16384^2 x 32: a
-// tile takes about 11.6 K cycles, 9.2 K of them multiply-adds and 1.45 K staging C and issuing
-// its stores (all warps at once; lane 0 waits about 0.7 K while the TMA unit takes the boxes).
-// C leaves the SMs at 6-7.7 TB/s at most, whatever the store pattern (t2s_probe_store_f32), so
-// the 1.07 GB of C needs 150-170 us against about 254 us of multiply-adds; K = 16 costs as much
-// as K = 32 because the 32-deep K block is zero-padded.
+// next tile: no gain at K = 32, slower from K = 64 on; a warpgroup of 4 store warps issuing them
+// (setmaxnreg: 40 registers each, 232 for the compute warps): +1 % at K = 32, slower at 8192 x
+// 4096 x 32 and 6144^2 x 96, the compute warps' multiply-adds 4 % slower. Per-warp cycle counts
+// at 16384^2 x 32: a tile takes about 11.6 K cycles, 9.2 K of them multiply-adds and 1.45 K
+// staging C and issuing its stores (all warps at once; lane 0 waits about 0.7 K while the TMA unit
+// takes the boxes). C leaves the SMs at 6-7.7 TB/s at most, whatever the store pattern
+// (t2s_probe_store_f32: 6.37 TB/s at 16384^2), so the 1.07 GB of C needs about 170 us against
+// about 254 us of multiply-adds; K = 16 costs as much as K = 32 because the 32-deep K block is
+// zero-padded.
 cudaError_t launch_ffma_pstore(const Problem& p) { return launch_pstore<Huge, 2, 1>(p); }
 
 bool pstore_ok(const Problem& p) {
