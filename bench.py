@@ -224,6 +224,42 @@ def cpu_oracle_rate(A, B, target_s: float):
     return flops / dt / 1e12, info
 
 
+def cpu_oracle_configs(budget_s: float = 4.0):
+    """Times the oracle (two roundings per term, all host threads) on the workload of every
+    configuration of the pages' measurements: the integer pattern at 256^3 and 1024^3, the
+    constants 0.5 / 0.4 at 1024^3, the ragged 1000 x 1003 x 997, 4096^3 and the roofline sweep
+    shapes, all uniform on [-1, 1) but the first three. A product whose estimate (from one row
+    per thread) is within budget_s runs whole, three times up to 1024^3 and once above; a
+    larger one runs once on a row sample of about budget_s. Returns one record per workload."""
+    import oracle  # test infrastructure, used here only as the CPU baseline
+    from roofline_driven_tiling_gb300 import inputs
+    nt = max(1, oracle.num_threads())
+    work = [(name, M, N, K, kind, no) for name, (M, N, K, kind, no) in inputs.CONFIGS.items()]
+    work += [("c5_sweep_%dx%dx%d" % shape, *shape, "uniform", 5) for shape in inputs.SWEEP]
+    records = []
+    for name, M, N, K, kind, no in work:
+        A, B = inputs.make(kind, M, N, K, no)
+        t0 = time.perf_counter()
+        oracle.sgemm_rows(A, B, 0, min(nt, M), oracle.MUL_ADD)
+        per_round = max(time.perf_counter() - t0, 1e-5)
+        if per_round * -(-M // nt) <= budget_s:
+            rows, runs = M, (3 if M * N * K <= 1024 ** 3 else 1)
+        else:
+            rows, runs = int(min(M, nt * max(1, round(budget_s / per_round)))), 1
+        secs = []
+        for _ in range(runs):
+            t0 = time.perf_counter()
+            oracle.sgemm_rows(A, B, 0, rows, oracle.MUL_ADD)
+            secs.append(time.perf_counter() - t0)
+        med = statistics.median(secs)
+        records.append({"config": name, "shape": [M, N, K], "inputs": kind, "rows": rows,
+                        "whole_product": rows == M, "runs": runs,
+                        "seconds_mean": sum(secs) / runs, "seconds_median": med,
+                        "seconds_min": min(secs), "tflops": 2.0 * rows * N * K / med / 1e12,
+                        "cores": nt})
+    return records
+
+
 def cpu_blocked_rate(A, B, target_s: float = 4.0):
     """Times the cache-blocked multi-core CPU GEMM (a stronger CPU baseline than the oracle;
     it checks nothing) on a row block of C = A x B sized to take about target_s; returns the
@@ -697,7 +733,13 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--skip-cpu", action="store_true", help="omit the CPU oracle baseline")
     p.add_argument("--skip-extras", action="store_true", help="omit tf32x3 and 1024^3 lines")
+    p.add_argument("--cpu-configs", action="store_true",
+                   help="only time the CPU oracle on every configuration's workload (host cores, "
+                        "no GPU) and print one JSON line")
     args = p.parse_args(argv)
+    if args.cpu_configs:
+        print(json.dumps({"cpu_oracle_configs": cpu_oracle_configs(), "kind": "oracle"}), flush=True)
+        return 0
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
