@@ -23,6 +23,8 @@ the ragged 1000 x 1003 x 997, for the product and the other FP32 entry points.
 * Each result is compared with the product's: bit for bit for the naive and smem32 kernels
   (the same fused multiply-adds in the same order), within 1e-6 K max|a| max|b| for the
   others. A mismatch is reported in the line and fails the run.
+* `cublas` is the vendor library's FP32 product (torch.mm with TF32 off), timed the same way
+  as a comparison point; it is not part of this library.
 * --shapes replaces the sweep's shapes (one small shape and one kernel make a short run that
   a profiler can capture), --splitk-chunks fixes the split-K chunk count (0: the automatic
   choice), and --misalign offsets A, B and C by one float so that every kernel takes its
@@ -37,7 +39,7 @@ import sys
 
 SHAPES = [(n, n, n) for n in (128, 256, 512, 1024, 2048, 4096, 8192)] + [
     (16384, 16384, 32), (8192, 8192, 64), (1000, 1003, 997)]
-KERNELS = ("ffma", "tf32x3", "splitk", "streamk", "smem32", "naive")
+KERNELS = ("ffma", "tf32x3", "splitk", "streamk", "smem32", "naive", "cublas")
 SEED_A, SEED_B = 1005, 2005
 FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
@@ -53,8 +55,9 @@ def _hbm_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _calls(binding, lib, M, N, K, dA, dB, dC, ws, stream, chunks=0, shift=0):
-    """One closure per entry point (the workspace tensor is large enough for all)."""
+def _calls(binding, lib, M, N, K, dA, dB, dC, ws, stream, chunks=0, shift=0, torch=None):
+    """One closure per entry point (the workspace tensor is large enough for all), and the
+    vendor library's product for comparison."""
     a, b, c, s = (dA.data_ptr() + 4 * shift, dB.data_ptr() + 4 * shift,
                   dC.data_ptr() + 4 * shift, stream)
     w, wn = ws.data_ptr(), ws.numel()
@@ -74,6 +77,8 @@ def _calls(binding, lib, M, N, K, dA, dB, dC, ws, stream, chunks=0, shift=0):
         "smem32": lambda: check(lib.t2s_gemm_f32_smem32(M, N, K, a, b, c, s),
                                 "t2s_gemm_f32_smem32"),
         "naive": lambda: check(lib.t2s_gemm_f32_naive(M, N, K, a, b, c, s), "t2s_gemm_f32_naive"),
+        "cublas": lambda: torch.mm(dA[shift:].view(M, K), dB[shift:].view(K, N),
+                                   out=dC[shift:].view(M, N)),
     }
 
 
@@ -129,6 +134,10 @@ def main(argv=None) -> int:
     bw, bw_basis = _hbm_gbs()
     peak = rl.fp32_peak_tflops()
     kernels = [k for k in args.kernels.split(",") if k]
+    if "cublas" in kernels:
+        # The FP32 product, not TF32.
+        torch.backends.cuda.matmul.allow_tf32 = False
+        torch.set_float32_matmul_precision("highest")
     out = open(args.out, "w") if args.out else None
     rows, bad = [], 0
     for (M, N, K) in shapes:
@@ -142,7 +151,7 @@ def main(argv=None) -> int:
         ws = torch.empty(_workspace_bytes(lib, M, N, K, args.splitk_chunks), dtype=torch.uint8,
                          device=dev)
         calls = _calls(binding, lib, M, N, K, dA, dB, dC_buf, ws, stream.cuda_stream,
-                       args.splitk_chunks, shift)
+                       args.splitk_chunks, shift, torch)
         flops = rl.gemm_flops(M, N, K)
         tol = 1e-6 * K * float(abs(A).max()) * float(abs(B).max())
         ref = None
@@ -164,6 +173,8 @@ def main(argv=None) -> int:
                 exact = bool(torch.equal(dC.view(torch.int32), ref.view(torch.int32)))
                 if name in ("naive", "smem32"):
                     check = "bit-exact" if exact else "MISMATCH"
+                elif exact:
+                    check = "bit-exact"
                 else:
                     check = "within tolerance" if diff <= tol else "MISMATCH"
                 bad += check == "MISMATCH"

@@ -87,4 +87,5 @@ def test_sweep_covers_the_sweep_configuration():
     squares = {(n, n, n) for n in (128, 256, 512, 1024, 2048, 4096, 8192)}
     assert squares <= set(sweep.SHAPES)
     assert {(16384, 16384, 32), (8192, 8192, 64), (1000, 1003, 997)} <= set(sweep.SHAPES)
-    assert set(sweep.KERNELS) == {"ffma", "tf32x3", "splitk", "streamk", "smem32", "naive"}
+    # Every FP32 entry point, and the vendor library's product as a comparison column.
+    assert set(sweep.KERNELS) == {"ffma", "tf32x3", "splitk", "streamk", "smem32", "naive", "cublas"}
