@@ -14,9 +14,9 @@
 // GB300 design:
 //  * A STAGES-deep ring of shared-memory buffers per CTA, one "full" mbarrier per slot.
 //    On the TMA path there is no producer warp: every warp computes. CTA tiles run from
-//    32 x 32 to 256 x 128 of 4 or 8 warps, chosen per shape (pick_ffma), and an SM holds 8
-//    warps, two per sub-partition, at up to 255 registers per thread for the largest
-//    register tile.
+//    32 x 32 to 256 x 128 of 4 or 8 warps, chosen per shape (pick_ffma), and an SM holds at
+//    least 8 warps, two per sub-partition (16 for the small register tiles), at up to 255
+//    registers per thread for the largest register tile.
 //  * Aligned case (K % 4 == 0, N % 4 == 0, 16-byte aligned pointers): the Tensor Memory
 //    Accelerator loads a BM x BK box of A and a BK x BN box of B per stage; elements
 //    outside the matrices are filled with zeros by the TMA unit, and completion is
@@ -48,7 +48,9 @@
 //    instruction does two IEEE fused multiply-adds, which halves the issue slots the
 //    FMAs need and leaves the rest for shared loads.
 //  * The k loop runs in groups of 8 k values (fully unrolled inside a group) so that the
-//    loop body stays small enough for the instruction cache.
+//    loop body stays small enough for the instruction cache; the large tiles unroll the
+//    whole K block when K is long enough to pay for the code, and the small ones load the
+//    fragments of step k + 1 while step k is multiplied.
 //  * Every barrier wait is bounded; on expiry the kernel records T2S_ERR_TIMEOUT in the
 //    device status word and returns instead of hanging, after letting its own in-flight
 //    copies land.
