@@ -36,9 +36,9 @@
 //    whose warps hand C to TMA stores while the ring loads the next tile
 //    (sgemm_ffma_pstore_kernel).
 //  * A is stored K-major as it is in global memory (TMA cannot transpose 4-byte
-//    elements). Rows of BK floats are XOR-swizzled in 16-byte chunks (the TMA
-//    128/64/32-byte swizzle), so that the 8 rows a warp reads at one k chunk fall in
-//    8 distinct bank groups.
+//    elements). Rows of BK floats (of 32 in each 32-deep sub-block when BK = 64) are
+//    XOR-swizzled in 16-byte chunks (the TMA 128/64/32-byte swizzle), so that the 8 rows a
+//    warp reads at one k chunk fall in 8 distinct bank groups.
 //  * B is stored as it is (rows of BN floats); a warp reads 4 consecutive 16-byte
 //    chunks of one row per load, which is conflict-free without a swizzle.
 //  * Each thread owns a TM x TN register tile of C (8 x 16 in the large CTA tiles; 8 x 8,
@@ -79,7 +79,7 @@ struct FfmaConfig {
   static constexpr int WM = LM * TM, WN = LN * TN;
   static_assert(BM == WARPS_M * WM && BN == WARPS_N * WN, "tile / warp mismatch");
   static_assert(TN % 4 == 0 && TM >= 1, "columns come in float4 chunks");
-  static_assert(BK == 8 || BK == 16 || BK == 32, "A rows must be 32, 64 or 128 bytes");
+  static_assert(BK == 8 || BK == 16 || BK == 32 || BK == 64, "A rows of 32, 64 or 128 bytes");
   static_assert((AV == 1 || AV == 2 || AV == 4) && 8 % AV == 0, "A load width");
   static constexpr int WARPS = WARPS_M * WARPS_N;
   static constexpr int THREADS = WARPS * 32;
@@ -87,12 +87,18 @@ struct FfmaConfig {
   // 128-accumulator tile (up to 255 registers), more for smaller tiles.
   static constexpr int TARGET_WARPS = TM * TN >= 128 ? 8 : TM * TN >= 64 ? 12 : 16;
   static constexpr int MIN_BLOCKS = TARGET_WARPS / WARPS > 0 ? TARGET_WARPS / WARPS : 1;
-  static constexpr int A_ROW_BYTES = BK * 4;
+  // A is staged as BK / BKS sub-blocks of BKS k values (BK = 64: two of 32), each BM rows of
+  // BKS floats in the TMA swizzle, one after the other.
+  static constexpr int BKS = BK > 32 ? 32 : BK;
+  static constexpr int A_SUBS = BK / BKS;
+  static constexpr int A_ROW_BYTES = BKS * 4;
+  static constexpr int A_SUB_BYTES = BM * BKS * 4;
   static constexpr int SWZ_MASK = A_ROW_BYTES / 16 - 1;  // 7 (128 B), 3 (64 B), 1 (32 B)
   static constexpr int A_STAGE_BYTES = BM * BK * 4;
   static constexpr int B_STAGE_BYTES = BK * BN * 4;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   static_assert(A_STAGE_BYTES % 1024 == 0 && B_STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(A_SUB_BYTES % 1024 == 0, "sub-block alignment (the swizzle's 1 KB repeat)");
   // Ring, full[S] and empty[S] barriers, refill counters, and up to 1 KB to align the
   // base to 1024 B (the repeat of the 128-byte swizzle pattern).
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGES * 8 + STAGES * 4 + 1024;
@@ -123,8 +129,8 @@ struct GenRing {
 // every thread of the CTA, or its producer warps) into the same shared-memory image the TMA
 // path writes (A K-major with the 128-byte swizzle, B as stored), zeros for rows >= M,
 // k >= kend and columns >= N. Warp w of the group copies the A rows w, w + NT / 32, ... (lane =
-// k, one instruction per row); the group copies B rows NT / BN at a time (thread t: column
-// t % BN). A stage wholly inside the matrices takes no bounds checks. The thread arrives on the
+// k, one instruction per row and 32-deep sub-block); the group copies B rows NT / BN at a time
+// (thread t: column t % BN). A stage wholly inside the matrices takes no bounds checks. The thread arrives on the
 // stage's full barrier once its copies have landed.
 template <class Cfg, int NT>
 __device__ __forceinline__ void gen_copy_stage(const float* __restrict__ A,
@@ -132,7 +138,7 @@ __device__ __forceinline__ void gen_copy_stage(const float* __restrict__ A,
                                                int kend, int m0, int n0, int k0, uint32_t a_dst,
                                                uint32_t b_dst, uint32_t full_bar, int t) {
   constexpr int NW = NT / 32;
-  static_assert(Cfg::BK == 32, "one warp instruction per A row");
+  static_assert(Cfg::BKS == 32, "one warp instruction per A row and sub-block");
   static_assert(NT % 32 == 0 && Cfg::BM % NW == 0 && NT % Cfg::BN == 0, "copy mapping");
   constexpr int A_ROWS = Cfg::BM / NW;   // A rows per warp
   constexpr int B_STEP = NT / Cfg::BN;   // B rows per pass of the group
@@ -150,10 +156,13 @@ __device__ __forceinline__ void gen_copy_stage(const float* __restrict__ A,
   };
   if (m0 + Cfg::BM <= M && k0 + Cfg::BK <= kend && n0 + Cfg::BN <= N) {
 #pragma unroll
-    for (int i = 0; i < A_ROWS; ++i) {
-      const int r = warp + NW * i;
-      cp_async_4_full(a_dst + a_off(r), a_src + static_cast<int64_t>(NW) * i * K);
-    }
+    for (int sb = 0; sb < Cfg::A_SUBS; ++sb)
+#pragma unroll
+      for (int i = 0; i < A_ROWS; ++i) {
+        const int r = warp + NW * i;
+        cp_async_4_full(a_dst + sb * Cfg::A_SUB_BYTES + a_off(r),
+                        a_src + sb * 32 + static_cast<int64_t>(NW) * i * K);
+      }
 #pragma unroll
     for (int i = 0; i < B_PASSES; ++i)
       cp_async_4_full(b_dst0 + static_cast<uint32_t>(i * B_STEP * Cfg::BN * 4),
@@ -161,14 +170,17 @@ __device__ __forceinline__ void gen_copy_stage(const float* __restrict__ A,
   } else {
     // Out-of-range elements are zero-filled; their source pointer is replaced by the
     // matrix's first element, which nothing reads (0 source bytes).
-    const bool k_ok = k0 + lane < kend;
     const int rows_left = M - m0 - warp;
 #pragma unroll
-    for (int i = 0; i < A_ROWS; ++i) {
-      const int r = warp + NW * i;
-      const bool v = k_ok && NW * i < rows_left;
-      cp_async_4(a_dst + a_off(r), v ? a_src + static_cast<int64_t>(NW) * i * K : A,
-                 v ? 4u : 0u);
+    for (int sb = 0; sb < Cfg::A_SUBS; ++sb) {
+      const bool k_ok = k0 + sb * 32 + lane < kend;
+#pragma unroll
+      for (int i = 0; i < A_ROWS; ++i) {
+        const int r = warp + NW * i;
+        const bool v = k_ok && NW * i < rows_left;
+        cp_async_4(a_dst + sb * Cfg::A_SUB_BYTES + a_off(r),
+                   v ? a_src + sb * 32 + static_cast<int64_t>(NW) * i * K : A, v ? 4u : 0u);
+      }
     }
     const bool n_ok = n0 + bcol < N;
     const int k_left = kend - k0 - brow;
@@ -206,7 +218,9 @@ __device__ __forceinline__ void tma_stage(const CUtensorMap* tmA, const CUtensor
                                           int m0, int n0, int k0, uint32_t a_dst,
                                           uint32_t b_dst, uint32_t full_bar) {
   mbar_arrive_expect_tx(full_bar, Cfg::STAGE_BYTES);
-  tma_load_2d(a_dst, tmA, k0, m0, full_bar);
+#pragma unroll
+  for (int sb = 0; sb < Cfg::A_SUBS; ++sb)
+    tma_load_2d(a_dst + sb * Cfg::A_SUB_BYTES, tmA, k0 + sb * Cfg::BKS, m0, full_bar);
   tma_load_2d(b_dst, tmB, n0, k0, full_bar);
 }
 
@@ -219,8 +233,11 @@ __device__ __forceinline__ void ffma_kblock_direct(uint64_t (&acc)[Cfg::TM][Cfg:
                                                    uint32_t xr) {
 #pragma unroll Cfg::KG_UNROLL
   for (int kg = 0; kg < Cfg::BK / 8; ++kg) {
-    // 8 k values = two 16-byte chunks of each A row, swizzled.
-    const uint32_t c0 = ((2u * kg) ^ xr) << 4, c1 = ((2u * kg + 1u) ^ xr) << 4;
+    // 8 k values = two 16-byte chunks of each A row of sub-block kg / (BKS / 8), swizzled.
+    constexpr int KGS = Cfg::BKS / 8;
+    const uint32_t kgl = static_cast<uint32_t>(kg % KGS);
+    const uint32_t sub = static_cast<uint32_t>(kg / KGS) * Cfg::A_SUB_BYTES;
+    const uint32_t c0 = sub + (((2u * kgl) ^ xr) << 4), c1 = sub + (((2u * kgl + 1u) ^ xr) << 4);
     const uint32_t b_kg = b_base + kg * (8 * Cfg::BN * 4);
 #pragma unroll
     for (int kv = 0; kv < 8 / Cfg::AV; ++kv) {
@@ -266,7 +283,9 @@ __device__ __forceinline__ void ffma_kblock_pipelined(uint64_t (&acc)[Cfg::TM][C
   float a[2][Cfg::TM][AV];
   uint64_t b[2][Cfg::TN / 2];
   auto load_a = [&](int kq, int buf) {
-    const uint32_t koff = ((static_cast<uint32_t>(kq >> 2) ^ xr) << 4) + (kq & 3) * 4;
+    const int kql = kq % Cfg::BKS;
+    const uint32_t koff = static_cast<uint32_t>(kq / Cfg::BKS) * Cfg::A_SUB_BYTES +
+                          ((static_cast<uint32_t>(kql >> 2) ^ xr) << 4) + (kql & 3) * 4;
 #pragma unroll
     for (int i = 0; i < Cfg::TM; ++i)
       lds_vec<AV>(a_base + i * Cfg::LM * Cfg::A_ROW_BYTES + koff, a[buf][i]);
@@ -860,7 +879,7 @@ cudaError_t run(const Problem& p, int splits = 1, int k_chunk = 0, float* out = 
     const CUtensorMapSwizzle sw = Cfg::A_ROW_BYTES == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : Cfg::A_ROW_BYTES == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                            : CU_TENSOR_MAP_SWIZZLE_32B;
-    cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BK, Cfg::BM, sw);
+    cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BKS, Cfg::BM, sw);
     if (e != cudaSuccess) return e;
     e = encode_tmap_f32_2d(&tb, p.B, p.N, p.K, Cfg::BN, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
@@ -923,6 +942,15 @@ using BigShortK = FfmaConfig<128, 128, 32, 3, 2, 2, 2, 8, 16, 1>;
 // quarters of the staged bytes and half the barrier rounds per FLOP: in whole rounds 4-5 %
 // faster (3072^3: 63.4 against 60.5 TFLOP/s), while its coarser rounds leave longer tails.
 using Huge = FfmaConfig<256, 128, 32, 3, 4, 2, 2, 8, 16, 4>;
+// The same tile with 64-deep K blocks (two 32-deep sub-blocks of A per stage) in 2 stages of
+// 96 KB: half the K-block boundaries per FLOP, each of which costs every warp a barrier wait and
+// the first fragment loads of the block. It runs the whole-round launches over all of K on the
+// TMA path: 4096^3 65.2 -> 66.0 TFLOP/s, 3072^3 63.4 -> 64.2, 2048^3 55.4 -> 56.2, the same
+// bits. The k loop is unrolled over 4 of its 8 groups: all 8 ran 56.3 at 4096^3 (the code
+// outgrows the instruction cache). K ranges, whose chunk ends TMA does not zero-fill, the
+// general path (a 2-stage ring cannot issue a stage S - 2 blocks ahead) and the short-K kernel
+// keep the 32-deep tile.
+using Huge64 = FfmaConfig<256, 128, 64, 2, 4, 2, 2, 8, 16, 4>;
 // 4 x 8 per thread (64 x 64 CTA tiles of 4 warps, BK = 32, 3 stages): many small CTAs (four
 // per SM) that even out the last wave. Measured fastest up to ~2.4 tiles of 128 x 128 per SM:
 // 1024^3 37.0 TFLOP/s (BK = 16 and 4 stages: 32.4; 128 x 64 tiles of 8 x 8: 35.8), 2048^3 52.3
@@ -944,6 +972,12 @@ using Tall84 = FfmaConfig<128, 64, 32, 3, 2, 4, 2, 8, 4, 1>;
 // values at a time in the 128 x 64 tile, 4 x 8 per thread in it, 120 x 64 tiles of 12 warps,
 // 4 stages: none faster.)
 using Wide74 = FfmaConfig<56, 128, 32, 3, 1, 8, 4, 7, 4, 1>;
+// The same tile with 64-deep K blocks for launches over all of K (K ranges keep the 32-deep
+// one): a 7 x 4 tile's short K block does not hide the barrier wait and the first fragment
+// loads at each block boundary (16-deep blocks had measured 13.5 % slower at 1024^3). 1024^3
+// 44.0-45.0 -> 49.2 TFLOP/s, 1024^2 x 4096 49.7 -> 55.0, the same bits; the ragged
+// 1000 x 1003 x 997 (producer warps, 4 stages of 46 KB) is unchanged at 38.6.
+using Wide74K64 = FfmaConfig<56, 128, 64, 3, 1, 8, 4, 7, 4, 1>;
 // 32 x 32 tiles of 4 warps, 2 x 4 per thread: for products so small that 64 x 64 tiles leave
 // most SMs idle, four times as many CTAs, each with a quarter of the work. Its FMA issue rate
 // is low, so it pays only while 64 x 64 tiles come to at most about half an SM each: 256^3
@@ -962,6 +996,17 @@ cudaError_t run_any(const Problem& p, int splits = 1, int k_chunk = 0, float* ou
                     TilePart part = TilePart()) {
   return tma_ok(p) ? run<Cfg, true>(p, splits, k_chunk, out, part)
                    : run<Cfg, false>(p, splits, k_chunk, out, part);
+}
+
+// The 256 x 128 and 56 x 128 tiles with 64-deep K blocks where the launch covers all of K
+// (`whole_k`), the 256 x 128 one on the TMA path only; the 32-deep configurations otherwise.
+cudaError_t run_huge(const Problem& p, bool whole_k, const TilePart& part) {
+  if (whole_k && tma_ok(p)) return run<Huge64, true>(p, 1, 0, nullptr, part);
+  return run_any<Huge>(p, 1, 0, nullptr, part);
+}
+cudaError_t run_wide74(const Problem& p, bool whole_k, const TilePart& part) {
+  return whole_k ? run_any<Wide74K64>(p, 1, 0, nullptr, part)
+                 : run_any<Wide74>(p, 1, 0, nullptr, part);
 }
 
 }  // namespace
@@ -1108,7 +1153,7 @@ cudaError_t run_pick(FfmaPick pick, const Problem& p, Ts... args) {
 
 // 256 x 128 tiles in whole rounds over the SMs, then the rest of them as 64 x 64 tiles in a
 // second launch (disjoint parts of C, so the order of the two launches changes no bit).
-cudaError_t run_huge_tail(const Problem& p, int sms, const TilePart& range) {
+cudaError_t run_huge_tail(const Problem& p, int sms, const TilePart& range, bool whole_k) {
   const int64_t tiles = ((p.M + 255) / 256) * ((p.N + 127) / 128);
   const int64_t main = tiles / sms * sms;
   TilePart head = range, tail = range;
@@ -1116,7 +1161,7 @@ cudaError_t run_huge_tail(const Problem& p, int sms, const TilePart& range) {
   head.wbn = tail.wbn = Huge::BN;
   head.count = main;
   tail.off = main;
-  cudaError_t e = run_any<Huge>(p, 1, 0, nullptr, head);
+  cudaError_t e = run_huge(p, whole_k, head);
   if (e != cudaSuccess) return e;
   return run_any<Small48>(p, 1, 0, nullptr, tail);
 }
@@ -1157,8 +1202,12 @@ cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int6
     if (kc == 0 && tma_ok(p)) return launch_ffma_persistent(p);
     return run_pick(FfmaPick::kBigShortK, p, 1, 0, nullptr, range);
   }
-  if (pick == FfmaPick::kHuge) return run_any<Huge>(p, 1, 0, nullptr, range);
-  if (pick == FfmaPick::kHugeTail) return run_huge_tail(p, sms, range);
+  // 64-deep K blocks only where this launch covers all of K: a K range's last block would
+  // read past the range, which the TMA unit does not zero-fill.
+  const bool whole_k = kc == 0;
+  if (pick == FfmaPick::kHuge) return run_huge(p, whole_k, range);
+  if (pick == FfmaPick::kHugeTail) return run_huge_tail(p, sms, range, whole_k);
+  if (pick == FfmaPick::kWide74) return run_wide74(p, whole_k, range);
   return run_pick(pick, p, 1, 0, nullptr, range);
 }
 
@@ -1510,7 +1559,7 @@ cudaError_t launch_ffma_persistent(const Problem& p) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   CUtensorMap ta, tb;
-  cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BK, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BKS, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = encode_tmap_f32_2d(&tb, p.B, p.N, p.K, Cfg::BN, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
@@ -1542,7 +1591,7 @@ cudaError_t launch_pstore(const Problem& p) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   CUtensorMap ta, tb, tc;
-  cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BK, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BKS, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e == cudaSuccess) e = encode_tmap_f32_2d(&tb, p.B, p.N, p.K, Cfg::BN, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e == cudaSuccess) e = encode_tmap_f32_2d(&tc, p.C, p.N, p.M, 32, P::ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
@@ -1590,7 +1639,7 @@ cudaError_t launch_ffma_streamk(const Problem& p, float* workspace) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   CUtensorMap ta, tb;
-  cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BK, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  cudaError_t e = encode_tmap_f32_2d(&ta, p.A, p.K, p.M, Cfg::BKS, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = encode_tmap_f32_2d(&tb, p.B, p.N, p.K, Cfg::BN, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;

@@ -406,13 +406,15 @@ def test_tf32x3_sweep_and_long_k_sampled(shape):
 @pytest.mark.parametrize("shape", [(4096, 4096, 4096), (1000, 1003, 997), (1537, 260, 129),
                                    (3, 5, 0), (600, 17, 33), (2100, 130, 1001), (2048, 96, 600),
                                    (3072, 64, 4096), (1500, 700, 2051), (2500, 1000, 3000),
-                                   (1100, 333, 2100), (512, 512, 9000), (3000, 2900, 2600)],
+                                   (1100, 333, 2100), (512, 512, 9000), (3000, 2900, 2600),
+                                   (1024, 1024, 2600)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_host_pipeline_equals_device_entry(shape):
     """Copy-overlapped product of host matrices, by row blocks or by K chunks that resume from
-    the sums stored in C (4096^3, 3072 x 64 x 4096 and the last five shapes; 4096^3 and
-    3000 x 2900 x 2600 have the shorter edge chunks of products with at least 2^23 outputs):
-    the bits of t2s_gemm_f32."""
+    the sums stored in C (4096^3, 3072 x 64 x 4096 and the last six shapes; 4096^3 and
+    3000 x 2900 x 2600 have the shorter edge chunks of products with at least 2^23 outputs, and
+    1024 x 1024 x 2600 runs chunks that are not multiples of 64 on the tile whose whole-K
+    launches take 64-deep K blocks): the bits of t2s_gemm_f32."""
     M, N, K = shape
     A = inputs.uniform(M, K, 31 + M)
     B = inputs.uniform(K, N, 37 + N)
