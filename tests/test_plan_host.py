@@ -19,7 +19,9 @@ def built():
     __graft_entry__.build()
 
 
-# (M, N, K) -> the configuration measured fastest (or within 1 % of it) on GB300.
+# (M, N, K) -> the configuration measured fastest (or within 1 % of it) on GB300, measured with
+# 32-deep K blocks; the 56 x 128 and 256 x 128 tiles have since taken 64-deep blocks over all of K,
+# which made them faster still.
 MEASURED = {
     (256, 256, 256): TINY24,          # 3.1 TFLOP/s; 64 x 64 tiles 2.6
     (384, 384, 384): TINY24,          # 8.8; 64 x 64 tiles 6.7
@@ -27,8 +29,8 @@ MEASURED = {
     (512, 512, 2048): TINY24,         # 20.7; 64 x 64 tiles 17.0
     (640, 640, 640): SMALL48,         # 20.8; 32 x 32 tiles 19.2
     (768, 768, 768): SMALL48,         # 33.2; 32 x 32 tiles 22.9
-    (1024, 1024, 1024): WIDE74,       # 45.0; 128 x 64 tiles of 8 warps 41.4
-    (1024, 1024, 4096): WIDE74,       # 50.3; 128 x 64 tiles of 8 warps 45.9
+    (1024, 1024, 1024): WIDE74,       # 45.0 (48.4-49.2 with 64-deep K blocks); 128 x 64 of 8 warps 41.4
+    (1024, 1024, 4096): WIDE74,       # 50.3 (55.0 with 64-deep K blocks); 128 x 64 of 8 warps 45.9
     (1000, 1003, 997): WIDE74,        # 26.5; 128 x 64 tiles of 8 warps 24.2
     (1280, 1280, 1280): SMALL48,
     (1536, 1536, 1536): BIG88,        # 55.9; 128 x 64 tiles 52.6
@@ -36,7 +38,7 @@ MEASURED = {
     (2048, 2048, 2048): HUGE,         # 55.4 TFLOP/s; 64 x 64 tiles 54.0
     (2560, 2560, 2560): HUGE_TAIL,    # 59.7; 128 x 128 tiles 56.4
     (3072, 3072, 3072): HUGE,         # 63.4; 128 x 128 60.5, with the tail 58.2
-    (4096, 4096, 4096): HUGE_TAIL,    # 65.3; 128 x 128 62.8, 256 x 128 alone 57.0
+    (4096, 4096, 4096): HUGE_TAIL,    # 65.3 (66.0 with 64-deep K blocks); 128 x 128 62.8
     (5120, 5120, 5120): HUGE_TAIL,    # 64.8; 128 x 128 63.6
     (6144, 6144, 6144): HUGE_TAIL,    # 65.6; 128 x 128 63.6
     (8192, 8192, 8192): HUGE_TAIL,    # 66.3; 128 x 128 66.5
