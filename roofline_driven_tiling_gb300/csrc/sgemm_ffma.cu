@@ -956,14 +956,24 @@ using Huge64 = FfmaConfig<256, 128, 64, 2, 4, 2, 2, 8, 16, 4>;
 // 1024^3 37.0 TFLOP/s (BK = 16 and 4 stages: 32.4; 128 x 64 tiles of 8 x 8: 35.8), 2048^3 52.3
 // (128 x 128: 51.1), 2304^3 52.1 (45.9).
 using Small48 = FfmaConfig<64, 64, 32, 3, 2, 2, 2, 4, 8, 1>;
+// With 64-deep K blocks over all of K (3 stages of 32 KB, two CTAs per SM instead of four):
+// 768^3 30.9 -> 35.1 TFLOP/s, 640^3 20.8 -> 22.6, 1280^3 44.2 -> 45.2, the 4096^3 tail 65.9 ->
+// 66.0 per call.
+using Small48K64 = FfmaConfig<64, 64, 64, 3, 2, 2, 2, 4, 8, 1>;
 // 128 x 64 tiles of 4 warps, 8 x 8 per thread (pipelined fragments): about one tile per SM.
 using Tall88 = FfmaConfig<128, 64, 32, 3, 2, 2, 2, 8, 8, 1>;
+// (64-deep K blocks leave one CTA per SM here, three stages of 48 KB: 1792^3 50.0 -> 47.5, so
+// this tile keeps 32-deep ones.)
 // Tiles of 8 warps for problems of at most one tile per SM, where a CTA runs alone on its SM
 // and its latency shows: 128 x 128 of 8 x 8 per thread (1536^3: 55.9 TFLOP/s against 52.6
 // with two 128 x 64 tiles per SM) and 128 x 64 of 8 x 4 per thread (1024^3: 41.4 against
 // 39.9 with 4 warps of 8 x 8).
 using Big88 = FfmaConfig<128, 128, 32, 3, 2, 4, 2, 8, 8, 1>;
 using Tall84 = FfmaConfig<128, 64, 32, 3, 2, 4, 2, 8, 4, 1>;
+// With 64-deep K blocks over all of K: 1408^3 46.7 -> 48.0 TFLOP/s, 1536^3 55.5 -> 55.9
+// (128 x 128); 1152 x 1024 x 512 39.6 -> 41.2 (128 x 64).
+using Big88K64 = FfmaConfig<128, 128, 64, 3, 2, 4, 2, 8, 8, 1>;
+using Tall84K64 = FfmaConfig<128, 64, 64, 3, 2, 4, 2, 8, 4, 1>;
 // 56 x 128 tiles of 8 warps (1 x 8 of 56 x 16), 7 x 4 per thread, A read 4 k values at a time:
 // a 1024 x 1024 C is 19 x 8 = 152 of them, one per SM, where 128 x 64 tiles leave 24 SMs idle
 // and give the busiest SM 14 % more work. Per SM both run the FMA pipe about 70 % busy, so the
@@ -985,6 +995,8 @@ using Wide74K64 = FfmaConfig<56, 128, 64, 3, 1, 8, 4, 7, 4, 1>;
 // against 17.0; 640^3 19.2 against 20.8 and 768^3 22.9 against 33.2 (BK = 16 in 4 stages was
 // slower everywhere, 32 x 64 tiles of 2 x 8 per thread no faster).
 using Tiny24 = FfmaConfig<32, 32, 32, 3, 2, 2, 2, 2, 4, 1>;
+// With 64-deep K blocks over all of K: 384^3 8.8 -> 10.4 TFLOP/s, 512^2 x 2048 19.9 -> 21.6.
+using Tiny24K64 = FfmaConfig<32, 32, 64, 3, 2, 2, 2, 2, 4, 1>;
 
 bool tma_ok(const Problem& p) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.A), b = reinterpret_cast<uintptr_t>(p.B);
@@ -998,15 +1010,11 @@ cudaError_t run_any(const Problem& p, int splits = 1, int k_chunk = 0, float* ou
                    : run<Cfg, false>(p, splits, k_chunk, out, part);
 }
 
-// The 256 x 128 and 56 x 128 tiles with 64-deep K blocks where the launch covers all of K
-// (`whole_k`), the 256 x 128 one on the TMA path only; the 32-deep configurations otherwise.
+// The 256 x 128 tile with 64-deep K blocks where the launch covers all of K (`whole_k`) on the
+// TMA path; the 32-deep configuration otherwise.
 cudaError_t run_huge(const Problem& p, bool whole_k, const TilePart& part) {
   if (whole_k && tma_ok(p)) return run<Huge64, true>(p, 1, 0, nullptr, part);
   return run_any<Huge>(p, 1, 0, nullptr, part);
-}
-cudaError_t run_wide74(const Problem& p, bool whole_k, const TilePart& part) {
-  return whole_k ? run_any<Wide74K64>(p, 1, 0, nullptr, part)
-                 : run_any<Wide74>(p, 1, 0, nullptr, part);
 }
 
 }  // namespace
@@ -1037,13 +1045,17 @@ enum class FfmaPick {
 // 1.04 (never ahead of 128 x 64, so not built), 32 x 32 0.6 (fitted from 256^3 to 768^3); 128 x 128 tiles 1.15 from three tiles per SM on,
 // 1.05 at two and 1.03 at one (with the compact k loop; the fully unrolled one pays only from
 // three); 256 x 128 tiles 1.17 (K >= 256); the 8-warp tiles only where they come to at most
-// one per SM: 128 x 128 1.116, 128 x 64 1.091, 56 x 128 1.043. The 256 x 128 tiles also run
+// one per SM: 128 x 128 1.116, 128 x 64 1.091, 56 x 128 1.043, except that a launch over all
+// of K (`whole_k`), where the 56 x 128 tile runs 64-deep K blocks, takes it at two or more
+// per SM too, at 1.02 (1408^3 51.1 against 48.4 TFLOP/s for 128 x 128 tiles of 8 warps,
+// 1792^3 56.6 against 50.5 for 128 x 64, 2048 x 1024 x 2048 55.0 against 51.6; from 2304^3
+// on the 256 x 128 tiles stay ahead: 60.2 against 57.3). The 256 x 128 tiles also run
 // as whole rounds followed by the rest of their tiles cut into 64 x 64 ones, which the tail
 // spreads over all SMs: floor(tiles / SMs) rounds plus ceil(8 x rest / SMs) small tiles.
 // Every measured winner of the sweep is the model's pick, up to 1 %, including the
-// non-monotone ones (1024^3 goes to 56 x 128 tiles of 8 warps, 1280^3 to 64 x 64, 1536^3 to
-// 128 x 128 of 8 warps, 1792^3 to 128 x 64, 2048^3 and 3072^3 to 256 x 128, 2560^3, 4096^3 and
-// 6144^3 to 256 x 128 with the 64 x 64 tail). `copies` products of this size share the GPU;
+// non-monotone ones (1024^3 goes to 56 x 128 tiles of 8 warps, 1280^3 to 64 x 64, 1408^3 to
+// 56 x 128 again, 1536^3 to 128 x 128 of 8 warps, 1792^3 to 56 x 128, 2048^3 and 3072^3 to
+// 256 x 128, 2560^3, 4096^3 and 6144^3 to 256 x 128 with the 64 x 64 tail). `copies` products of this size share the GPU;
 // they (and K < 256) keep to the one-launch configurations of at most 128 x 128. `cost`, when
 // given, receives the busiest SM's work per k value in the model's units (area / efficiency).
 // Measured against the one-launch tilings (L2 flushed): 16384^2 x 32 51.1 against 47.6 TFLOP/s,
@@ -1052,7 +1064,8 @@ enum class FfmaPick {
 // 128: 58.1 against 59.4).
 constexpr int64_t kPStoreMaxK = 96;
 
-FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, double* cost = nullptr) {
+FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, bool whole_k,
+                   double* cost = nullptr) {
   struct Cand {
     FfmaPick pick;
     int bm, bn;
@@ -1088,8 +1101,11 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, double*
     for (int i = 0; i < 3; ++i) {
       const int64_t tiles = ((M + one[i].bm - 1) / one[i].bm) * ((N + one[i].bn - 1) / one[i].bn) *
                             n_copies;
-      if (tiles > sms) continue;
-      const double cost = static_cast<double>(one[i].bm) * one[i].bn / one[i].eff;
+      const int64_t per_sm = (tiles + sms - 1) / sms;
+      const bool deep_wide = whole_k && n_copies == 1 && one[i].pick == FfmaPick::kWide74;
+      if (per_sm > 1 && !deep_wide) continue;
+      const double cost = static_cast<double>(per_sm) * one[i].bm * one[i].bn /
+                          (per_sm > 1 ? 1.02 : one[i].eff);
       if (cost < best_cost) {
         best = one[i].pick;
         best_cost = cost;
@@ -1163,13 +1179,14 @@ cudaError_t run_huge_tail(const Problem& p, int sms, const TilePart& range, bool
   tail.off = main;
   cudaError_t e = run_huge(p, whole_k, head);
   if (e != cudaSuccess) return e;
-  return run_any<Small48>(p, 1, 0, nullptr, tail);
+  return whole_k ? run_any<Small48K64>(p, 1, 0, nullptr, tail)
+                 : run_any<Small48>(p, 1, 0, nullptr, tail);
 }
 
 }  // namespace
 
 int ffma_plan(int64_t M, int64_t N, int64_t K, int sms) {
-  return static_cast<int>(pick_ffma(M, N, K, sms, 1));
+  return static_cast<int>(pick_ffma(M, N, K, sms, 1, true));
 }
 
 cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int64_t kc,
@@ -1191,7 +1208,8 @@ cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int6
   // choice for two copies (128 x 64).
   if (concurrent > 1)
     return run_pick(span >= 256 ? FfmaPick::kBig : FfmaPick::kBigShortK, p, 1, 0, nullptr, range);
-  FfmaPick pick = pick_ffma(p.M, p.N, span, sms, 1);
+  const bool whole_k = kc == 0;
+  FfmaPick pick = pick_ffma(p.M, p.N, span, sms, 1, whole_k);
   if (pick == FfmaPick::kPersistentStore) {
     // Whole products on the TMA path with an aligned C; otherwise the product's own tiles.
     if (kc == 0 && pstore_ok(p)) return launch_ffma_pstore(p);
@@ -1204,10 +1222,18 @@ cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int6
   }
   // 64-deep K blocks only where this launch covers all of K: a K range's last block would
   // read past the range, which the TMA unit does not zero-fill.
-  const bool whole_k = kc == 0;
   if (pick == FfmaPick::kHuge) return run_huge(p, whole_k, range);
   if (pick == FfmaPick::kHugeTail) return run_huge_tail(p, sms, range, whole_k);
-  if (pick == FfmaPick::kWide74) return run_wide74(p, whole_k, range);
+  if (whole_k) {
+    switch (pick) {
+      case FfmaPick::kWide74: return run_any<Wide74K64>(p, 1, 0, nullptr, range);
+      case FfmaPick::kBig88: return run_any<Big88K64>(p, 1, 0, nullptr, range);
+      case FfmaPick::kTall84: return run_any<Tall84K64>(p, 1, 0, nullptr, range);
+      case FfmaPick::kTiny24: return run_any<Tiny24K64>(p, 1, 0, nullptr, range);
+      case FfmaPick::kSmall48: return run_any<Small48K64>(p, 1, 0, nullptr, range);
+      default: break;
+    }
+  }
   return run_pick(pick, p, 1, 0, nullptr, range);
 }
 
@@ -1276,7 +1302,7 @@ int splitk_choice(int64_t M, int64_t N, int64_t K, int sms) {
   constexpr double kWorkPerKB = 40.9;
   constexpr double kPlaneSumLaunch = 3.0e5;
   double per_k = 0.0;
-  pick_ffma(M, N, K, sms, 1, &per_k);
+  pick_ffma(M, N, K, sms, 1, true, &per_k);
   double best = per_k * static_cast<double>(K);
   int best_s = 1;
   const int64_t max_s = K / 128 < 16 ? K / 128 : 16;
@@ -1284,7 +1310,7 @@ int splitk_choice(int64_t M, int64_t N, int64_t K, int sms) {
     const int64_t kc = splitk_chunk(K, s);
     const int planes = splitk_planes(K, s);
     if (planes < 2) continue;
-    pick_ffma(M, N, kc, sms, planes, &per_k);
+    pick_ffma(M, N, kc, sms, planes, false, &per_k);
     const double plane_kb = static_cast<double>(planes + 1) * static_cast<double>(M) *
                             static_cast<double>(N) * 4.0 / 1000.0;
     const double t = per_k * static_cast<double>(kc) + kWorkPerKB * plane_kb + kPlaneSumLaunch;
@@ -1311,7 +1337,7 @@ cudaError_t launch_ffma_splitk(const Problem& p, int splits, float* workspace) {
   if (sms <= 0) return cudaErrorInvalidDevice;
   // Configuration by the tiles of all chunks together, as for the unsplit product.
   const int chunk = static_cast<int>(kc);
-  cudaError_t e = run_pick(pick_ffma(p.M, p.N, kc, sms, planes), p, planes, chunk, workspace);
+  cudaError_t e = run_pick(pick_ffma(p.M, p.N, kc, sms, planes, false), p, planes, chunk, workspace);
   if (e != cudaSuccess) return e;
   const int64_t n = p.M * p.N;
   const bool v4 = n % 4 == 0 && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0;

@@ -19,28 +19,41 @@ def built():
     __graft_entry__.build()
 
 
-# (M, N, K) -> the configuration measured fastest (or within 1 % of it) on GB300, measured with
-# 32-deep K blocks; the 56 x 128 and 256 x 128 tiles have since taken 64-deep blocks over all of K,
-# which made them faster still.
+# (M, N, K) -> the configuration measured fastest (or within 1 % of it) on GB300: each
+# configuration forced in turn, L2 flushed, best of the timed calls in TFLOP/s, with the
+# current kernels (64-deep K blocks where a launch covers all of K). 256^3, 384^3, 5120^3 and
+# 8192^3 were measured with 32-deep K blocks throughout.
 MEASURED = {
-    (256, 256, 256): TINY24,          # 3.1 TFLOP/s; 64 x 64 tiles 2.6
+    (256, 256, 256): TINY24,          # 3.1; 64 x 64 tiles 2.6
     (384, 384, 384): TINY24,          # 8.8; 64 x 64 tiles 6.7
-    (512, 512, 512): TINY24,          # 14.1; 64 x 64 tiles 12.7
-    (512, 512, 2048): TINY24,         # 20.7; 64 x 64 tiles 17.0
-    (640, 640, 640): SMALL48,         # 20.8; 32 x 32 tiles 19.2
-    (768, 768, 768): SMALL48,         # 33.2; 32 x 32 tiles 22.9
-    (1024, 1024, 1024): WIDE74,       # 45.0 (48.4-49.2 with 64-deep K blocks); 128 x 64 of 8 warps 41.4
-    (1024, 1024, 4096): WIDE74,       # 50.3 (55.0 with 64-deep K blocks); 128 x 64 of 8 warps 45.9
-    (1000, 1003, 997): WIDE74,        # 26.5; 128 x 64 tiles of 8 warps 24.2
-    (1280, 1280, 1280): SMALL48,
-    (1536, 1536, 1536): BIG88,        # 55.9; 128 x 64 tiles 52.6
-    (1792, 1792, 1792): TALL88,
-    (2048, 2048, 2048): HUGE,         # 55.4 TFLOP/s; 64 x 64 tiles 54.0
-    (2560, 2560, 2560): HUGE_TAIL,    # 59.7; 128 x 128 tiles 56.4
-    (3072, 3072, 3072): HUGE,         # 63.4; 128 x 128 60.5, with the tail 58.2
-    (4096, 4096, 4096): HUGE_TAIL,    # 65.3 (66.0 with 64-deep K blocks); 128 x 128 62.8
+    (512, 512, 512): TINY24,          # 15.7; 64 x 64 tiles 14.1
+    (512, 512, 2048): TINY24,         # 21.6; 64 x 64 tiles 19.2
+    (640, 640, 640): SMALL48,         # 22.6; 32 x 32 tiles 19.2
+    (768, 768, 768): SMALL48,         # 36.0; 56 x 128 tiles 25.6
+    (1024, 1024, 512): WIDE74,        # 42.6; 128 x 64 tiles of 8 warps 39.4
+    (1024, 1024, 1024): WIDE74,       # 49.2; 128 x 64 tiles of 8 warps 45.0
+    (1024, 1024, 4096): WIDE74,       # 55.0; 128 x 64 tiles of 8 warps 49.8
+    (1000, 1003, 997): WIDE74,        # 38.6; 128 x 64 tiles of 8 warps 37.1
+    (1152, 1152, 1152): SMALL48,      # 36.1; 56 x 128 tiles 33.7
+    (1280, 1280, 1280): SMALL48,      # 45.2; 56 x 128 tiles 41.9
+    (1408, 1408, 512): WIDE74,        # 44.5; 128 x 128 tiles of 8 warps 44.3
+    (1408, 1408, 1408): WIDE74,       # 51.1; 128 x 128 tiles of 8 warps 48.4
+    (1536, 1536, 1536): BIG88,        # 57.7; 128 x 64 tiles of 8 warps 55.0
+    (1792, 1792, 1792): WIDE74,       # 56.6; 128 x 64 tiles of 8 warps 51.4
+    (2048, 1024, 2048): WIDE74,       # 55.0; 128 x 64 tiles of 8 warps 49.8
+    (1024, 3584, 1024): TALL88,       # 56.2; 128 x 64 tiles of 8 warps 56.2
+    (2048, 2048, 2048): HUGE,         # 56.2; 56 x 128 tiles 56.2
+    (2048, 4096, 1024): HUGE_TAIL,    # 57.9; 128 x 64 tiles 58.1
+    (2304, 2304, 2304): HUGE_TAIL,    # 60.2; 56 x 128 tiles 57.3
+    (2560, 2560, 2560): HUGE_TAIL,    # 60.4; 128 x 128 tiles 56.6
+    (3000, 2000, 1000): HUGE_TAIL,    # 58.1; 64 x 64 tiles 52.4
+    (3072, 3072, 3072): HUGE,         # 64.3; 128 x 128 61.4, with the tail 58.8
+    (3584, 3584, 3584): HUGE_TAIL,    # 63.6; 256 x 128 alone 58.7
+    (4096, 1024, 4096): HUGE,         # 56.8; 56 x 128 tiles 56.8
+    (4096, 4096, 4096): HUGE_TAIL,    # 66.1; 128 x 128 63.5
     (5120, 5120, 5120): HUGE_TAIL,    # 64.8; 128 x 128 63.6
-    (6144, 6144, 6144): HUGE_TAIL,    # 65.6; 128 x 128 63.6
+    (6144, 6144, 6144): HUGE_TAIL,    # 66.5; 128 x 128 63.7
+    (8192, 512, 1024): HUGE,          # 55.0; 56 x 128 tiles 54.2
     (8192, 8192, 8192): HUGE_TAIL,    # 66.3; 128 x 128 66.5
 }
 
@@ -77,15 +90,19 @@ def test_plan_tail_only_with_a_whole_round():
     assert binding.t2s_gemm_f32_plan(2500, 2000, 512, 152) == HUGE_TAIL  # 160 = 152 + 8
 
 
-def test_plan_eight_warp_tiles_only_for_one_round():
+def test_plan_eight_warp_tiles():
     # 152 tiles of 56 x 128 on 152 SMs: one each, 8 warps (128 x 64 tiles: 128, less even).
     assert binding.t2s_gemm_f32_plan(1024, 1024, 512, 152) == WIDE74
     # 1152 rows are 21 tiles of 56: 168 > 152; 9 x 16 = 144 tiles of 128 x 64 fit.
     assert binding.t2s_gemm_f32_plan(1152, 1024, 512, 152) == TALL84
     # 162 tiles of 128 x 64 would need a second round on some SMs: not the 8-warp tile.
     assert binding.t2s_gemm_f32_plan(1152, 1152, 1152, 152) != TALL84
-    assert binding.t2s_gemm_f32_plan(1408, 1408, 1408, 152) == BIG88   # 121 tiles of 128^2
-    assert binding.t2s_gemm_f32_plan(1792, 1792, 512, 152) == TALL88  # 196 tiles of 128^2
+    # The 56 x 128 tile (64-deep K blocks over all of K) also at two or three per SM: 286
+    # tiles at 1408^3, 448 at 1792^3 and 1792^2 x 512.
+    assert binding.t2s_gemm_f32_plan(1408, 1408, 1408, 152) == WIDE74
+    assert binding.t2s_gemm_f32_plan(1792, 1792, 512, 152) == WIDE74
+    # 121 tiles of 128 x 128 on a GPU of 128 SMs, where 286 tiles of 56 x 128 take 3 rounds.
+    assert binding.t2s_gemm_f32_plan(1408, 1408, 1408, 128) == BIG88
 
 
 def test_plan_depends_on_sm_count():
@@ -151,13 +168,13 @@ def test_plan_names():
 
 
 def test_plan_properties_on_random_shapes():
-    """Invariants of the tiling choice on seeded random shapes: a one-round 8-warp tiling
-    only when its tiles fit the SMs once, the tail split only with at least one whole round
+    """Invariants of the tiling choice on seeded random shapes: the 128 x 128 and 128 x 64
+    tilings of 8 warps only when their tiles fit the SMs once, the tail split only with at least one whole round
     of 256 x 128 tiles and K >= 256, and a split-K count that keeps chunks of 128 values."""
     import numpy as np
 
     rng = np.random.default_rng(20261202)
-    one_round = {BIG88: (128, 128), TALL84: (128, 64), WIDE74: (56, 128)}
+    one_round = {BIG88: (128, 128), TALL84: (128, 64)}
     for _ in range(2000):
         M, N = (int(x) for x in rng.integers(1, 9000, size=2))
         K = int(rng.integers(1, 20000))
