@@ -1046,10 +1046,12 @@ enum class FfmaPick {
 // 1.05 at two and 1.03 at one (with the compact k loop; the fully unrolled one pays only from
 // three); 256 x 128 tiles 1.17 (K >= 256); the 8-warp tiles only where they come to at most
 // one per SM: 128 x 128 1.116, 128 x 64 1.091, 56 x 128 1.043, except that a launch over all
-// of K (`whole_k`), where the 56 x 128 tile runs 64-deep K blocks, takes it at two or more
-// per SM too, at 1.02 (1408^3 51.1 against 48.4 TFLOP/s for 128 x 128 tiles of 8 warps,
-// 1792^3 56.6 against 50.5 for 128 x 64, 2048 x 1024 x 2048 55.0 against 51.6; from 2304^3
-// on the 256 x 128 tiles stay ahead: 60.2 against 57.3). The 256 x 128 tiles also run
+// of K (`whole_k`) with K >= 512, where the 56 x 128 tile runs at least eight 64-deep K
+// blocks, takes it at two or more per SM too, at 1.02 (1408^3 51.1 against 48.4 TFLOP/s for
+// 128 x 128 tiles of 8 warps, 1792^3 56.6 against 50.5 for 128 x 64, 2048 x 1024 x 2048 55.0
+// against 51.6, 1408^2 x 512 44.5 against 44.3; from 2304^3 on the 256 x 128 tiles stay ahead:
+// 60.2 against 57.3; at K = 256 level, at K = 128 behind: 2048^2 x 128 34.3 against 36.7 for
+// 64 x 64 tiles, 1408^2 x 128 26.7 against 29.9). The 256 x 128 tiles also run
 // as whole rounds followed by the rest of their tiles cut into 64 x 64 ones, which the tail
 // spreads over all SMs: floor(tiles / SMs) rounds plus ceil(8 x rest / SMs) small tiles.
 // Every measured winner of the sweep is the model's pick, up to 1 %, including the
@@ -1102,7 +1104,7 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, bool wh
       const int64_t tiles = ((M + one[i].bm - 1) / one[i].bm) * ((N + one[i].bn - 1) / one[i].bn) *
                             n_copies;
       const int64_t per_sm = (tiles + sms - 1) / sms;
-      const bool deep_wide = whole_k && n_copies == 1 && one[i].pick == FfmaPick::kWide74;
+      const bool deep_wide = whole_k && n_copies == 1 && K >= 512 && one[i].pick == FfmaPick::kWide74;
       if (per_sm > 1 && !deep_wide) continue;
       const double cost = static_cast<double>(per_sm) * one[i].bm * one[i].bn /
                           (per_sm > 1 ? 1.02 : one[i].eff);

@@ -503,14 +503,21 @@ DISPATCH_SHAPES = {
     "persistent_k32": (2560, 2560, 32),    # 400 tiles of 128^2, one K block (cp.async: 1)
     "pstore_k32": (8192, 4096, 32),        # 1024 tiles of 256 x 128, TMA stores (cp.async: 1)
     "pstore_k96": (3000, 4100, 96),        # 384 tiles of 256 x 128, ragged edges of C
-    "tall88_1792": (1792, 1792, 512),      # 392 tiles of 128 x 64: 8 x 8 per thread, pipelined
+    "tall88_1024": (1024, 3584, 1024),     # 448 tiles of 128 x 64: 8 x 8 per thread, pipelined
     "tall84_1152": (1152, 1024, 512),      # 144 tiles of 128 x 64, 8 warps of 8 x 4
     "wide74_1024": (1024, 1024, 512),      # 152 tiles of 56 x 128, 8 warps of 7 x 4
+    "wide74_1792": (1792, 1792, 516),      # 448 tiles of 56 x 128: three per SM
     "big88_1536": (1536, 1536, 512),       # 144 tiles of 128 x 128, 8 warps of 8 x 8
     "small48_2048": (2048, 2048, 128),     # 1024 tiles of 64 x 64: 4 x 8 per thread, pipelined
     "small48_640": (640, 700, 300),        # 110 tiles of 64 x 64
     "tiny24_384": (384, 384, 384),         # 144 tiles of 32 x 32, 2 x 4 per thread
 }
+
+
+# The plan code (t2s_gemm_f32_plan) each name stands for, by its prefix.
+DISPATCH_PLANS = {"big_flat": 0, "big_short_k": 1, "tall88": 2, "small48": 3, "huge_tail": 5,
+                  "huge": 4, "big88": 6, "tall84": 7, "persistent": 8, "wide74": 9, "tiny24": 10,
+                  "pstore": 11}
 
 
 @pytest.mark.parametrize("ragged", [False, True], ids=["tma", "cpasync"])
@@ -519,6 +526,9 @@ def test_every_configuration(name, ragged):
     M, N, K = DISPATCH_SHAPES[name]
     if ragged:
         N, K = N - 1, K - 3
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        code = next(v for k, v in DISPATCH_PLANS.items() if name.startswith(k))
+        assert binding.t2s_gemm_f32_plan(M, N, K, 152) == code
     A = inputs.uniform(M, K, 61 + M)
     B = inputs.uniform(K, N, 67 + N)
     C = run("ffma", A, B)

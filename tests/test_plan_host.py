@@ -97,10 +97,12 @@ def test_plan_eight_warp_tiles():
     assert binding.t2s_gemm_f32_plan(1152, 1024, 512, 152) == TALL84
     # 162 tiles of 128 x 64 would need a second round on some SMs: not the 8-warp tile.
     assert binding.t2s_gemm_f32_plan(1152, 1152, 1152, 152) != TALL84
-    # The 56 x 128 tile (64-deep K blocks over all of K) also at two or three per SM: 286
-    # tiles at 1408^3, 448 at 1792^3 and 1792^2 x 512.
+    # The 56 x 128 tile (64-deep K blocks over all of K) also at two or three per SM from
+    # K = 512 on: 286 tiles at 1408^3, 448 at 1792^3 and 1792^2 x 512; not at K = 128.
     assert binding.t2s_gemm_f32_plan(1408, 1408, 1408, 152) == WIDE74
     assert binding.t2s_gemm_f32_plan(1792, 1792, 512, 152) == WIDE74
+    assert binding.t2s_gemm_f32_plan(2048, 2048, 128, 152) == SMALL48  # 36.7 against 34.3
+    assert binding.t2s_gemm_f32_plan(1408, 1408, 128, 152) == BIG88    # 29.9 against 26.7
     # 121 tiles of 128 x 128 on a GPU of 128 SMs, where 286 tiles of 56 x 128 take 3 rounds.
     assert binding.t2s_gemm_f32_plan(1408, 1408, 1408, 128) == BIG88
 
