@@ -986,7 +986,9 @@ using Wide74 = FfmaConfig<56, 128, 32, 3, 1, 8, 4, 7, 4, 1>;
 // one): a 7 x 4 tile's short K block does not hide the barrier wait and the first fragment
 // loads at each block boundary (16-deep blocks had measured 13.5 % slower at 1024^3). 1024^3
 // 44.0-45.0 -> 49.2 TFLOP/s, 1024^2 x 4096 49.7 -> 55.0, the same bits; the ragged
-// 1000 x 1003 x 997 (producer warps, 4 stages of 46 KB) is unchanged at 38.6.
+// 1000 x 1003 x 997 (producer warps, 4 stages of 46 KB) is unchanged at 38.6. Unlike the
+// other 8-warp tiles it also pays at two or three tiles per SM once K >= 512 (1408^3 51.1,
+// 1792^3 56.6 TFLOP/s; see pick_ffma).
 using Wide74K64 = FfmaConfig<56, 128, 64, 3, 1, 8, 4, 7, 4, 1>;
 // 32 x 32 tiles of 4 warps, 2 x 4 per thread: for products so small that 64 x 64 tiles leave
 // most SMs idle, four times as many CTAs, each with a quarter of the work. Its FMA issue rate
