@@ -45,14 +45,14 @@ F16_PROFILE = os.path.join(ROOT, "profiles", "gemm_f16_4096.md")
 F64_PROFILE = os.path.join(ROOT, "profiles", "dgemm_f64_2048.md")
 # Codes of t2s_gemm_f32_plan.
 PLAN_HUGE_TAIL = 5
-# Tiles as BM x BN x BK (the K-block depth); the 256 x 128 and 56 x 128 tiles take 64-deep K
-# blocks when a launch covers all of K (256 x 128 on the TMA path only).
+# Tiles as BM x BN x BK (the K-block depth) of a launch over all of K: every tile but the 4-warp
+# 128 x 128 and 128 x 64 ones then takes 64-deep K blocks (256 x 128 on the TMA path only).
 PLAN_NAMES = {0: "128x128x32 tiles", 1: "128x128x32 tiles, compact k loop", 2: "128x64x32 tiles",
-              3: "64x64x32 tiles", 4: "256x128x64 tiles",
-              5: "256x128x64 tiles in whole rounds over the SMs, the rest as 64x64x32 tiles "
-                 "in a second launch", 6: "128x128x32 tiles of 8 warps",
-              7: "128x64x32 tiles of 8 warps", 8: "128x128x32 tiles on a persistent grid",
-              9: "56x128x64 tiles of 8 warps", 10: "32x32x32 tiles",
+              3: "64x64x64 tiles", 4: "256x128x64 tiles",
+              5: "256x128x64 tiles in whole rounds over the SMs, the rest as 64x64x64 tiles "
+                 "in a second launch", 6: "128x128x64 tiles of 8 warps",
+              7: "128x64x64 tiles of 8 warps", 8: "128x128x32 tiles on a persistent grid",
+              9: "56x128x64 tiles of 8 warps", 10: "32x32x64 tiles",
               11: "256x128x32 tiles on a persistent grid with TMA stores of C"}
 
 KERNEL_SOURCES = {
