@@ -995,6 +995,11 @@ using Wide74 = FfmaConfig<56, 128, 32, 3, 1, 8, 4, 7, 4, 1>;
 // other 8-warp tiles it also pays at two or three tiles per SM once K >= 512 (1408^3 51.1,
 // 1792^3 56.6 TFLOP/s; see pick_ffma).
 using Wide74K64 = FfmaConfig<56, 128, 64, 3, 1, 8, 4, 7, 4, 1>;
+// The same in 2 stages (94 KB), so that two CTAs share an SM, on the TMA path where the tiles
+// outnumber the SMs: 1408^3 50.2 -> 52.1 TFLOP/s, 1792^3 56.6 -> 58.4, 1792^2 x 512 49.7 ->
+// 53.0, 1408^2 x 512 44.4 -> 46.5, 2048 x 1024 x 2048 55.0 -> 55.7. At one tile per SM the
+// CTA runs alone and keeps the deeper ring.
+using Wide74K64T = FfmaConfig<56, 128, 64, 2, 1, 8, 4, 7, 4, 1>;
 // 32 x 32 tiles of 4 warps, 2 x 4 per thread: for products so small that 64 x 64 tiles leave
 // most SMs idle, four times as many CTAs, each with a quarter of the work. Its FMA issue rate
 // is low, so it pays only while 64 x 64 tiles come to at most about half an SM each: 256^3
@@ -1022,6 +1027,14 @@ cudaError_t run_any(const Problem& p, int splits = 1, int k_chunk = 0, float* ou
 cudaError_t run_huge(const Problem& p, bool whole_k, const TilePart& part) {
   if (whole_k && tma_ok(p)) return run<Huge64, true>(p, 1, 0, nullptr, part);
   return run_any<Huge>(p, 1, 0, nullptr, part);
+}
+
+// The 56 x 128 tile over all of K: 2 stages (two CTAs per SM) on the TMA path when there are
+// more tiles than SMs, else 3.
+cudaError_t run_wide74_whole(const Problem& p, int sms, const TilePart& part) {
+  if (tma_ok(p) && ((p.M + 55) / 56) * ((p.N + 127) / 128) > sms)
+    return run<Wide74K64T, true>(p, 1, 0, nullptr, part);
+  return run_any<Wide74K64>(p, 1, 0, nullptr, part);
 }
 
 // The 64 x 64 tile over all of K: 2 stages on the TMA path, 3 on the general path.
@@ -1054,29 +1067,33 @@ enum class FfmaPick {
 
 // Picks the configuration whose busiest SM has the least work: ceil(tiles / SMs) tiles of the
 // configuration's area, divided by its relative efficiency per FLOP, fitted to a sweep of square
-// and rectangular shapes from 768 to 8192 on GB300: 64 x 64 tiles 1.0, 128 x 64 1.05, 64 x 128
-// 1.04 (never ahead of 128 x 64, so not built), 32 x 32 0.6 (fitted from 256^3 to 768^3); 128 x 128 tiles 1.15 from three tiles per SM on,
-// 1.05 at two and 1.03 at one (with the compact k loop; the fully unrolled one pays only from
-// three); 256 x 128 tiles 1.17 (K >= 256); the 8-warp tiles only where they come to at most
-// one per SM: 128 x 128 1.116, 128 x 64 1.091, 56 x 128 1.043, except that a launch over all
-// of K (`whole_k`) with K >= 512, where the 56 x 128 tile runs at least eight 64-deep K
-// blocks, takes it at two or more per SM too, at 1.02 (1408^3 51.1 against 48.4 TFLOP/s for
-// 128 x 128 tiles of 8 warps, 1792^3 56.6 against 50.5 for 128 x 64, 2048 x 1024 x 2048 55.0
-// against 51.6, 1408^2 x 512 44.5 against 44.3; from 2304^3 on the 256 x 128 tiles stay ahead:
-// 60.2 against 57.3; at K = 256 level, at K = 128 behind: 2048^2 x 128 34.3 against 36.7 for
-// 64 x 64 tiles, 1408^2 x 128 26.7 against 29.9). The 256 x 128 tiles also run
-// as whole rounds followed by the rest of their tiles cut into 64 x 64 ones, which the tail
-// spreads over all SMs: floor(tiles / SMs) rounds plus ceil(8 x rest / SMs) small tiles.
-// Every measured winner of the sweep is the model's pick, up to 1 %, including the
+// and rectangular shapes from 768 to 8192 on GB300:
+//  * 64 x 64 tiles 1.0; 128 x 64 1.05; 64 x 128 1.04 (never ahead of 128 x 64, so not built);
+//    32 x 32 0.6 (fitted from 256^3 to 768^3);
+//  * 128 x 128 tiles 1.15 from three tiles per SM on, 1.05 at two and 1.03 at one (with the
+//    compact k loop; the fully unrolled one pays only from three);
+//  * 256 x 128 tiles 1.17 (K >= 256). They also run as whole rounds followed by the rest of
+//    their tiles cut into 64 x 64 ones, which the tail spreads over all SMs: floor(tiles / SMs)
+//    rounds plus ceil(8 x rest / SMs) small tiles;
+//  * the 8-warp tiles where they come to at most one per SM: 128 x 128 1.116, 128 x 64 1.091,
+//    56 x 128 1.043;
+//  * the 56 x 128 tile also at two or more per SM in a launch over all of K (`whole_k`) with
+//    K >= 128, where it runs 64-deep K blocks in 2 stages, two CTAs per SM: 1.05 (1408^3 52.2
+//    against 48.4 TFLOP/s for 128 x 128 tiles of 8 warps, 1792^3 58.4 against 50.5 for 128 x 64,
+//    2048^3 58.1 against 56.2 and 4096 x 1024 x 4096 59.0 against 56.8 for one round of
+//    256 x 128, 896 x 5760 x 256 49.0 against 42.6 for 256 x 128 with the tail; from 2304^3 on
+//    the 256 x 128 tiles stay ahead, 60.4 against 59.3; level at K = 128).
+// Every measured winner of the sweep is the model's pick, up to 1-2 %, including the
 // non-monotone ones (1024^3 goes to 56 x 128 tiles of 8 warps, 1280^3 to 64 x 64, 1408^3 to
-// 56 x 128 again, 1536^3 to 128 x 128 of 8 warps, 1792^3 to 56 x 128, 2048^3 and 3072^3 to
-// 256 x 128, 2560^3, 4096^3 and 6144^3 to 256 x 128 with the 64 x 64 tail). `copies` products of this size share the GPU;
-// they (and K < 256) keep to the one-launch configurations of at most 128 x 128. `cost`, when
-// given, receives the busiest SM's work per k value in the model's units (area / efficiency).
-// Measured against the one-launch tilings (L2 flushed): 16384^2 x 32 51.1 against 47.6 TFLOP/s,
-// 16384^2 x 16 25.4 against 23.5, 8192 x 4096 x 32 43.1 against 39.8, 8192^2 x 64 54.2
-// against 53.6, 6144^2 x 96 54.2 against 53.4; from K = 128 on the plain tiles win (8192^2 x
-// 128: 58.1 against 59.4).
+// 56 x 128 again, 1536^3 to 128 x 128 of 8 warps, 1792^3 and 2048^3 to 56 x 128, 3072^3 to
+// 256 x 128, 2304^3, 2560^3, 4096^3 and 6144^3 to 256 x 128 with the 64 x 64 tail).
+// `copies` products of this size share the GPU; they (and K < 256) keep to the one-launch
+// configurations of at most 128 x 128. `cost`, when given, receives the busiest SM's work per
+// k value in the model's units (area / efficiency).
+// Short K: measured against the one-launch tilings (L2 flushed): 16384^2 x 32 51.1 against
+// 47.6 TFLOP/s, 16384^2 x 16 25.4 against 23.5, 8192 x 4096 x 32 43.1 against 39.8, 8192^2 x
+// 64 54.2 against 53.6, 6144^2 x 96 54.2 against 53.4; from K = 128 on the plain tiles win
+// (8192^2 x 128: 58.1 against 59.4).
 constexpr int64_t kPStoreMaxK = 96;
 
 FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, bool whole_k,
@@ -1117,10 +1134,10 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, bool wh
       const int64_t tiles = ((M + one[i].bm - 1) / one[i].bm) * ((N + one[i].bn - 1) / one[i].bn) *
                             n_copies;
       const int64_t per_sm = (tiles + sms - 1) / sms;
-      const bool deep_wide = whole_k && n_copies == 1 && K >= 512 && one[i].pick == FfmaPick::kWide74;
+      const bool deep_wide = whole_k && n_copies == 1 && K >= 128 && one[i].pick == FfmaPick::kWide74;
       if (per_sm > 1 && !deep_wide) continue;
       const double cost = static_cast<double>(per_sm) * one[i].bm * one[i].bn /
-                          (per_sm > 1 ? 1.02 : one[i].eff);
+                          (per_sm > 1 ? 1.05 : one[i].eff);
       if (cost < best_cost) {
         best = one[i].pick;
         best_cost = cost;
@@ -1240,7 +1257,7 @@ cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int6
   if (pick == FfmaPick::kHugeTail) return run_huge_tail(p, sms, range, whole_k);
   if (whole_k) {
     switch (pick) {
-      case FfmaPick::kWide74: return run_any<Wide74K64>(p, 1, 0, nullptr, range);
+      case FfmaPick::kWide74: return run_wide74_whole(p, sms, range);
       case FfmaPick::kBig88: return run_any<Big88K64>(p, 1, 0, nullptr, range);
       case FfmaPick::kTall84: return run_any<Tall84K64>(p, 1, 0, nullptr, range);
       case FfmaPick::kTiny24: return run_any<Tiny24K64>(p, 1, 0, nullptr, range);

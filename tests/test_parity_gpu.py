@@ -496,7 +496,7 @@ def test_vector_add_matches_oracle(n, shift):
 # comments), each on the TMA path (aligned) and the cp.async path (K and N not multiples of 4).
 DISPATCH_SHAPES = {
     "big_flat": (128, 131072, 288),        # 1024 tiles of 128^2 (7 per SM), K >= 256
-    "huge_2048": (2048, 2048, 512),        # 128 tiles of 256 x 128: one round
+    "huge_2560": (2560, 1920, 512),        # 150 tiles of 256 x 128: one round
     "huge_tail_2500": (2500, 2000, 512),   # 160 tiles of 256 x 128: 152, then 8 as 64 x 64
     "huge_tail_4096": (4096, 4096, 1024),  # 512 tiles of 256 x 128: 456, then 56 as 64 x 64
     "big_short_k": (3072, 3072, 128),      # 576 tiles of 128^2, K < 256
@@ -508,7 +508,7 @@ DISPATCH_SHAPES = {
     "wide74_1024": (1024, 1024, 512),      # 152 tiles of 56 x 128, 8 warps of 7 x 4
     "wide74_1792": (1792, 1792, 516),      # 448 tiles of 56 x 128: three per SM
     "big88_1536": (1536, 1536, 512),       # 144 tiles of 128 x 128, 8 warps of 8 x 8
-    "small48_2048": (2048, 2048, 128),     # 1024 tiles of 64 x 64: 4 x 8 per thread, pipelined
+    "small48_1280": (1280, 1280, 256),     # 400 tiles of 64 x 64: 4 x 8 per thread, pipelined
     "small48_640": (640, 700, 300),        # 110 tiles of 64 x 64
     "tiny24_384": (384, 384, 384),         # 144 tiles of 32 x 32, 2 x 4 per thread
 }

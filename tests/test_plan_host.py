@@ -21,8 +21,9 @@ def built():
 
 # (M, N, K) -> the configuration measured fastest (or within 1 % of it) on GB300: each
 # configuration forced in turn, L2 flushed, best of the timed calls in TFLOP/s, with the
-# current kernels (64-deep K blocks where a launch covers all of K). 256^3, 384^3, 5120^3 and
-# 8192^3 were measured with 32-deep K blocks throughout.
+# current kernels (64-deep K blocks where a launch covers all of K; the 56 x 128 and 64 x 64
+# tiles in 2 stages where their CTAs share SMs). 256^3, 384^3, 5120^3 and 8192^3 were measured
+# with 32-deep K blocks throughout.
 MEASURED = {
     (256, 256, 256): TINY24,          # 3.1; 64 x 64 tiles 2.6
     (384, 384, 384): TINY24,          # 8.8; 64 x 64 tiles 6.7
@@ -34,26 +35,29 @@ MEASURED = {
     (1024, 1024, 1024): WIDE74,       # 49.2; 128 x 64 tiles of 8 warps 45.0
     (1024, 1024, 4096): WIDE74,       # 55.0; 128 x 64 tiles of 8 warps 49.8
     (1000, 1003, 997): WIDE74,        # 38.6; 128 x 64 tiles of 8 warps 37.1
-    (1152, 1152, 1152): SMALL48,      # 36.1; 56 x 128 tiles 33.7
-    (1280, 1280, 1280): SMALL48,      # 45.2; 56 x 128 tiles 41.9
-    (1408, 1408, 512): WIDE74,        # 44.5; 128 x 128 tiles of 8 warps 44.3
-    (1408, 1408, 1408): WIDE74,       # 51.1; 128 x 128 tiles of 8 warps 48.4
-    (1536, 1536, 1536): BIG88,        # 57.7; 128 x 64 tiles of 8 warps 55.0
-    (1792, 1792, 1792): WIDE74,       # 56.6; 128 x 64 tiles of 8 warps 51.4
-    (2048, 1024, 2048): WIDE74,       # 55.0; 128 x 64 tiles of 8 warps 49.8
+    (1152, 1152, 1152): SMALL48,      # 38.0; 56 x 128 tiles 34.5
+    (1280, 1280, 1280): SMALL48,      # 47.3; 56 x 128 tiles 43.2
+    (1408, 1408, 256): WIDE74,        # 40.4; 128 x 128 tiles of 8 warps 37.4
+    (1408, 1408, 512): WIDE74,        # 46.5; 128 x 128 tiles of 8 warps 44.3
+    (1408, 1408, 1408): WIDE74,       # 52.2; 128 x 128 tiles of 8 warps 48.4
+    (1536, 1536, 1536): BIG88,        # 56.8-57.7; 128 x 64 tiles of 8 warps 55.1
+    (1792, 1792, 1792): WIDE74,       # 58.4; 128 x 64 tiles of 8 warps 51.0
+    (2048, 1024, 2048): WIDE74,       # 55.7; 128 x 64 tiles of 8 warps 49.8
     (1024, 3584, 1024): TALL88,       # 56.2; 128 x 64 tiles of 8 warps 56.2
-    (2048, 2048, 2048): HUGE,         # 56.2; 56 x 128 tiles 56.2
-    (2048, 4096, 1024): HUGE_TAIL,    # 57.9; 128 x 64 tiles 58.1
-    (2304, 2304, 2304): HUGE_TAIL,    # 60.2; 56 x 128 tiles 57.3
-    (2560, 2560, 2560): HUGE_TAIL,    # 60.4; 128 x 128 tiles 56.6
-    (3000, 2000, 1000): HUGE_TAIL,    # 58.1; 64 x 64 tiles 52.4
-    (3072, 3072, 3072): HUGE,         # 64.3; 128 x 128 61.4, with the tail 58.8
+    (896, 5760, 256): WIDE74,         # 49.0; 256 x 128 with the tail 42.6
+    (2048, 2048, 2048): WIDE74,       # 58.1; 256 x 128 tiles 56.2
+    (2048, 4096, 1024): HUGE_TAIL,    # 58.7; 128 x 64 tiles and 56 x 128 tiles 58.1
+    (2304, 2304, 2304): HUGE_TAIL,    # 60.4; 56 x 128 tiles 59.3
+    (2560, 1920, 512): HUGE,          # 61.0; 56 x 128 tiles 50.9
+    (2560, 2560, 2560): HUGE_TAIL,    # 61.1; 128 x 128 tiles 56.6
+    (3000, 2000, 1000): HUGE_TAIL,    # 52.9-58.1; 56 x 128 tiles 53.6
+    (3072, 3072, 3072): HUGE,         # 64.3; 128 x 128 61.6, with the tail 59.4
     (3584, 3584, 3584): HUGE_TAIL,    # 63.6; 256 x 128 alone 58.7
-    (4096, 1024, 4096): HUGE,         # 56.8; 56 x 128 tiles 56.8
-    (4096, 4096, 4096): HUGE_TAIL,    # 66.1; 128 x 128 63.5
+    (4096, 1024, 4096): WIDE74,       # 59.0; 256 x 128 tiles 56.8
+    (4096, 4096, 4096): HUGE_TAIL,    # 66.4; 128 x 128 63.5
     (5120, 5120, 5120): HUGE_TAIL,    # 64.8; 128 x 128 63.6
     (6144, 6144, 6144): HUGE_TAIL,    # 66.5; 128 x 128 63.7
-    (8192, 512, 1024): HUGE,          # 55.0; 56 x 128 tiles 54.2
+    (8192, 512, 1024): WIDE74,        # 56.5; 256 x 128 tiles 55.0
     (8192, 8192, 8192): HUGE_TAIL,    # 66.3; 128 x 128 66.5
 }
 
@@ -84,7 +88,7 @@ def test_plan_short_k_and_copies():
 
 def test_plan_tail_only_with_a_whole_round():
     # Fewer 256 x 128 tiles than SMs: no whole round, so no split launch.
-    assert binding.t2s_gemm_f32_plan(2048, 2048, 512, 152) == HUGE  # 128 tiles
+    assert binding.t2s_gemm_f32_plan(2560, 1920, 512, 152) == HUGE  # 150 tiles
     # A whole number of rounds: nothing left for a tail.
     assert binding.t2s_gemm_f32_plan(256 * 19, 128 * 16, 1024, 152) != HUGE_TAIL  # 304 tiles
     assert binding.t2s_gemm_f32_plan(2500, 2000, 512, 152) == HUGE_TAIL  # 160 = 152 + 8
@@ -97,12 +101,13 @@ def test_plan_eight_warp_tiles():
     assert binding.t2s_gemm_f32_plan(1152, 1024, 512, 152) == TALL84
     # 162 tiles of 128 x 64 would need a second round on some SMs: not the 8-warp tile.
     assert binding.t2s_gemm_f32_plan(1152, 1152, 1152, 152) != TALL84
-    # The 56 x 128 tile (64-deep K blocks over all of K) also at two or three per SM from
-    # K = 512 on: 286 tiles at 1408^3, 448 at 1792^3 and 1792^2 x 512; not at K = 128.
+    # The 56 x 128 tile (64-deep K blocks over all of K, two CTAs per SM) also at two or more
+    # per SM from K = 128 on: 286 tiles at 1408^3, 448 at 1792^3 and 1792^2 x 512, 592 at
+    # 2048^2 x 128 (level with 64 x 64 tiles: 39.5 against 39.4); not below K = 128.
     assert binding.t2s_gemm_f32_plan(1408, 1408, 1408, 152) == WIDE74
     assert binding.t2s_gemm_f32_plan(1792, 1792, 512, 152) == WIDE74
-    assert binding.t2s_gemm_f32_plan(2048, 2048, 128, 152) == SMALL48  # 36.7 against 34.3
-    assert binding.t2s_gemm_f32_plan(1408, 1408, 128, 152) == BIG88    # 29.9 against 26.7
+    assert binding.t2s_gemm_f32_plan(2048, 2048, 128, 152) == WIDE74
+    assert binding.t2s_gemm_f32_plan(1408, 1408, 127, 152) == BIG88
     # 121 tiles of 128 x 128 on a GPU of 128 SMs, where 286 tiles of 56 x 128 take 3 rounds.
     assert binding.t2s_gemm_f32_plan(1408, 1408, 1408, 128) == BIG88
 
@@ -122,7 +127,7 @@ SPLITK_MEASURED = {
     (1000, 1003, 997): 1,      # 26.1; 2 chunks 26.1, 8 chunks 24.6
     (1280, 1280, 1280): 6,     # 48.4; 3 chunks 48.4, the product 44.9
     (1536, 1536, 1536): 1,     # 55.5; 5 chunks 53.1
-    (1792, 1792, 1792): 3,     # 56.6; 6 chunks 55.4, the product 50.0
+    (1792, 1792, 1792): 1,     # the product 58.4 (56 x 128 tiles); 3 chunks 56.6, 6 chunks 55.4
     (2048, 2048, 2048): 4,     # 57.9; 2 chunks 56.4, the product 55.4
     (1024, 1024, 4096): 7,     # 55.5; 8 chunks 53.9, the product 50.2
     (512, 512, 4096): 9,       # 43.1; 8 chunks 40.7, the product 18.0 (64 x 64 tiles)
