@@ -506,9 +506,9 @@ DISPATCH_SHAPES = {
     "tall88_1024": (1024, 3584, 1024),     # 448 tiles of 128 x 64: 8 x 8 per thread, pipelined
     "tall84_1152": (1152, 1024, 512),      # 144 tiles of 128 x 64, 8 warps of 8 x 4
     "wide74_1024": (1024, 1024, 512),      # 152 tiles of 56 x 128, 8 warps of 7 x 4
-    "wide74_1792": (1792, 1792, 516),      # 448 tiles of 56 x 128: three per SM
+    "wide74_1792": (1792, 1792, 516),      # 448 tiles of 56 x 128, 2 stages, two CTAs per SM
     "big88_1536": (1536, 1536, 512),       # 144 tiles of 128 x 128, 8 warps of 8 x 8
-    "small48_1280": (1280, 1280, 256),     # 400 tiles of 64 x 64: 4 x 8 per thread, pipelined
+    "small48_1280": (1280, 1280, 256),     # 400 tiles of 64 x 64, 4 x 8 per thread, 3 CTAs per SM
     "small48_640": (640, 700, 300),        # 110 tiles of 64 x 64
     "tiny24_384": (384, 384, 384),         # 144 tiles of 32 x 32, 2 x 4 per thread
 }
