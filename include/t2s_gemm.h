@@ -100,8 +100,9 @@ int t2s_gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B
  *  - Returns 0: 128 x 128 tiles, k loop unrolled over a K block; 1: 128 x 128 tiles, compact
  *    k loop; 2: 128 x 64 tiles; 3: 64 x 64 tiles; 4: 256 x 128 tiles; 5: 256 x 128 tiles in
  *    whole rounds of `sms` tiles, then the remaining 256 x 128 tiles as 64 x 64 tiles in a
- *    second launch; 6: 128 x 128 tiles of 8 warps; 7: 128 x 64 tiles of 8 warps; 9: 56 x 128
- *    tiles of 8 warps (6, 7 and 9 only for at most one tile per multiprocessor); 8: 128 x 128
+ *    second launch; 6: 128 x 128 tiles of 8 warps; 7: 128 x 64 tiles of 8 warps (6 and 7 only
+ *    for at most one tile per multiprocessor); 9: 56 x 128 tiles of 8 warps (at most one per
+ *    multiprocessor, or from K = 128 on also more, two CTAs sharing each); 8: 128 x 128
  *    tiles on a persistent grid of two CTAs per multiprocessor, one TMA ring across tiles
  *    (K <= 32; on the cp.async path the call runs 1 instead); 10: 32 x 32 tiles (small
  *    products); 11: 256 x 128 tiles on a persistent grid of one CTA per multiprocessor whose
