@@ -947,9 +947,9 @@ using Huge = FfmaConfig<256, 128, 32, 3, 4, 2, 2, 8, 16, 4>;
 // the first fragment loads of the block. It runs the whole-round launches over all of K on the
 // TMA path: 4096^3 65.2 -> 66.0 TFLOP/s, 3072^3 63.4 -> 64.2, 2048^3 55.4 -> 56.2, the same
 // bits. The k loop is unrolled over 4 of its 8 groups: all 8 ran 56.3 at 4096^3 (the code
-// outgrows the instruction cache). K ranges, whose chunk ends TMA does not zero-fill, the
-// general path (a 2-stage ring cannot issue a stage S - 2 blocks ahead) and the short-K kernel
-// keep the 32-deep tile.
+// outgrows the instruction cache). K ranges that end inside K and are not whole 64-deep blocks
+// (TMA zero-fills only beyond K), the general path (a 2-stage ring cannot issue a stage S - 2
+// blocks ahead) and the short-K kernel keep the 32-deep tile.
 using Huge64 = FfmaConfig<256, 128, 64, 2, 4, 2, 2, 8, 16, 4>;
 // 4 x 8 per thread (64 x 64 CTA tiles of 4 warps, BK = 32, 3 stages): many small CTAs (four
 // per SM) that even out the last wave. Measured fastest up to ~2.4 tiles of 128 x 128 per SM:
@@ -987,13 +987,13 @@ using Tall84K64 = FfmaConfig<128, 64, 64, 3, 2, 4, 2, 8, 4, 1>;
 // values at a time in the 128 x 64 tile, 4 x 8 per thread in it, 120 x 64 tiles of 12 warps,
 // 4 stages: none faster.)
 using Wide74 = FfmaConfig<56, 128, 32, 3, 1, 8, 4, 7, 4, 1>;
-// The same tile with 64-deep K blocks for launches over all of K (K ranges keep the 32-deep
-// one): a 7 x 4 tile's short K block does not hide the barrier wait and the first fragment
+// The same tile with 64-deep K blocks for launches over all of K (and K ranges that 64-deep
+// blocks can tile; see launch_ffma_range): a 7 x 4 tile's short K block does not hide the barrier wait and the first fragment
 // loads at each block boundary (16-deep blocks had measured 13.5 % slower at 1024^3). 1024^3
 // 44.0-45.0 -> 49.2 TFLOP/s, 1024^2 x 4096 49.7 -> 55.0, the same bits; the ragged
 // 1000 x 1003 x 997 (producer warps, 4 stages of 46 KB) is unchanged at 38.6. Unlike the
-// other 8-warp tiles it also pays at two or three tiles per SM once K >= 512 (1408^3 51.1,
-// 1792^3 56.6 TFLOP/s; see pick_ffma).
+// other 8-warp tiles it also pays at two or more tiles per SM, in 2 stages (see Wide74K64T
+// and pick_ffma).
 using Wide74K64 = FfmaConfig<56, 128, 64, 3, 1, 8, 4, 7, 4, 1>;
 // The same in 2 stages (94 KB), so that two CTAs share an SM, on the TMA path where the tiles
 // outnumber the SMs: 1408^3 50.2 -> 52.1 TFLOP/s, 1792^3 56.6 -> 58.4, 1792^2 x 512 49.7 ->
@@ -1022,10 +1022,10 @@ cudaError_t run_any(const Problem& p, int splits = 1, int k_chunk = 0, float* ou
                    : run<Cfg, false>(p, splits, k_chunk, out, part);
 }
 
-// The 256 x 128 tile with 64-deep K blocks where the launch covers all of K (`whole_k`) on the
-// TMA path; the 32-deep configuration otherwise.
-cudaError_t run_huge(const Problem& p, bool whole_k, const TilePart& part) {
-  if (whole_k && tma_ok(p)) return run<Huge64, true>(p, 1, 0, nullptr, part);
+// The 256 x 128 tile with 64-deep K blocks where the launch may take them (`deep64`, see
+// launch_ffma_range) on the TMA path; the 32-deep configuration otherwise.
+cudaError_t run_huge(const Problem& p, bool deep64, const TilePart& part) {
+  if (deep64 && tma_ok(p)) return run<Huge64, true>(p, 1, 0, nullptr, part);
   return run_any<Huge>(p, 1, 0, nullptr, part);
 }
 
@@ -1077,7 +1077,7 @@ enum class FfmaPick {
 //    rounds plus ceil(8 x rest / SMs) small tiles;
 //  * the 8-warp tiles where they come to at most one per SM: 128 x 128 1.116, 128 x 64 1.091,
 //    56 x 128 1.043;
-//  * the 56 x 128 tile also at two or more per SM in a launch over all of K (`whole_k`) with
+//  * the 56 x 128 tile also at two or more per SM in a launch of 64-deep K blocks (`deep64`) with
 //    K >= 128, where it runs 64-deep K blocks in 2 stages, two CTAs per SM: 1.05 (1408^3 52.2
 //    against 48.4 TFLOP/s for 128 x 128 tiles of 8 warps, 1792^3 58.4 against 50.5 for 128 x 64,
 //    2048^3 58.1 against 56.2 and 4096 x 1024 x 4096 59.0 against 56.8 for one round of
@@ -1096,7 +1096,7 @@ enum class FfmaPick {
 // (8192^2 x 128: 58.1 against 59.4).
 constexpr int64_t kPStoreMaxK = 96;
 
-FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, bool whole_k,
+FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, bool deep64,
                    double* cost = nullptr) {
   struct Cand {
     FfmaPick pick;
@@ -1134,7 +1134,7 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, bool wh
       const int64_t tiles = ((M + one[i].bm - 1) / one[i].bm) * ((N + one[i].bn - 1) / one[i].bn) *
                             n_copies;
       const int64_t per_sm = (tiles + sms - 1) / sms;
-      const bool deep_wide = whole_k && n_copies == 1 && K >= 128 && one[i].pick == FfmaPick::kWide74;
+      const bool deep_wide = deep64 && n_copies == 1 && K >= 128 && one[i].pick == FfmaPick::kWide74;
       if (per_sm > 1 && !deep_wide) continue;
       const double cost = static_cast<double>(per_sm) * one[i].bm * one[i].bn /
                           (per_sm > 1 ? 1.05 : one[i].eff);
@@ -1201,7 +1201,7 @@ cudaError_t run_pick(FfmaPick pick, const Problem& p, Ts... args) {
 
 // 256 x 128 tiles in whole rounds over the SMs, then the rest of them as 64 x 64 tiles in a
 // second launch (disjoint parts of C, so the order of the two launches changes no bit).
-cudaError_t run_huge_tail(const Problem& p, int sms, const TilePart& range, bool whole_k) {
+cudaError_t run_huge_tail(const Problem& p, int sms, const TilePart& range, bool deep64) {
   const int64_t tiles = ((p.M + 255) / 256) * ((p.N + 127) / 128);
   const int64_t main = tiles / sms * sms;
   TilePart head = range, tail = range;
@@ -1209,9 +1209,9 @@ cudaError_t run_huge_tail(const Problem& p, int sms, const TilePart& range, bool
   head.wbn = tail.wbn = Huge::BN;
   head.count = main;
   tail.off = main;
-  cudaError_t e = run_huge(p, whole_k, head);
+  cudaError_t e = run_huge(p, deep64, head);
   if (e != cudaSuccess) return e;
-  return whole_k ? run_small48_whole(p, tail) : run_any<Small48>(p, 1, 0, nullptr, tail);
+  return deep64 ? run_small48_whole(p, tail) : run_any<Small48>(p, 1, 0, nullptr, tail);
 }
 
 }  // namespace
@@ -1239,8 +1239,13 @@ cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int6
   // choice for two copies (128 x 64).
   if (concurrent > 1)
     return run_pick(span >= 256 ? FfmaPick::kBig : FfmaPick::kBigShortK, p, 1, 0, nullptr, range);
-  const bool whole_k = kc == 0;
-  FfmaPick pick = pick_ffma(p.M, p.N, span, sms, 1, whole_k);
+  // 64-deep K blocks where no block reads past this launch's K values: over all of K, a range
+  // that ends at K (zero fill beyond K), or a range of whole 64-deep blocks (the host
+  // pipeline's K chunks of 256 and 1024 values: end to end 4096^3 57.7 -> 58.0 TFLOP/s,
+  // 2048^3 37.1 -> 38.5, the same bits). Other ranges keep 32-deep blocks: the last one would
+  // read past the range, which the TMA unit does not zero-fill.
+  const bool deep64 = kc == 0 || k0 + kc >= p.K || kc % 64 == 0;
+  FfmaPick pick = pick_ffma(p.M, p.N, span, sms, 1, deep64);
   if (pick == FfmaPick::kPersistentStore) {
     // Whole products on the TMA path with an aligned C; otherwise the product's own tiles.
     if (kc == 0 && pstore_ok(p)) return launch_ffma_pstore(p);
@@ -1251,11 +1256,9 @@ cudaError_t launch_ffma_range(const Problem& p, int concurrent, int64_t k0, int6
     if (kc == 0 && tma_ok(p)) return launch_ffma_persistent(p);
     return run_pick(FfmaPick::kBigShortK, p, 1, 0, nullptr, range);
   }
-  // 64-deep K blocks only where this launch covers all of K: a K range's last block would
-  // read past the range, which the TMA unit does not zero-fill.
-  if (pick == FfmaPick::kHuge) return run_huge(p, whole_k, range);
-  if (pick == FfmaPick::kHugeTail) return run_huge_tail(p, sms, range, whole_k);
-  if (whole_k) {
+  if (pick == FfmaPick::kHuge) return run_huge(p, deep64, range);
+  if (pick == FfmaPick::kHugeTail) return run_huge_tail(p, sms, range, deep64);
+  if (deep64) {
     switch (pick) {
       case FfmaPick::kWide74: return run_wide74_whole(p, sms, range);
       case FfmaPick::kBig88: return run_any<Big88K64>(p, 1, 0, nullptr, range);
