@@ -988,12 +988,12 @@ using Tall84K64 = FfmaConfig<128, 64, 64, 3, 2, 4, 2, 8, 4, 1>;
 // 4 stages: none faster.)
 using Wide74 = FfmaConfig<56, 128, 32, 3, 1, 8, 4, 7, 4, 1>;
 // The same tile with 64-deep K blocks for launches over all of K (and K ranges that 64-deep
-// blocks can tile; see launch_ffma_range): a 7 x 4 tile's short K block does not hide the barrier wait and the first fragment
-// loads at each block boundary (16-deep blocks had measured 13.5 % slower at 1024^3). 1024^3
-// 44.0-45.0 -> 49.2 TFLOP/s, 1024^2 x 4096 49.7 -> 55.0, the same bits; the ragged
-// 1000 x 1003 x 997 (producer warps, 4 stages of 46 KB) is unchanged at 38.6. Unlike the
-// other 8-warp tiles it also pays at two or more tiles per SM, in 2 stages (see Wide74K64T
-// and pick_ffma).
+// blocks can tile; see launch_ffma_range): a 7 x 4 tile's short K block does not hide the
+// barrier wait and the first fragment loads at each block boundary (16-deep blocks had
+// measured 13.5 % slower at 1024^3). 1024^3 44.0-45.0 -> 49.2 TFLOP/s, 1024^2 x 4096 49.7 ->
+// 55.0, the same bits; the ragged 1000 x 1003 x 997 (producer warps, 4 stages of 46 KB) is
+// unchanged at 38.6. Unlike the other 8-warp tiles it also pays at two or more tiles per SM,
+// in 2 stages (see Wide74K64T and pick_ffma).
 using Wide74K64 = FfmaConfig<56, 128, 64, 3, 1, 8, 4, 7, 4, 1>;
 // The same in 2 stages (94 KB), so that two CTAs share an SM, on the TMA path where the tiles
 // outnumber the SMs: 1408^3 50.2 -> 52.1 TFLOP/s, 1792^3 56.6 -> 58.4, 1792^2 x 512 49.7 ->
@@ -1077,8 +1077,8 @@ enum class FfmaPick {
 //    rounds plus ceil(8 x rest / SMs) small tiles;
 //  * the 8-warp tiles where they come to at most one per SM: 128 x 128 1.116, 128 x 64 1.091,
 //    56 x 128 1.043;
-//  * the 56 x 128 tile also at two or more per SM in a launch of 64-deep K blocks (`deep64`) with
-//    K >= 128, where it runs 64-deep K blocks in 2 stages, two CTAs per SM: 1.05 (1408^3 52.2
+//  * the 56 x 128 tile also at two or more per SM in a launch of 64-deep K blocks (`deep64`)
+//    with K >= 128, where it runs 64-deep K blocks in 2 stages, two CTAs per SM: 1.05 (1408^3 52.2
 //    against 48.4 TFLOP/s for 128 x 128 tiles of 8 warps, 1792^3 58.4 against 50.5 for 128 x 64,
 //    2048^3 58.1 against 56.2 and 4096 x 1024 x 4096 59.0 against 56.8 for one round of
 //    256 x 128, 896 x 5760 x 256 49.0 against 42.6 for 256 x 128 with the tail; from 2304^3 on
@@ -1134,7 +1134,8 @@ FfmaPick pick_ffma(int64_t M, int64_t N, int64_t K, int sms, int copies, bool de
       const int64_t tiles = ((M + one[i].bm - 1) / one[i].bm) * ((N + one[i].bn - 1) / one[i].bn) *
                             n_copies;
       const int64_t per_sm = (tiles + sms - 1) / sms;
-      const bool deep_wide = deep64 && n_copies == 1 && K >= 128 && one[i].pick == FfmaPick::kWide74;
+      const bool deep_wide =
+          deep64 && n_copies == 1 && K >= 128 && one[i].pick == FfmaPick::kWide74;
       if (per_sm > 1 && !deep_wide) continue;
       const double cost = static_cast<double>(per_sm) * one[i].bm * one[i].bn /
                           (per_sm > 1 ? 1.05 : one[i].eff);
