@@ -70,3 +70,25 @@ def test_kernel_hash_ignores_comments_only():
     assert bench.code_only(a) != bench.code_only(c)
     assert '"a // b"' in bench.code_only(a)
     assert len(bench.kernel_hash("ffma")) == 16
+
+
+def test_profile_traffic_only_for_the_current_source(tmp_path):
+    """The bench takes a kernel's DRAM bytes from a committed summary only when the summary
+    records the hash of the kernel's present code; a stale hash, a missing field or a missing
+    file gives no traffic figure rather than an old one."""
+    import bench
+    current = bench.kernel_hash("ffma")
+    good = tmp_path / "good.md"
+    good.write_text("kernel_source_sha256_16: %s\ndram_bytes_per_launch: 342682624\n" % current)
+    assert bench.profile_traffic(str(good), "ffma") == 342682624.0
+    stale = tmp_path / "stale.md"
+    other = "0" * 16 if current != "0" * 16 else "f" * 16
+    stale.write_text("kernel_source_sha256_16: %s\ndram_bytes_per_launch: 342682624\n" % other)
+    assert bench.profile_traffic(str(stale), "ffma") is None
+    no_bytes = tmp_path / "no_bytes.md"
+    no_bytes.write_text("kernel_source_sha256_16: %s\n" % current)
+    assert bench.profile_traffic(str(no_bytes), "ffma") is None
+    assert bench.profile_traffic(str(tmp_path / "missing.md"), "ffma") is None
+    # A summary taken on another kernel's sources does not serve this one.
+    assert bench.profile_traffic(str(good), "tf32x3") is None or \
+        bench.kernel_hash("tf32x3") == current
