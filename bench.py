@@ -22,11 +22,8 @@ import hashlib
 import json
 import os
 import re
-import shutil
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 
 import numpy as np
@@ -143,62 +140,6 @@ def measured_peaks():
             return json.load(f)
     except (OSError, ValueError):
         return {}
-
-
-class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms (background)."""
-
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = None
-
-    def __enter__(self):
-        if shutil.which("nvidia-smi"):
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
-                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
-        return self
-
-    def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-
-    def summary(self):
-        if not self.path or not os.path.exists(self.path):
-            return None
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for name, flag in zip(names, parts[5:9]):
-                    if flag.lower() == "active":
-                        reasons.add(name)
-        os.unlink(self.path)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
 
 
 # --------------------------------------------------------------------------- CPU leg
@@ -459,6 +400,8 @@ def run_ours(args):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     plan = binding.t2s_gemm_f32_plan(M, N, K, sms)
     launches_per_call = 2 if plan == PLAN_HUGE_TAIL else 1
+    from roofline_driven_tiling_gb300.clocks import ClockSampler
+
     with ClockSampler(torch.cuda.current_device()) as clk:
         times = time_steps(step, args.steps, max(args.warmup, 3), stream, flush)
     clocks = clk.summary()

@@ -124,6 +124,7 @@ def main(argv=None) -> int:
     import torch
 
     from . import binding, inputs, roofline as rl
+    from .clocks import ClockSampler
 
     if not torch.cuda.is_available():
         raise SystemExit("the sweep needs a CUDA device")
@@ -140,64 +141,66 @@ def main(argv=None) -> int:
         torch.set_float32_matmul_precision("highest")
     out = open(args.out, "w") if args.out else None
     rows, bad = [], 0
-    for (M, N, K) in shapes:
-        A, B = inputs.uniform(M, K, SEED_A), inputs.uniform(K, N, SEED_B)
-        dA = torch.zeros(M * K + shift, dtype=torch.float32, device=dev)
-        dB = torch.zeros(K * N + shift, dtype=torch.float32, device=dev)
-        dA[shift:] = torch.from_numpy(A.ravel()).to(dev)
-        dB[shift:] = torch.from_numpy(B.ravel()).to(dev)
-        dC_buf = torch.empty(M * N + shift, dtype=torch.float32, device=dev)
-        dC = dC_buf[shift:].view(M, N)
-        ws = torch.empty(_workspace_bytes(lib, M, N, K, args.splitk_chunks), dtype=torch.uint8,
-                         device=dev)
-        calls = _calls(binding, lib, M, N, K, dA, dB, dC_buf, ws, stream.cuda_stream,
-                       args.splitk_chunks, shift, torch)
-        flops = rl.gemm_flops(M, N, K)
-        tol = 1e-6 * K * float(abs(A).max()) * float(abs(B).max())
-        ref = None
-        for name in kernels:
-            fn = calls[name]
-            with torch.cuda.stream(stream):
-                dC.fill_(float("nan"))
-                fn()
-            torch.cuda.synchronize()
-            if binding.t2s_device_status(stream.cuda_stream) != binding.T2S_OK:
-                raise SystemExit("device status reports a timed-out wait (%s)" % name)
-            if name == "ffma":
-                ref = dC.clone()
-                check = "reference"
-            elif ref is None:
-                check = "unchecked"
-            else:
-                diff = float((dC - ref).abs().max())
-                exact = bool(torch.equal(dC.view(torch.int32), ref.view(torch.int32)))
-                if name in ("naive", "smem32"):
-                    check = "bit-exact" if exact else "MISMATCH"
-                elif exact:
-                    check = "bit-exact"
+    clk = ClockSampler(torch.cuda.current_device())
+    with clk:
+        for (M, N, K) in shapes:
+            A, B = inputs.uniform(M, K, SEED_A), inputs.uniform(K, N, SEED_B)
+            dA = torch.zeros(M * K + shift, dtype=torch.float32, device=dev)
+            dB = torch.zeros(K * N + shift, dtype=torch.float32, device=dev)
+            dA[shift:] = torch.from_numpy(A.ravel()).to(dev)
+            dB[shift:] = torch.from_numpy(B.ravel()).to(dev)
+            dC_buf = torch.empty(M * N + shift, dtype=torch.float32, device=dev)
+            dC = dC_buf[shift:].view(M, N)
+            ws = torch.empty(_workspace_bytes(lib, M, N, K, args.splitk_chunks), dtype=torch.uint8,
+                             device=dev)
+            calls = _calls(binding, lib, M, N, K, dA, dB, dC_buf, ws, stream.cuda_stream,
+                           args.splitk_chunks, shift, torch)
+            flops = rl.gemm_flops(M, N, K)
+            tol = 1e-6 * K * float(abs(A).max()) * float(abs(B).max())
+            ref = None
+            for name in kernels:
+                fn = calls[name]
+                with torch.cuda.stream(stream):
+                    dC.fill_(float("nan"))
+                    fn()
+                torch.cuda.synchronize()
+                if binding.t2s_device_status(stream.cuda_stream) != binding.T2S_OK:
+                    raise SystemExit("device status reports a timed-out wait (%s)" % name)
+                if name == "ffma":
+                    ref = dC.clone()
+                    check = "reference"
+                elif ref is None:
+                    check = "unchecked"
                 else:
-                    check = "within tolerance" if diff <= tol else "MISMATCH"
-                bad += check == "MISMATCH"
-            # Keep each point to about half a second of device time.
-            est = flops / (1e12 * (5.0 if name in ("naive", "smem32") else 30.0))
-            iters = max(3, min(args.iters, int(0.5 / max(est, 1e-6))))
-            med, mn, mean = _time(torch, fn, iters, stream, flush)
-            pt = rl.place(flops, med / 1e3, rl.gemm_bytes(M, N, K), peak, bw)
-            rec = {"shape": [M, N, K], "kernel": name, "iters": iters, "ms_median": med,
-                   "ms_min": mn, "ms_mean": mean, "tflops": pt["tflops"], "ai": pt["ai"],
-                   "roof_tflops": pt["roof_tflops"], "frac_of_roof": pt["frac_of_roof"],
-                   "region": pt["region"], "check": check, "l2_flush": flush is not None,
-                   "bw_gbs": bw, "bw_basis": bw_basis}
-            if name == "ffma":
-                rec["plan"] = binding.t2s_gemm_f32_plan(
-                    M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count)
-            line = json.dumps(rec)
-            print(line, flush=True)
-            if out:
-                out.write(line + "\n")
-            rows.append(rec)
-        del dA, dB, dC, dC_buf, ws
-        torch.cuda.empty_cache()
+                    diff = float((dC - ref).abs().max())
+                    exact = bool(torch.equal(dC.view(torch.int32), ref.view(torch.int32)))
+                    if name in ("naive", "smem32"):
+                        check = "bit-exact" if exact else "MISMATCH"
+                    elif exact:
+                        check = "bit-exact"
+                    else:
+                        check = "within tolerance" if diff <= tol else "MISMATCH"
+                    bad += check == "MISMATCH"
+                # Keep each point to about half a second of device time.
+                est = flops / (1e12 * (5.0 if name in ("naive", "smem32") else 30.0))
+                iters = max(3, min(args.iters, int(0.5 / max(est, 1e-6))))
+                med, mn, mean = _time(torch, fn, iters, stream, flush)
+                pt = rl.place(flops, med / 1e3, rl.gemm_bytes(M, N, K), peak, bw)
+                rec = {"shape": [M, N, K], "kernel": name, "iters": iters, "ms_median": med,
+                       "ms_min": mn, "ms_mean": mean, "tflops": pt["tflops"], "ai": pt["ai"],
+                       "roof_tflops": pt["roof_tflops"], "frac_of_roof": pt["frac_of_roof"],
+                       "region": pt["region"], "check": check, "l2_flush": flush is not None,
+                       "bw_gbs": bw, "bw_basis": bw_basis}
+                if name == "ffma":
+                    rec["plan"] = binding.t2s_gemm_f32_plan(
+                        M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count)
+                line = json.dumps(rec)
+                print(line, flush=True)
+                if out:
+                    out.write(line + "\n")
+                rows.append(rec)
+            del dA, dB, dC, dC_buf, ws
+            torch.cuda.empty_cache()
     if out:
         out.close()
     # Summary table: TFLOP/s (fraction of the roof) per shape and kernel.
@@ -210,6 +213,11 @@ def main(argv=None) -> int:
                  else "—" for k in kernels]
         print("| %dx%dx%d | %.1f | %.1f | %s |" % (M, N, K, first["ai"], first["roof_tflops"],
                                                    " | ".join(cells)))
+    c = clk.summary()
+    if c:
+        print("\nclocks during the sweep: median %.0f MHz (maximum %.0f), %d samples, throttle "
+              "reasons: %s" % (c["sm_mhz"], c["sm_max_mhz"], c["samples"],
+                               ", ".join(c["reasons"]) or "none"))
     return 1 if bad else 0
 
 

@@ -92,3 +92,27 @@ def test_profile_traffic_only_for_the_current_source(tmp_path):
     # A summary taken on another kernel's sources does not serve this one.
     assert bench.profile_traffic(str(good), "tf32x3") is None or \
         bench.kernel_hash("tf32x3") == current
+
+
+def test_clock_sampler_summary_from_samples(tmp_path):
+    """The clock record of the bench and the sweep: the median SM clock, the largest maximum,
+    the sample count and every throttle reason seen active in nvidia-smi's CSV rows (index,
+    clock, maximum clock, power, active mask, then the four reasons); malformed rows are
+    skipped, and no rows give no record."""
+    from roofline_driven_tiling_gb300.clocks import ClockSampler
+    rows = ["0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 2070, 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "garbage line",
+            "0, [N/A], 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    path = tmp_path / "clocks.csv"
+    path.write_text("\n".join(rows) + "\n")
+    clk = ClockSampler(0)
+    clk.path = str(path)
+    s = clk.summary()
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
+    assert not path.exists()  # the sample file is removed once read
+    empty = tmp_path / "empty.csv"
+    empty.write_text("")
+    clk.path = str(empty)
+    assert clk.summary() is None
